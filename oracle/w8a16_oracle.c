@@ -1,0 +1,297 @@
+/*
+ * CPU oracle for the W8A16 block-scaled GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the checker, not the product: only
+ * tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference leg
+ * may load or run it. It shares no code, header, table or constant with the
+ * CUDA library under fp8_weight_only_gemm_gb300/, and includes none of it.
+ *
+ * What it computes (source: "metrale_model_layers/layers/ops/
+ * w8a16_gemm_pipelined_m32.rs", doc comments of `w8a16_gemm_pipelined_m32_strided`
+ * (tensor layouts, strides in elements, first k of each A row read, first n of
+ * each C row written) and of `W8A16_M32_K_BLOCK` (one FP8 scale block per
+ * 128-K step)):
+ *
+ *   C[m][n] = bf16_rne( sum_{k<K} A[m][k] * ( e4m3(W[n][k]) * scale[n/128][k/128] ) )
+ *
+ * The sum runs in FP64 in plain k order and is rounded once to BF16 with
+ * round-to-nearest-even. Every term is exact in FP64: e4m3 x fp32 needs at most
+ * 4 + 24 significant bits and bf16 x that at most 8 + 28 = 36 < 53, so only the
+ * additions round; the result is the exact sum to within K ulps of FP64, far
+ * below one BF16 ulp. Columns n >= N and A columns k >= K are never touched.
+ *
+ * Readings where the page is silent (each one is also listed in the design
+ * notes): E4M3 is the OCP "FN" flavour (bias 7, no infinities, 0x7F/0xFF NaN,
+ * max +-448, subnormals m * 2^-9); the scale grid has ceil(N/128) rows, row n
+ * using scale row floor(n/128); NaN inputs propagate as in IEEE arithmetic.
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -pthread (no fast-math).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0 /* >0 only in the mutation tests, which plant one known mistake */
+#endif
+
+/* ---- E4M3 (FN) decode, from the format definition ------------------------
+ * 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits. Exponent field 0 is
+ * subnormal: (m/8) * 2^(1-7). Exponent 15 with mantissa 7 is NaN; there is no
+ * infinity, so exponent 15 with mantissa 0..6 is an ordinary normal number. */
+double oracle_e4m3_to_double(uint8_t code)
+{
+    const int sign = (code >> 7) & 1;
+    const int e = (code >> 3) & 0xF;
+    const int m = code & 0x7;
+    double mag;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9); /* m/8 * 2^-6 */
+    else
+#if ORACLE_MUTANT == 1
+        mag = ldexp(8.0 + m, e - 7 - 2); /* mutant: exponent bias off by one */
+#else
+        mag = ldexp(8.0 + m, e - 7 - 3); /* (1 + m/8) * 2^(e-7) */
+#endif
+    return sign ? -mag : mag;
+}
+
+/* ---- BF16 <-> FP64 -------------------------------------------------------
+ * BF16 is the upper half of an IEEE binary32: the value is that of the float
+ * whose upper 16 bits are the code and lower 16 bits are zero. */
+double oracle_bf16_to_double(uint16_t code)
+{
+    uint32_t u = (uint32_t)code << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to BF16 with round-to-nearest, ties to even, in one step
+ * (no intermediate binary32 rounding). BF16 keeps 8 significant bits, has
+ * binary32's exponent range (normal down to 2^-126) and subnormal quantum
+ * 2^-133. Results past the largest finite value become infinities. */
+uint16_t oracle_double_to_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    const int neg = signbit(x) ? 1 : 0;
+    const double a = fabs(x);
+    uint16_t mag;
+    if (a == 0.0) {
+        mag = 0;
+    } else if (isinf(a)) {
+        mag = 0x7F80;
+    } else {
+        int e;
+        (void)frexp(a, &e); /* a = f * 2^e with f in [0.5, 1): leading bit 2^(e-1) */
+        int q = (e - 1) - 7; /* weight of the last of 8 significant bits */
+        if (q < -133)
+            q = -133; /* subnormal range: fixed quantum */
+#if ORACLE_MUTANT == 2
+        const double r = floor(ldexp(a, -q)); /* mutant: truncation instead of RNE */
+#else
+        const double r = nearbyint(ldexp(a, -q)); /* default mode: ties to even */
+#endif
+        const double v = ldexp(r, q);
+        if (v >= 0x1p128) {
+            mag = 0x7F80;
+        } else {
+            const float f = (float)v; /* exact: v has <= 8 significant bits */
+            uint32_t u;
+            memcpy(&u, &f, sizeof u);
+            mag = (uint16_t)(u >> 16);
+        }
+    }
+    return (uint16_t)(mag | (neg ? 0x8000u : 0u));
+}
+
+/* ---- the GEMM -------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *A;
+    uint32_t a_row_stride;
+    const uint8_t *W;
+    const float *scale;
+    uint16_t *C;
+    uint32_t c_row_stride;
+    uint32_t M, N, K;
+    double *exact; /* optional [M*N] pre-rounding sums */
+    double *absum; /* optional [M*N] sums of |terms| (error-bound input) */
+    const uint32_t *sm, *sn; /* sampled mode: output indices */
+    uint16_t *sout;          /* sampled mode: [count] BF16 results */
+    uint64_t begin, end;     /* this thread's share */
+    const double *dec;       /* 256-entry E4M3 table */
+} oracle_job;
+
+/* One output element, exactly as the definition reads. */
+static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_out,
+                       double *abs_out)
+{
+    const uint32_t kb_count = j->K / 128;
+    const uint16_t *arow = j->A + (uint64_t)m * j->a_row_stride;
+    const uint8_t *wrow = j->W + (uint64_t)n * j->K;
+    const float *srow = j->scale + (uint64_t)(n / 128) * kb_count;
+    double sum = 0.0, asum = 0.0;
+    for (uint32_t k = 0; k < j->K; ++k) {
+#if ORACLE_MUTANT == 3
+        const double s = (double)srow[0]; /* mutant: first K block's scale everywhere */
+#elif ORACLE_MUTANT == 4
+        const double s = (double)j->scale[(uint64_t)(k / 128) * ((j->N + 127) / 128) + n / 128];
+        /* mutant: scale grid read transposed */
+#else
+        const double s = (double)srow[k / 128];
+#endif
+#if ORACLE_MUTANT == 5
+        const double w = j->dec[j->W[(uint64_t)k * j->N + n]]; /* mutant: W read as [K][N] */
+#else
+        const double w = j->dec[wrow[k]];
+#endif
+        const double a = oracle_bf16_to_double(arow[k]);
+#if ORACLE_MUTANT == 6
+        if (k == j->K - 1)
+            continue; /* mutant: last term dropped */
+#endif
+        const double t = a * (w * s);
+        sum += t;
+        asum += fabs(t);
+    }
+    *sum_out = sum;
+    *abs_out = asum;
+}
+
+static void *run_full(void *arg)
+{
+    const oracle_job *j = (const oracle_job *)arg;
+    for (uint64_t idx = j->begin; idx < j->end; ++idx) {
+        /* Outputs are handed out n-major so a thread reuses one W row across m. */
+        const uint32_t n = (uint32_t)(idx / j->M);
+        const uint32_t m = (uint32_t)(idx % j->M);
+        double sum, asum;
+        one_output(j, m, n, &sum, &asum);
+        j->C[(uint64_t)m * j->c_row_stride + n] = oracle_double_to_bf16_rne(sum);
+        if (j->exact)
+            j->exact[(uint64_t)m * j->N + n] = sum;
+        if (j->absum)
+            j->absum[(uint64_t)m * j->N + n] = asum;
+    }
+    return NULL;
+}
+
+static void *run_samples(void *arg)
+{
+    const oracle_job *j = (const oracle_job *)arg;
+    for (uint64_t i = j->begin; i < j->end; ++i) {
+        double sum, asum;
+        one_output(j, j->sm[i], j->sn[i], &sum, &asum);
+        j->sout[i] = oracle_double_to_bf16_rne(sum);
+        if (j->exact)
+            j->exact[i] = sum;
+        if (j->absum)
+            j->absum[i] = asum;
+    }
+    return NULL;
+}
+
+static int run_threads(oracle_job *base, uint64_t total, int nthreads, void *(*fn)(void *))
+{
+    double dec[256];
+    for (int c = 0; c < 256; ++c)
+        dec[c] = oracle_e4m3_to_double((uint8_t)c);
+    base->dec = dec;
+    if (nthreads < 1)
+        nthreads = 1;
+    if ((uint64_t)nthreads > total)
+        nthreads = total ? (int)total : 1;
+    oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *base;
+        jobs[t].begin = total * (uint64_t)t / (uint64_t)nthreads;
+        jobs[t].end = total * (uint64_t)(t + 1) / (uint64_t)nthreads;
+    }
+    char *joined = (char *)calloc((size_t)nthreads, 1);
+    if (!joined) {
+        free(jobs);
+        free(tids);
+        return -1;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, fn, &jobs[t]) == 0)
+            joined[t] = 1;
+        else
+            fn(&jobs[t]); /* no thread available: run the share inline */
+    }
+    fn(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (joined[t])
+            pthread_join(tids[t], NULL);
+    free(joined);
+    free(jobs);
+    free(tids);
+    return 0;
+}
+
+/* Full product. A: [M][a_row_stride] BF16 codes, W: [N][K] E4M3 codes,
+ * scale: [ceil(N/128)][K/128] FP32, C: [M][c_row_stride] BF16 codes (only the
+ * first N columns of each row are written). exact/absum may be NULL.
+ * Returns 0, or -1 on bad sizes / allocation failure. */
+int oracle_w8a16_gemm(const uint16_t *A, uint32_t a_row_stride, const uint8_t *W,
+                      const float *scale, uint16_t *C, uint32_t c_row_stride, uint32_t M,
+                      uint32_t N, uint32_t K, double *exact, double *absum, int nthreads)
+{
+    if (M == 0 || N == 0 || K == 0 || K % 128 != 0 || a_row_stride < K || c_row_stride < N)
+        return -1;
+    oracle_job j;
+    memset(&j, 0, sizeof j);
+    j.A = A;
+    j.a_row_stride = a_row_stride;
+    j.W = W;
+    j.scale = scale;
+    j.C = C;
+    j.c_row_stride = c_row_stride;
+    j.M = M;
+    j.N = N;
+    j.K = K;
+    j.exact = exact;
+    j.absum = absum;
+    return run_threads(&j, (uint64_t)M * N, nthreads, run_full);
+}
+
+/* Sampled product: out[i] = C[sm[i]][sn[i]] for i < count, with the same
+ * definition; exact/absum (optional) are [count]. */
+int oracle_w8a16_gemm_samples(const uint16_t *A, uint32_t a_row_stride, const uint8_t *W,
+                              const float *scale, uint32_t M, uint32_t N, uint32_t K,
+                              const uint32_t *sm, const uint32_t *sn, uint64_t count,
+                              uint16_t *out, double *exact, double *absum, int nthreads)
+{
+    if (M == 0 || N == 0 || K == 0 || K % 128 != 0 || a_row_stride < K)
+        return -1;
+    for (uint64_t i = 0; i < count; ++i)
+        if (sm[i] >= M || sn[i] >= N)
+            return -1;
+    oracle_job j;
+    memset(&j, 0, sizeof j);
+    j.A = A;
+    j.a_row_stride = a_row_stride;
+    j.W = W;
+    j.scale = scale;
+    j.M = M;
+    j.N = N;
+    j.K = K;
+    j.sm = sm;
+    j.sn = sn;
+    j.sout = out;
+    j.exact = exact;
+    j.absum = absum;
+    return run_threads(&j, count, nthreads, run_samples);
+}
