@@ -1,0 +1,14 @@
+"""GB300-native (sm_103a) W8A16 block-scaled GEMM.
+
+C[M, N] (BF16) = A[M, K] (BF16, any row pitch) x dequant(W[N, K] FP8 E4M3, one FP32
+scale per 128x128 block)^T, computed by hand-written tcgen05/TMA kernels in
+``libw8a16.so`` behind a C ABI (include/w8a16.h). This package is the thin
+Python binding: torch provides device memory and streams only.
+"""
+from .binding import (Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, W8A16Error, check_args,
+                      device_status, gemm, gemm_host, gemm_ptr, header_functions, last_error,
+                      load, plan_for, plan_variant, selftest_wait_timeout, strerror, version)
+
+__all__ = ["Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "W8A16Error", "check_args",
+           "device_status", "gemm", "gemm_host", "gemm_ptr", "header_functions", "last_error",
+           "load", "plan_for", "plan_variant", "selftest_wait_timeout", "strerror", "version"]

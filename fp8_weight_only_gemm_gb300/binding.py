@@ -1,0 +1,214 @@
+"""ctypes binding of libw8a16.so: argument marshalling only.
+
+Every step of the operation runs in the library's CUDA kernels; this module only
+turns torch tensors into pointers, pitches and a stream handle, and turns the
+library's error codes into exceptions. There is no fallback: if the library is
+not built or not loadable, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "_build" / "libw8a16.so"
+HEADER = PKG.parent / "include" / "w8a16.h"
+
+# Values mirrored from include/w8a16.h (checked against the header by the tests).
+W8A16_OK = 0
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC = 0, 1, 2
+STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int32), ("token_tile", ctypes.c_uint32),
+                ("split_k", ctypes.c_uint32), ("stages", ctypes.c_uint32),
+                ("ctas_per_sm", ctypes.c_uint32), ("grid", ctypes.c_uint32 * 3),
+                ("block", ctypes.c_uint32 * 3), ("cluster", ctypes.c_uint32 * 3),
+                ("smem_bytes", ctypes.c_uint32), ("tmem_cols", ctypes.c_uint32)]
+
+    def as_dict(self) -> dict:
+        return {"variant": self.variant, "token_tile": self.token_tile, "split_k": self.split_k,
+                "stages": self.stages, "ctas_per_sm": self.ctas_per_sm, "grid": list(self.grid),
+                "block": list(self.block), "cluster": list(self.cluster),
+                "smem_bytes": self.smem_bytes, "tmem_cols": self.tmem_cols}
+
+
+class W8A16Error(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"w8a16 error {code}: {message}")
+        self.code = code
+
+
+_VP, _U32, _I32, _INT = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int
+_SIGS = {
+    "w8a16_gemm": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _VP]),
+    "w8a16_gemm_contiguous": (_INT, [_VP, _VP, _VP, _VP, _U32, _U32, _U32, _VP]),
+    "w8a16_gemm_host": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP,
+                               _VP, _INT, _VP]),
+    "w8a16_check_args": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32]),
+    "w8a16_plan_for": (_INT, [_U32, _U32, _U32, _U32, _U32, ctypes.POINTER(Plan)]),
+    "w8a16_plan_variant": (_INT, [_U32, _U32, _U32, _I32, _U32, _U32, _U32, ctypes.POINTER(Plan)]),
+    "w8a16_gemm_with_plan": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32,
+                                    ctypes.POINTER(Plan), _VP]),
+    "w8a16_last_error": (ctypes.c_char_p, []),
+    "w8a16_strerror": (ctypes.c_char_p, [_INT]),
+    "w8a16_device_status": (_INT, [_VP, _INT, ctypes.POINTER(_U32), ctypes.POINTER(_U32),
+                                   ctypes.POINTER(_U32)]),
+    "w8a16_selftest_wait_timeout": (_INT, [_U32, _VP]),
+    "w8a16_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/w8a16.h declares."""
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"W8A16_API\s+(?:int|const char \*)\s*(w8a16_\w+)\s*\(", text)))
+
+
+def load(path: Path | str | None = None):
+    """Load the library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"{p} is missing: build it first (python -m fp8_weight_only_gemm_gb300.build "
+                           "or __graft_entry__.build()); there is no fallback path")
+    lib = ctypes.CDLL(str(p))
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load().w8a16_last_error().decode()
+
+
+def strerror(code: int) -> str:
+    return load().w8a16_strerror(code).decode()
+
+
+def _check(rc: int):
+    if rc != W8A16_OK:
+        raise W8A16Error(rc, last_error() or strerror(rc))
+
+
+def _stream_handle(stream) -> int | None:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# -------------------------------------------------------------- pure host --
+def check_args(M, N, K, a_row_stride, c_row_stride, A=0, W=0, scale=0, C=0) -> int:
+    return load().w8a16_check_args(A or None, a_row_stride, W or None, scale or None, C or None,
+                                   c_row_stride, M, N, K)
+
+
+def plan_for(M, N, K, sm_count=152, cluster_slots=0) -> dict:
+    p = Plan()
+    _check(load().w8a16_plan_for(M, N, K, sm_count, cluster_slots, ctypes.byref(p)))
+    return p.as_dict()
+
+
+def plan_variant(M, N, K, variant=VARIANT_TC, split_k=0, stages=0, sm_count=152) -> Plan:
+    p = Plan()
+    _check(load().w8a16_plan_variant(M, N, K, variant, split_k, stages, sm_count, ctypes.byref(p)))
+    return p
+
+
+# ----------------------------------------------------------- device calls --
+def _shapes(A, W, scale, C):
+    import torch
+    if A.dim() != 2 or W.dim() != 2:
+        raise ValueError("A and W must be 2-D")
+    if A.dtype != torch.bfloat16:
+        raise TypeError(f"A must be bfloat16, got {A.dtype}")
+    if W.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"W must be uint8 E4M3 codes or float8_e4m3fn, got {W.dtype}")
+    if scale.dtype != torch.float32:
+        raise TypeError(f"block_scale must be float32, got {scale.dtype}")
+    if A.stride(1) != 1 or (C is not None and C.stride(1) != 1):
+        raise ValueError("A and C rows must be contiguous (stride 1 along K / N)")
+    if not W.is_contiguous() or not scale.is_contiguous():
+        raise ValueError("W and block_scale must be contiguous")
+    M, K = A.shape
+    N, Kw = W.shape
+    if Kw != K:
+        raise ValueError(f"A has K={K} columns, W has {Kw}")
+    return M, N, K
+
+
+def gemm(A, W, scale, C=None, *, stream=None, plan: Plan | None = None):
+    """C[:, :N] = A @ dequant(W)^T on the GPU. A: bf16 [M, K] (any row pitch, rows
+    contiguous); W: uint8/float8_e4m3fn [N, K]; scale: fp32 [ceil(N/128), K/128];
+    C: optional bf16 [M, >=N] output view (allocated [M, N] if None)."""
+    import torch
+    M, N, K = _shapes(A, W, scale, C)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N:
+        raise ValueError("C must be bfloat16 [M, >=N]")
+    if not (A.is_cuda and W.is_cuda and scale.is_cuda and C.is_cuda):
+        raise ValueError("all tensors must be on a CUDA device")
+    lib = load()
+    args = (A.data_ptr(), A.stride(0), W.data_ptr(), scale.data_ptr(), C.data_ptr(), C.stride(0),
+            M, N, K)
+    with torch.cuda.device(A.device):
+        s = _stream_handle(stream)
+        if plan is None:
+            rc = lib.w8a16_gemm(*args, s)
+        else:
+            rc = lib.w8a16_gemm_with_plan(*args, ctypes.byref(plan), s)
+    _check(rc)
+    return C
+
+
+def gemm_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, stream=0,
+             plan: Plan | None = None) -> int:
+    """Raw-pointer call (returns the library's code; does not raise)."""
+    lib = load()
+    if plan is None:
+        return lib.w8a16_gemm(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K,
+                              stream or None)
+    return lib.w8a16_gemm_with_plan(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride,
+                                    M, N, K, ctypes.byref(plan), stream or None)
+
+
+def gemm_host(A_host, W_host, scale_host, C_host, dA, dW, dScale, dC, *, copy_weights=True,
+              stream=None):
+    """Host-buffer call: the library queues H2D copies, the GEMM and the D2H copy.
+    Host tensors should be pinned; device tensors have the same shapes/pitches."""
+    import torch
+    M, N, K = _shapes(A_host, W_host, scale_host, C_host)
+    with torch.cuda.device(dA.device):
+        rc = load().w8a16_gemm_host(
+            A_host.data_ptr(), A_host.stride(0), W_host.data_ptr(), scale_host.data_ptr(),
+            C_host.data_ptr(), C_host.stride(0), M, N, K, dA.data_ptr(), dW.data_ptr(),
+            dScale.data_ptr(), dC.data_ptr(), 1 if copy_weights else 0, _stream_handle(stream))
+    _check(rc)
+    return C_host
+
+
+def device_status(stream=None, clear=False) -> tuple[int, int, int]:
+    st, wh, de = ctypes.c_uint32(), ctypes.c_uint32(), ctypes.c_uint32()
+    _check(load().w8a16_device_status(_stream_handle(stream), 1 if clear else 0, ctypes.byref(st),
+                                      ctypes.byref(wh), ctypes.byref(de)))
+    return st.value, wh.value, de.value
+
+
+def selftest_wait_timeout(timeout_us: int, stream=None):
+    _check(load().w8a16_selftest_wait_timeout(timeout_us, _stream_handle(stream)))
+
+
+def version() -> str:
+    return load().w8a16_version().decode()

@@ -1,0 +1,434 @@
+// C ABI of libw8a16.so: argument checks, planning, dispatch, errors, status.
+//
+// The checks are those of the page "metrale_model_layers/layers/ops/
+// w8a16_gemm_pipelined_m32.rs" (the `ensure!` clauses of
+// `w8a16_gemm_pipelined_m32_strided`: m >= 1; K a positive multiple of 128; row
+// pitches covering K and N; a_row_stride a multiple of 8), in that order, each
+// with its own code and a message naming the values, followed by this library's
+// own (N >= 1, pointers, alignment, index ranges). All of them run before any
+// device work.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "w8a16_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int ok() {
+    g_last_error.clear();
+    return W8A16_OK;
+}
+
+std::string u(uint64_t v) { return std::to_string(v); }
+
+// Bounded-wait limit for the kernels: W8A16_WAIT_TIMEOUT_MS, read once.
+struct TimeoutSetting {
+    uint64_t ns = 2000ull * 1000 * 1000;
+    bool valid = true;
+    std::string raw;
+};
+
+const TimeoutSetting& timeout_setting() {
+    static TimeoutSetting t;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const char* v = std::getenv("W8A16_WAIT_TIMEOUT_MS");
+        if (v && *v) {
+            char* end = nullptr;
+            const unsigned long long ms = std::strtoull(v, &end, 10);
+            if (end && *end == '\0' && ms >= 1 && ms <= 600000ull) {
+                t.ns = ms * 1000ull * 1000ull;
+            } else {
+                t.valid = false;
+                t.raw = v;
+            }
+        }
+    });
+    return t;
+}
+
+struct DeviceInfo {
+    bool checked = false;
+    bool ok = false;
+    int sm_count = 0;
+    int major = 0, minor = 0;
+};
+
+int current_device_info(DeviceInfo* out, std::string* err) {
+    static std::mutex mu;
+    static DeviceInfo infos[64];
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        *err = std::string("no usable CUDA device: ") + cudaGetErrorString(e);
+        return W8A16_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = infos[dev];
+    if (!d.checked) {
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();
+        d.ok = (d.major == 10 && d.minor == 3);
+        d.checked = true;
+    }
+    *out = d;
+    if (!d.ok) {
+        *err = "device " + std::to_string(dev) + " is sm_" + std::to_string(d.major) +
+               std::to_string(d.minor) + "; this library is built for sm_103a (GB300) only";
+        return W8A16_ERR_DEVICE;
+    }
+    return W8A16_OK;
+}
+
+uint32_t ceil_div(uint32_t a, uint32_t b) { return (a + b - 1) / b; }
+
+uint32_t token_tile_for(uint32_t M) {
+    if (M <= 16) return 16;
+    if (M <= 32) return 32;
+    if (M <= 64) return 64;
+    return 128;
+}
+
+uint32_t default_stages(uint32_t tn) { return tn == 64 ? 3 : 4; }
+
+uint32_t tc_ctas_per_sm(uint32_t tn, uint32_t stages) {
+    const uint32_t smem = w8a16::tc_smem_bytes(tn, stages);
+    uint32_t by_smem = (232448u) / (smem + 1024u);            // 227 KiB usable per SM
+    uint32_t by_tmem = 512u / w8a16::tc_tmem_cols(tn);
+    uint32_t by_regs = tn <= 64 ? 2u : 1u;                    // launch bounds of the kernel
+    uint32_t c = by_smem < by_tmem ? by_smem : by_tmem;
+    return c < by_regs ? c : by_regs;
+}
+
+// Fill a TC plan for a given token tile, stage count and split.
+void fill_tc(uint32_t M, uint32_t N, uint32_t tn, uint32_t stages, uint32_t split,
+             w8a16_plan_t* p) {
+    std::memset(p, 0, sizeof *p);
+    p->variant = W8A16_VARIANT_TC;
+    p->token_tile = tn;
+    p->split_k = split;
+    p->stages = stages;
+    p->ctas_per_sm = tc_ctas_per_sm(tn, stages);
+    p->grid[0] = ceil_div(N, w8a16::kTcRows) * split;
+    p->grid[1] = ceil_div(M, tn);
+    p->grid[2] = 1;
+    p->block[0] = w8a16::kTcThreads;
+    p->block[1] = p->block[2] = 1;
+    p->cluster[0] = split;
+    p->cluster[1] = p->cluster[2] = 1;
+    p->smem_bytes = w8a16::tc_smem_bytes(tn, stages);
+    p->tmem_cols = w8a16::tc_tmem_cols(tn);
+}
+
+void fill_simt(uint32_t M, uint32_t N, w8a16_plan_t* p) {
+    std::memset(p, 0, sizeof *p);
+    p->variant = W8A16_VARIANT_SIMT;
+    p->token_tile = 8;
+    p->split_k = 1;
+    p->stages = 0;
+    p->ctas_per_sm = 8;
+    p->grid[0] = ceil_div(N, 8);
+    p->grid[1] = ceil_div(M, 8);
+    p->grid[2] = 1;
+    p->block[0] = 256;
+    p->block[1] = p->block[2] = 1;
+    p->cluster[0] = p->cluster[1] = p->cluster[2] = 1;
+}
+
+// Choose the split-K factor by a wave model: CTAs beyond the co-resident slots
+// form further waves; a CTA's time is its share of K steps plus a fixed ramp;
+// splitting adds a cluster reduction.
+uint32_t choose_split(uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps, uint32_t slots) {
+    const uint32_t max_split = ksteps < 16u ? ksteps : 16u;
+    double best = 1e300;
+    uint32_t best_s = 1;
+    for (uint32_t s = 1; s <= max_split; ++s) {
+        const uint64_t ctas = static_cast<uint64_t>(row_tiles) * token_tiles * s;
+        const uint64_t waves = (ctas + slots - 1) / slots;
+        const double steps = static_cast<double>((ksteps + s - 1) / s);
+        const double cost = static_cast<double>(waves) * (steps + 2.0) + (s > 1 ? 1.0 + 0.1 * s : 0.0);
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
+int check_sizes(uint32_t a_row_stride, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K) {
+    if (M < 1) return fail(W8A16_ERR_M_ZERO, "w8a16_gemm: m=0 has no rows to compute");
+    if (K < w8a16::kKStep || K % w8a16::kKStep != 0)
+        return fail(W8A16_ERR_K_BLOCK, "w8a16_gemm: K=" + u(K) +
+                                           " must be a positive multiple of 128 (one FP8 scale "
+                                           "block per K-step)");
+    if (a_row_stride < K || c_row_stride < N)
+        return fail(W8A16_ERR_PITCH, "w8a16_gemm: row pitches (a=" + u(a_row_stride) +
+                                         ", c=" + u(c_row_stride) + ") must cover the used extents (k=" +
+                                         u(K) + ", n=" + u(N) + ")");
+    if (a_row_stride % 8 != 0)
+        return fail(W8A16_ERR_A_PITCH_ALIGN, "w8a16_gemm: a_row_stride=" + u(a_row_stride) +
+                                                 " must keep rows 16B-aligned (multiple of 8)");
+    if (N < 1) return fail(W8A16_ERR_N_ZERO, "w8a16_gemm: n=0 has no columns to compute");
+    if (M > 0x7FFFFFFFu || N > 0x7FFFFFFFu || K > 0x7FFFFFFFu)
+        return fail(W8A16_ERR_RANGE, "w8a16_gemm: M, N and K must each be below 2^31 (M=" + u(M) +
+                                         ", N=" + u(N) + ", K=" + u(K) + ")");
+    if (ceil_div(M, 16) > 65535u * 8u)
+        return fail(W8A16_ERR_RANGE, "w8a16_gemm: M=" + u(M) + " needs more token tiles than grid.y allows");
+    return W8A16_OK;
+}
+
+int check_ptrs(const void* A, const void* W, const float* S, const void* C) {
+    if (!A || !W || !S || !C)
+        return fail(W8A16_ERR_NULL, std::string("w8a16_gemm: NULL ") +
+                                        (!A ? "A" : !W ? "W" : !S ? "block_scale" : "C") + " pointer");
+    const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(A) % 16 || addr(W) % 16 || addr(S) % 4 || addr(C) % 2)
+        return fail(W8A16_ERR_ALIGN,
+                    "w8a16_gemm: alignment (A and W need 16 bytes, block_scale 4, C 2); got A%16=" +
+                        u(addr(A) % 16) + " W%16=" + u(addr(W) % 16) + " scale%4=" + u(addr(S) % 4) +
+                        " C%2=" + u(addr(C) % 2));
+    return W8A16_OK;
+}
+
+int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
+    const uint32_t ksteps = K / w8a16::kKStep;
+    if (p.variant == W8A16_VARIANT_SIMT) {
+        if (p.grid[0] != ceil_div(N, 8) || p.grid[1] != ceil_div(M, 8) || p.block[0] != 256)
+            return fail(W8A16_ERR_PLAN, "SIMT plan does not match the shape");
+        return W8A16_OK;
+    }
+    if (p.variant != W8A16_VARIANT_TC)
+        return fail(W8A16_ERR_PLAN, "unknown variant " + std::to_string(p.variant));
+    if (!w8a16::tc_supported_stages(p.token_tile, p.stages))
+        return fail(W8A16_ERR_PLAN, "TC plan: token_tile=" + u(p.token_tile) + " stages=" +
+                                        u(p.stages) + " has no kernel instance");
+    if (p.split_k < 1 || p.split_k > 16 || p.split_k > ksteps)
+        return fail(W8A16_ERR_PLAN, "TC plan: split_k=" + u(p.split_k) +
+                                        " must be in 1..min(16, K/128=" + u(ksteps) + ")");
+    w8a16_plan_t ref;
+    fill_tc(M, N, p.token_tile, p.stages, p.split_k, &ref);
+    if (p.grid[0] != ref.grid[0] || p.grid[1] != ref.grid[1] || p.cluster[0] != ref.cluster[0])
+        return fail(W8A16_ERR_PLAN, "TC plan grid does not match the shape");
+    if (ref.grid[1] > 65535u) return fail(W8A16_ERR_RANGE, "TC plan: too many token tiles");
+    return W8A16_OK;
+}
+
+int plan_auto(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, uint32_t cluster_slots,
+              w8a16_plan_t* out) {
+    const uint32_t tn = token_tile_for(M);
+    const uint32_t stages = default_stages(tn);
+    const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows);
+    const uint32_t token_tiles = ceil_div(M, tn);
+    const uint32_t ksteps = K / w8a16::kKStep;
+    const uint32_t per_sm = tc_ctas_per_sm(tn, stages);
+    uint32_t slots = cluster_slots ? cluster_slots : (sm_count ? sm_count : 152u) * per_sm;
+    if (slots < 1) slots = 1;
+    const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, slots);
+    fill_tc(M, N, tn, stages, split, out);
+    return W8A16_OK;
+}
+
+int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, cudaStream_t stream) {
+    int rc = check_sizes(g.lda, g.ldc, g.M, g.N, g.K);
+    if (rc) return rc;
+    rc = check_ptrs(g.A, g.W, g.scale, g.C);
+    if (rc) return rc;
+    const TimeoutSetting& ts = timeout_setting();
+    if (!ts.valid)
+        return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
+                                       "' is not an integer number of milliseconds in 1..600000");
+    if (forced) {
+        rc = validate_plan(g.M, g.N, g.K, *forced);
+        if (rc) return rc;
+    }
+    DeviceInfo info;
+    std::string err;
+    rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    w8a16_plan_t plan;
+    if (forced)
+        plan = *forced;
+    else
+        plan_auto(g.M, g.N, g.K, static_cast<uint32_t>(info.sm_count), 0, &plan);
+    if (plan.variant == W8A16_VARIANT_SIMT)
+        rc = w8a16::launch_simt(g, plan, stream, &err);
+    else
+        rc = w8a16::launch_tc(g, plan, stream, ts.ns, &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int w8a16_check_args(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale,
+                     const void* C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K) {
+    int rc = check_sizes(a_row_stride, c_row_stride, M, N, K);
+    if (rc) return rc;
+    const auto misaligned = [](const void* p, uintptr_t a) {
+        return p != nullptr && reinterpret_cast<uintptr_t>(p) % a != 0;
+    };
+    if (misaligned(A, 16) || misaligned(W, 16) || misaligned(block_scale, 4) || misaligned(C, 2))
+        return fail(W8A16_ERR_ALIGN,
+                    "w8a16_gemm: alignment (A and W need 16 bytes, block_scale 4, C 2)");
+    return ok();
+}
+
+int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, uint32_t cluster_slots,
+                   w8a16_plan_t* out) {
+    if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_for: NULL plan pointer");
+    int rc = check_sizes(K, N, M, N, K);
+    if (rc) return rc;
+    plan_auto(M, N, K, sm_count, cluster_slots, out);
+    return ok();
+}
+
+int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint32_t split_k,
+                       uint32_t stages, uint32_t sm_count, w8a16_plan_t* out) {
+    if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_variant: NULL plan pointer");
+    int rc = check_sizes(K, N, M, N, K);
+    if (rc) return rc;
+    w8a16_plan_t p;
+    if (variant == W8A16_VARIANT_AUTO) {
+        plan_auto(M, N, K, sm_count, 0, &p);
+    } else if (variant == W8A16_VARIANT_SIMT) {
+        fill_simt(M, N, &p);
+    } else if (variant == W8A16_VARIANT_TC) {
+        w8a16_plan_t a;
+        plan_auto(M, N, K, sm_count, 0, &a);
+        const uint32_t tn = a.token_tile;
+        const uint32_t st = stages ? stages : a.stages;
+        const uint32_t sp = split_k ? split_k : a.split_k;
+        fill_tc(M, N, tn, st, sp, &p);
+    } else {
+        return fail(W8A16_ERR_PLAN, "w8a16_plan_variant: unknown variant " + std::to_string(variant));
+    }
+    rc = validate_plan(M, N, K, p);
+    if (rc) return rc;
+    *out = p;
+    return ok();
+}
+
+int w8a16_gemm(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale,
+               void* C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
+               w8a16_stream_t stream) {
+    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, nullptr,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w8a16_gemm_contiguous(const void* A, const void* W, const float* block_scale, void* C,
+                          uint32_t M, uint32_t N, uint32_t K, w8a16_stream_t stream) {
+    return w8a16_gemm(A, K, W, block_scale, C, N, M, N, K, stream);
+}
+
+int w8a16_gemm_with_plan(const void* A, uint32_t a_row_stride, const void* W,
+                         const float* block_scale, void* C, uint32_t c_row_stride, uint32_t M,
+                         uint32_t N, uint32_t K, const w8a16_plan_t* plan, w8a16_stream_t stream) {
+    if (!plan) return fail(W8A16_ERR_NULL, "w8a16_gemm_with_plan: NULL plan pointer");
+    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, plan,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w8a16_gemm_host(const void* A_host, uint32_t a_row_stride, const void* W_host,
+                    const float* scale_host, void* C_host, uint32_t c_row_stride, uint32_t M,
+                    uint32_t N, uint32_t K, void* dA, void* dW, float* dScale, void* dC,
+                    int copy_weights, w8a16_stream_t stream) {
+    int rc = check_sizes(a_row_stride, c_row_stride, M, N, K);
+    if (rc) return rc;
+    if (!A_host || !C_host || (copy_weights && (!W_host || !scale_host)))
+        return fail(W8A16_ERR_NULL, "w8a16_gemm_host: NULL host pointer");
+    rc = check_ptrs(dA, dW, dScale, dC);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t scale_bytes = static_cast<size_t>(ceil_div(N, 128)) * (K / 128) * sizeof(float);
+    cudaError_t e = cudaMemcpy2DAsync(dA, static_cast<size_t>(a_row_stride) * 2, A_host,
+                                      static_cast<size_t>(a_row_stride) * 2, static_cast<size_t>(K) * 2,
+                                      M, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && copy_weights)
+        e = cudaMemcpyAsync(dW, W_host, static_cast<size_t>(N) * K, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && copy_weights)
+        e = cudaMemcpyAsync(dScale, scale_host, scale_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(W8A16_ERR_COPY, std::string("w8a16_gemm_host: upload failed: ") + cudaGetErrorString(e));
+    }
+    rc = w8a16_gemm(dA, a_row_stride, dW, dScale, dC, c_row_stride, M, N, K, stream);
+    if (rc) return rc;
+    e = cudaMemcpy2DAsync(C_host, static_cast<size_t>(c_row_stride) * 2, dC,
+                          static_cast<size_t>(c_row_stride) * 2, static_cast<size_t>(N) * 2, M,
+                          cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(W8A16_ERR_COPY, std::string("w8a16_gemm_host: download failed: ") + cudaGetErrorString(e));
+    }
+    return ok();
+}
+
+const char* w8a16_last_error(void) { return g_last_error.c_str(); }
+
+const char* w8a16_strerror(int code) {
+    switch (code) {
+        case W8A16_OK: return "success";
+        case W8A16_ERR_M_ZERO: return "M is 0: no rows to compute";
+        case W8A16_ERR_K_BLOCK: return "K is not a positive multiple of 128";
+        case W8A16_ERR_PITCH: return "a row pitch is shorter than K (A) or N (C)";
+        case W8A16_ERR_A_PITCH_ALIGN: return "a_row_stride is not a multiple of 8";
+        case W8A16_ERR_N_ZERO: return "N is 0: no columns to compute";
+        case W8A16_ERR_NULL: return "a required pointer is NULL";
+        case W8A16_ERR_ALIGN: return "a pointer is not aligned (A, W: 16 B; block_scale: 4 B; C: 2 B)";
+        case W8A16_ERR_RANGE: return "a size is beyond what the kernels address";
+        case W8A16_ERR_DEVICE: return "no usable sm_103 CUDA device";
+        case W8A16_ERR_LAUNCH: return "the CUDA launch failed";
+        case W8A16_ERR_PLAN: return "the requested plan cannot run this shape";
+        case W8A16_ERR_COPY: return "a host/device copy could not be queued";
+        case W8A16_ERR_ARG: return "invalid argument";
+        default: return "unknown error code";
+    }
+}
+
+int w8a16_device_status(w8a16_stream_t stream, int clear, uint32_t* status, uint32_t* where,
+                        uint32_t* detail) {
+    w8a16::StatusWord w{0, 0, 0};
+    const cudaError_t e = w8a16::tc_status_read(&w, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(W8A16_ERR_DEVICE, std::string("w8a16_device_status: ") + cudaGetErrorString(e));
+    }
+    if (status) *status = w.code;
+    if (where) *where = w.where;
+    if (detail) *detail = w.detail;
+    return ok();
+}
+
+int w8a16_selftest_wait_timeout(uint32_t timeout_us, w8a16_stream_t stream) {
+    DeviceInfo info;
+    std::string err;
+    int rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    if (timeout_us < 1 || timeout_us > 10u * 1000u * 1000u)
+        return fail(W8A16_ERR_ARG, "w8a16_selftest_wait_timeout: timeout_us must be in 1..10^7");
+    rc = w8a16::launch_wait_selftest(static_cast<uint64_t>(timeout_us) * 1000ull,
+                                     reinterpret_cast<cudaStream_t>(stream), &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
+const char* w8a16_version(void) { return "w8a16 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+/*
+ * w8a16.h -- C ABI of the GB300 (sm_103a) W8A16 block-scaled GEMM library
+ * (libw8a16.so).
+ *
+ * The operation (page "metrale_model_layers/layers/ops/w8a16_gemm_pipelined_m32.rs",
+ * module doc and the doc comments of `w8a16_gemm_pipelined_m32_strided`,
+ * `W8A16_M32_K_BLOCK` and `w8a16_gemm_pipelined_by_m`):
+ *
+ *     C[m][n] = bf16( sum_k  A[m][k] * e4m3(W[n][k]) * block_scale[n/128][k/128] )
+ *
+ * for m < M, n < N, k < K, with
+ *   A            BF16, M rows of a_row_stride elements; the first K of each row are read;
+ *   W            FP8 E4M3 ("FN": bias 7, no infinities, 0x7F/0xFF NaN), N rows of K
+ *                bytes, row-major;
+ *   block_scale  FP32, ceil(N/128) rows of K/128 values: one scale per 128x128 block of W;
+ *   C            BF16, M rows of c_row_stride elements; the first N of each row are
+ *                written and nothing else is.
+ * Strides count elements, not bytes. Accumulation is FP32 on the tensor cores; the
+ * block scale is folded into the FP32 accumulator once per 128-K step and the
+ * result is rounded to BF16 (round-to-nearest-even). Each call is deterministic:
+ * the same arguments on the same plan give bit-identical outputs.
+ *
+ * Ownership and asynchrony. The caller owns every buffer and the stream; the
+ * library allocates nothing and keeps no per-call state besides a host-side
+ * cache of TMA descriptors. Device calls are asynchronous on `stream` (NULL is
+ * the legacy default stream), as the page's launchers are (`.launch(stream)`):
+ * the output is ready once the stream has reached the call. All checks run on
+ * the host before any device work; a failed check returns a negative W8A16_ERR_*
+ * code, touches no device memory, and leaves a message for w8a16_last_error().
+ *
+ * Device-side failure. Every wait inside the kernels is bounded (default 2 s,
+ * environment variable W8A16_WAIT_TIMEOUT_MS, read once). A wait that runs out
+ * makes the kernel record W8A16_STATUS_WAIT_TIMEOUT, release what it holds and
+ * return; w8a16_device_status() reports it. The CUDA context stays usable.
+ */
+#ifndef W8A16_H
+#define W8A16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define W8A16_API __attribute__((visibility("default")))
+#else
+#define W8A16_API
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *w8a16_stream_t;
+
+/* Return codes. The first four are the page's checks (doc comment and `ensure!`
+ * clauses of `w8a16_gemm_pipelined_m32_strided`); the rest are this library's. */
+enum {
+    W8A16_OK = 0,
+    W8A16_ERR_M_ZERO = -1,         /* M == 0: no rows to compute */
+    W8A16_ERR_K_BLOCK = -2,        /* K is not a positive multiple of 128 */
+    W8A16_ERR_PITCH = -3,          /* a_row_stride < K or c_row_stride < N */
+    W8A16_ERR_A_PITCH_ALIGN = -4,  /* a_row_stride % 8 != 0 (A rows must stay 16-byte aligned) */
+    W8A16_ERR_N_ZERO = -5,         /* N == 0 */
+    W8A16_ERR_NULL = -6,           /* a required pointer is NULL */
+    W8A16_ERR_ALIGN = -7,          /* A or W not 16-byte aligned, block_scale not 4-byte,
+                                      C not 2-byte aligned */
+    W8A16_ERR_RANGE = -8,          /* a size past what the kernels address (see w8a16_gemm) */
+    W8A16_ERR_DEVICE = -9,         /* no CUDA device, or the current device is not sm_103 */
+    W8A16_ERR_LAUNCH = -10,        /* the CUDA launch failed (message has the CUDA error) */
+    W8A16_ERR_PLAN = -11,          /* a requested plan is invalid for this shape */
+    W8A16_ERR_COPY = -12,          /* a host<->device copy could not be queued */
+    W8A16_ERR_ARG = -13            /* another invalid argument (message says which) */
+};
+
+/* Device status words (w8a16_device_status). */
+enum {
+    W8A16_STATUS_OK = 0,
+    W8A16_STATUS_WAIT_TIMEOUT = 1  /* a bounded in-kernel wait ran out; output undefined */
+};
+
+/* Kernel variants. */
+enum {
+    W8A16_VARIANT_AUTO = 0,  /* the planner's choice (w8a16_plan) */
+    W8A16_VARIANT_SIMT = 1,  /* CUDA-core kernel: one warp per weight row, no tensor cores */
+    W8A16_VARIANT_TC = 2     /* TMA weight ring + in-register E4M3->BF16 + tcgen05 MMA
+                                (weight rows = MMA M, tokens = MMA N), cluster split-K */
+};
+
+/*
+ * w8a16_gemm -- the operation above on the current CUDA device.
+ *
+ * A            device pointer, 16-byte aligned, BF16 [M][a_row_stride]
+ * a_row_stride elements between A rows; >= K and a multiple of 8
+ * W            device pointer, 16-byte aligned, E4M3 bytes [N][K]
+ * block_scale  device pointer, 4-byte aligned, FP32 [ceil(N/128)][K/128]
+ * C            device pointer, 2-byte aligned, BF16 [M][c_row_stride]; only columns < N
+ *              of the M rows are written
+ * c_row_stride elements between C rows; >= N, no alignment rule
+ * M, N, K      M >= 1, N >= 1, K a positive multiple of 128. Limits (W8A16_ERR_RANGE):
+ *              N, K, M < 2^31; a_row_stride * 2 and K are TMA strides below 2^40 bytes.
+ * stream       CUDA stream for the work
+ *
+ * Returns W8A16_OK once the work is queued, or a W8A16_ERR_* code (nothing queued).
+ * C may alias neither A, W nor block_scale.
+ */
+W8A16_API int w8a16_gemm(const void *A, uint32_t a_row_stride, const void *W, const float *block_scale,
+               void *C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
+               w8a16_stream_t stream);
+
+/* Contiguous form: a_row_stride = K, c_row_stride = N (the page's
+ * `w8a16_gemm_pipelined_m32`, which calls the strided launcher with pitches (k, n)). */
+W8A16_API int w8a16_gemm_contiguous(const void *A, const void *W, const float *block_scale, void *C,
+                          uint32_t M, uint32_t N, uint32_t K, w8a16_stream_t stream);
+
+/*
+ * w8a16_gemm_host -- the same operation on HOST buffers: queues on `stream` the
+ * host-to-device copies of A (M rows, full pitch), W and block_scale into the
+ * caller's device buffers dA, dW, dScale, the GEMM into dC, and the copy of dC
+ * (M rows, full pitch) back to C_host. Pinned host memory makes the copies
+ * asynchronous; pageable memory works but the copies then synchronise with the
+ * host. Pass copy_weights = 0 to skip the W and block_scale uploads when dW/dScale
+ * already hold them. Buffer rules and return codes are those of w8a16_gemm, plus
+ * W8A16_ERR_COPY when a copy cannot be queued. The output is in C_host once the
+ * stream has reached the call.
+ */
+W8A16_API int w8a16_gemm_host(const void *A_host, uint32_t a_row_stride, const void *W_host,
+                    const float *scale_host, void *C_host, uint32_t c_row_stride, uint32_t M,
+                    uint32_t N, uint32_t K, void *dA, void *dW, float *dScale, void *dC,
+                    int copy_weights, w8a16_stream_t stream);
+
+/* ---- planning (pure host code; no device work) -------------------------- */
+
+typedef struct {
+    int32_t variant;       /* W8A16_VARIANT_SIMT or W8A16_VARIANT_TC */
+    uint32_t token_tile;   /* tokens (rows of A/C) per CTA: the MMA N of the TC variant */
+    uint32_t split_k;      /* CTAs (one cluster) sharing a 128-row weight tile, each on a
+                              contiguous range of 128-K steps; 1 = no split */
+    uint32_t stages;       /* depth of the shared-memory ring (TC) */
+    uint32_t ctas_per_sm;  /* residency the plan assumes */
+    uint32_t grid[3];
+    uint32_t block[3];
+    uint32_t cluster[3];
+    uint32_t smem_bytes;   /* dynamic shared memory per CTA */
+    uint32_t tmem_cols;    /* tensor-memory columns per CTA (TC) */
+} w8a16_plan_t;
+
+/* The page's checks plus this library's (pointers may be NULL here: only sizes,
+ * pitches and the alignment of non-NULL pointers are checked). */
+W8A16_API int w8a16_check_args(const void *A, uint32_t a_row_stride, const void *W,
+                     const float *block_scale, const void *C, uint32_t c_row_stride, uint32_t M,
+                     uint32_t N, uint32_t K);
+
+/* The plan w8a16_gemm would use for (M, N, K) on a GPU with `sm_count` SMs of
+ * which `cluster_slots` CTAs can be co-resident in clusters (0 = assume sm_count). */
+W8A16_API int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
+                   uint32_t cluster_slots, w8a16_plan_t *out);
+
+/* Build the plan for an explicit variant / split / stage count (0 = planner's
+ * choice for that field). Returns W8A16_ERR_PLAN if it cannot run this shape. */
+W8A16_API int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint32_t split_k,
+                       uint32_t stages, uint32_t sm_count, w8a16_plan_t *out);
+
+/* w8a16_gemm with a plan from w8a16_plan_variant (for tests and tuning sweeps). */
+W8A16_API int w8a16_gemm_with_plan(const void *A, uint32_t a_row_stride, const void *W,
+                         const float *block_scale, void *C, uint32_t c_row_stride, uint32_t M,
+                         uint32_t N, uint32_t K, const w8a16_plan_t *plan,
+                         w8a16_stream_t stream);
+
+/* ---- errors and status -------------------------------------------------- */
+
+/* Message of the last failed call on this host thread ("" if none). */
+W8A16_API const char *w8a16_last_error(void);
+
+/* Fixed description of a W8A16_ERR_* code. */
+W8A16_API const char *w8a16_strerror(int code);
+
+/* Synchronises `stream`, then reports the first device-side failure recorded on the
+ * current device since the last clear: *status = W8A16_STATUS_*, *where =
+ * blockIdx.x | blockIdx.y << 16 of the failing CTA, *detail = which wait. Any
+ * pointer may be NULL. clear != 0 resets the record. Returns W8A16_OK or
+ * W8A16_ERR_DEVICE. */
+W8A16_API int w8a16_device_status(w8a16_stream_t stream, int clear, uint32_t *status, uint32_t *where,
+                        uint32_t *detail);
+
+/* Failure-path self-test: launches one CTA whose mbarrier wait can never complete
+ * (nothing arrives on it) with a limit of `timeout_us` microseconds, so the kernel
+ * must record W8A16_STATUS_WAIT_TIMEOUT and return. Used by the tests to show a
+ * wait that runs out leaves the context usable. */
+W8A16_API int w8a16_selftest_wait_timeout(uint32_t timeout_us, w8a16_stream_t stream);
+
+/* Library version string. */
+W8A16_API const char *w8a16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A16_H */

@@ -25,6 +25,7 @@ from __future__ import annotations
 import ctypes
 import hashlib
 import os
+import platform
 import subprocess
 from pathlib import Path
 
@@ -43,7 +44,7 @@ _f64p = ctypes.POINTER(ctypes.c_double)
 
 def _src_tag(mutant: int) -> str:
     h = hashlib.sha1(_SRC.read_bytes()).hexdigest()[:12]
-    return f"{h}_m{mutant}"
+    return f"{h}_{platform.machine()}_m{mutant}"
 
 
 def build(mutant: int = 0, outdir: Path | None = None) -> Path:

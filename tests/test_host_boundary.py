@@ -1,0 +1,143 @@
+"""Host-side tests of the C-ABI library (no GPU, no compute calls): it builds,
+loads, exports every function include/w8a16.h declares, applies the page's checks
+in the page's order with their own codes and messages, and plans launches."""
+from __future__ import annotations
+
+import ctypes
+import re
+
+import pytest
+
+from fp8_weight_only_gemm_gb300 import binding
+from fp8_weight_only_gemm_gb300.build import build_library
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return binding.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = binding.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/w8a16.h but not exported"
+    assert set(names) == set(binding._SIGS), "binding signatures out of sync with the header"
+
+
+def test_header_constants_match_binding():
+    text = binding.HEADER.read_text()
+    def val(name):
+        return int(re.search(rf"{name}\s*=\s*(-?\d+)", text).group(1))
+    assert val("W8A16_VARIANT_SIMT") == binding.VARIANT_SIMT
+    assert val("W8A16_VARIANT_TC") == binding.VARIANT_TC
+    assert val("W8A16_STATUS_WAIT_TIMEOUT") == binding.STATUS_WAIT_TIMEOUT
+
+
+ERR = dict(M_ZERO=-1, K_BLOCK=-2, PITCH=-3, A_PITCH_ALIGN=-4, N_ZERO=-5, NULL=-6, ALIGN=-7,
+           RANGE=-8, DEVICE=-9, PLAN=-11)
+
+
+@pytest.mark.parametrize("args,code,needle", [
+    # (M, N, K, lda, ldc)
+    ((0, 128, 128, 128, 128), ERR["M_ZERO"], "m=0"),
+    ((1, 128, 0, 128, 128), ERR["K_BLOCK"], "K=0"),
+    ((1, 128, 64, 128, 128), ERR["K_BLOCK"], "K=64"),
+    ((1, 128, 200, 256, 128), ERR["K_BLOCK"], "multiple of 128"),
+    ((1, 128, 256, 255, 128), ERR["PITCH"], "a=255"),
+    ((1, 128, 256, 256, 100), ERR["PITCH"], "c=100"),
+    ((1, 128, 256, 260, 128), ERR["A_PITCH_ALIGN"], "a_row_stride=260"),
+    ((1, 0, 256, 256, 0), ERR["N_ZERO"], "n=0"),
+    ((2 ** 31, 128, 128, 128, 128), ERR["RANGE"], "below 2^31"),
+])
+def test_checks_codes_and_messages(lib, args, code, needle):
+    M, N, K, lda, ldc = args
+    assert binding.check_args(M, N, K, lda, ldc) == code
+    assert needle in binding.last_error()
+
+
+def test_checks_run_in_the_pages_order(lib):
+    # m=0 reported before the K rule, K before pitches, pitches before alignment
+    assert binding.check_args(0, 128, 64, 3, 1) == ERR["M_ZERO"]
+    assert binding.check_args(1, 128, 64, 3, 1) == ERR["K_BLOCK"]
+    assert binding.check_args(1, 128, 128, 3, 1) == ERR["PITCH"]
+    assert binding.check_args(1, 128, 128, 132, 128) == ERR["A_PITCH_ALIGN"]
+    assert binding.check_args(1, 128, 128, 136, 128) == 0
+
+
+def test_alignment_and_null_checks_before_any_device_work(lib):
+    # the full entry point refuses before touching the device (there is none here)
+    rc = binding.gemm_ptr(0, 128, 0, 0, 0, 128, 1, 128, 128)
+    assert rc == ERR["NULL"] and "NULL A" in binding.last_error()
+    rc = binding.gemm_ptr(0x1008, 128, 0x2000, 0x3000, 0x4000, 128, 1, 128, 128)
+    assert rc == ERR["ALIGN"]
+    rc = binding.gemm_ptr(0x1000, 128, 0x2000, 0x3002, 0x4000, 128, 1, 128, 128)
+    assert rc == ERR["ALIGN"]
+    rc = binding.gemm_ptr(0x1000, 128, 0x2000, 0x3000, 0x4001, 128, 1, 128, 128)
+    assert rc == ERR["ALIGN"]
+    assert binding.check_args(1, 128, 128, 128, 128, A=0x1008) == ERR["ALIGN"]
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = binding.gemm_ptr(0x1000, 128, 0x2000, 0x3000, 0x4000, 128, 1, 128, 128)
+    assert rc == ERR["DEVICE"], binding.last_error()
+    assert binding.last_error()
+
+
+def test_strerror_covers_codes(lib):
+    for c in list(ERR.values()) + [0, -10, -12, -13]:
+        assert binding.strerror(c) and binding.strerror(c) != "unknown error code"
+    assert binding.strerror(-999) == "unknown error code"
+
+
+@pytest.mark.parametrize("M,N,K,tn", [(1, 256, 256, 16), (1, 4096, 4096, 16), (8, 12288, 4096, 16),
+                                      (32, 14336, 5120, 32), (128, 28672, 8192, 128),
+                                      (17, 1000, 1024, 32), (64, 512, 512, 64), (300, 512, 512, 128)])
+def test_plans_for_the_workloads(lib, M, N, K, tn):
+    p = binding.plan_for(M, N, K, sm_count=152)
+    assert p["variant"] == binding.VARIANT_TC
+    assert p["token_tile"] == tn
+    ksteps = K // 128
+    assert 1 <= p["split_k"] <= min(16, ksteps)
+    assert p["grid"][0] == -(-N // 128) * p["split_k"]
+    assert p["grid"][1] == -(-M // tn)
+    assert p["cluster"][0] == p["split_k"]
+    assert p["block"][0] == 320
+    assert p["tmem_cols"] * p["ctas_per_sm"] <= 512
+    assert p["smem_bytes"] * p["ctas_per_sm"] <= 232448
+
+
+def test_planner_fills_the_gpu_for_decode(lib):
+    # a 32-tile decode GEMV must split K so that most SMs get work
+    p = binding.plan_for(1, 4096, 4096, sm_count=152)
+    ctas = p["grid"][0] * p["grid"][1]
+    assert ctas >= 152
+    assert ctas <= 152 * p["ctas_per_sm"]
+
+
+def test_plan_variant_validation(lib):
+    p = binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=4, stages=6)
+    assert p.split_k == 4 and p.stages == 6 and p.grid[0] == 8 * 4
+    with pytest.raises(binding.W8A16Error) as e:
+        binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=9)   # > K/128 = 8
+    assert e.value.code == ERR["PLAN"]
+    with pytest.raises(binding.W8A16Error):
+        binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, stages=5)    # no instance
+    s = binding.plan_variant(8, 1024, 1024, binding.VARIANT_SIMT)
+    assert s.variant == binding.VARIANT_SIMT and s.grid[0] == 128
+    with pytest.raises(binding.W8A16Error):
+        binding.plan_variant(8, 1024, 1024, 7)
+
+
+def test_forced_plan_must_match_shape(lib):
+    p = binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=2)
+    rc = binding.gemm_ptr(0x1000, 1024, 0x2000, 0x3000, 0x4000, 2048, 8, 2048, 1024, plan=p)
+    assert rc == ERR["PLAN"]
+
+
+def test_version(lib):
+    assert "sm_103a" in binding.version()
