@@ -152,15 +152,16 @@ def bench_gpu(args, ws, rank, local):
     A0, W0, S0, C0 = (case.A.to(dev), case.W.to(dev), case.scale.to(dev), case.C0.to(dev))
     sets = [(A0.clone(), W0.clone(), S0.clone(), C0.clone()) for _ in range(nsets)]
     del A0, W0, S0, C0
-    plan = w8.plan_for(wl.M, wl.N, wl.K, props.multi_processor_count)
+    plan = w8.plan_current(wl.M, wl.N, wl.K)
     stream = torch.cuda.Stream(dev)
     lib = w8.load()
     sh = int(stream.cuda_stream)
+    flags = w8.FLAG_PDL if args.pdl == "on" else 0
 
-    def call(i):
+    def call(i, fl=None):
         A, W, S, C = sets[i % nsets]
-        rc = lib.w8a16_gemm(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
-                            C.stride(0), wl.M, wl.N, wl.K, sh)
+        rc = lib.w8a16_gemm_ex(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
+                               C.stride(0), wl.M, wl.N, wl.K, flags if fl is None else fl, sh)
         if rc != 0:
             raise RuntimeError(w8.last_error())
 
@@ -263,6 +264,9 @@ def bench_gpu(args, ws, rank, local):
                    "l2": f"inputs rotate over {nsets} buffer sets ({nsets * set_bytes / 1e6:.0f} MB, "
                          f">= 3x the {l2 / 1e6:.0f} MB L2): weights stream from HBM every step",
                    "graphs": f"steps replayed from CUDA graphs of {G} launches",
+                   "launch": ("programmatic dependent launch (W8A16_FLAG_PDL): each call's weight "
+                              "prefetch overlaps the previous call's tail" if flags else
+                              "plain stream order"),
                    "plan": plan, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "tflops": tflops,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
@@ -339,6 +343,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--pdl", choices=["on", "off"], default="on",
+                    help="queue the timed calls with W8A16_FLAG_PDL (weights are read-only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bounded CPU-oracle sample for cpu_baseline")
     args = ap.parse_args()

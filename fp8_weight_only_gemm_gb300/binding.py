@@ -17,6 +17,7 @@ HEADER = PKG.parent / "include" / "w8a16.h"
 
 # Values mirrored from include/w8a16.h (checked against the header by the tests).
 W8A16_OK = 0
+FLAG_PDL = 1
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC = 0, 1, 2
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
 
@@ -45,13 +46,16 @@ _VP, _U32, _I32, _INT = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes
 _SIGS = {
     "w8a16_gemm": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _VP]),
     "w8a16_gemm_contiguous": (_INT, [_VP, _VP, _VP, _VP, _U32, _U32, _U32, _VP]),
+    "w8a16_gemm_ex": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32, _VP]),
     "w8a16_gemm_host": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP,
                                _VP, _INT, _VP]),
     "w8a16_check_args": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32]),
-    "w8a16_plan_for": (_INT, [_U32, _U32, _U32, _U32, _U32, ctypes.POINTER(Plan)]),
+    "w8a16_plan_for": (_INT, [_U32, _U32, _U32, _U32, ctypes.POINTER(_U32), ctypes.POINTER(Plan)]),
+    "w8a16_plan_current": (_INT, [_U32, _U32, _U32, ctypes.POINTER(Plan)]),
+    "w8a16_cluster_capacity": (_INT, [_U32, _U32, ctypes.POINTER(_U32)]),
     "w8a16_plan_variant": (_INT, [_U32, _U32, _U32, _I32, _U32, _U32, _U32, ctypes.POINTER(Plan)]),
     "w8a16_gemm_with_plan": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32,
-                                    ctypes.POINTER(Plan), _VP]),
+                                    ctypes.POINTER(Plan), _U32, _VP]),
     "w8a16_last_error": (ctypes.c_char_p, []),
     "w8a16_strerror": (ctypes.c_char_p, [_INT]),
     "w8a16_device_status": (_INT, [_VP, _INT, ctypes.POINTER(_U32), ctypes.POINTER(_U32),
@@ -114,10 +118,28 @@ def check_args(M, N, K, a_row_stride, c_row_stride, A=0, W=0, scale=0, C=0) -> i
                                    c_row_stride, M, N, K)
 
 
-def plan_for(M, N, K, sm_count=152, cluster_slots=0) -> dict:
+def plan_for(M, N, K, sm_count=152, cluster_ctas=None) -> dict:
+    """Pure planner. cluster_ctas: optional 17-entry table (index = cluster size)
+    of co-resident CTAs, as cluster_capacity() reports for a device."""
     p = Plan()
-    _check(load().w8a16_plan_for(M, N, K, sm_count, cluster_slots, ctypes.byref(p)))
+    tab = None
+    if cluster_ctas is not None:
+        tab = (_U32 * 17)(*[int(x) for x in cluster_ctas])
+    _check(load().w8a16_plan_for(M, N, K, sm_count, tab, ctypes.byref(p)))
     return p.as_dict()
+
+
+def plan_current(M, N, K) -> dict:
+    """The plan w8a16_gemm uses on the current device."""
+    p = Plan()
+    _check(load().w8a16_plan_current(M, N, K, ctypes.byref(p)))
+    return p.as_dict()
+
+
+def cluster_capacity(token_tile, stages) -> list[int]:
+    out = (_U32 * 17)()
+    _check(load().w8a16_cluster_capacity(token_tile, stages, out))
+    return list(out)
 
 
 def plan_variant(M, N, K, variant=VARIANT_TC, split_k=0, stages=0, sm_count=152) -> Plan:
@@ -148,7 +170,7 @@ def _shapes(A, W, scale, C):
     return M, N, K
 
 
-def gemm(A, W, scale, C=None, *, stream=None, plan: Plan | None = None):
+def gemm(A, W, scale, C=None, *, stream=None, plan: Plan | None = None, flags: int = 0):
     """C[:, :N] = A @ dequant(W)^T on the GPU. A: bf16 [M, K] (any row pitch, rows
     contiguous); W: uint8/float8_e4m3fn [N, K]; scale: fp32 [ceil(N/128), K/128];
     C: optional bf16 [M, >=N] output view (allocated [M, N] if None)."""
@@ -166,22 +188,22 @@ def gemm(A, W, scale, C=None, *, stream=None, plan: Plan | None = None):
     with torch.cuda.device(A.device):
         s = _stream_handle(stream)
         if plan is None:
-            rc = lib.w8a16_gemm(*args, s)
+            rc = lib.w8a16_gemm_ex(*args, flags, s)
         else:
-            rc = lib.w8a16_gemm_with_plan(*args, ctypes.byref(plan), s)
+            rc = lib.w8a16_gemm_with_plan(*args, ctypes.byref(plan), flags, s)
     _check(rc)
     return C
 
 
 def gemm_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, stream=0,
-             plan: Plan | None = None) -> int:
+             plan: Plan | None = None, flags: int = 0) -> int:
     """Raw-pointer call (returns the library's code; does not raise)."""
     lib = load()
     if plan is None:
-        return lib.w8a16_gemm(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K,
-                              stream or None)
+        return lib.w8a16_gemm_ex(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N,
+                                 K, flags, stream or None)
     return lib.w8a16_gemm_with_plan(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride,
-                                    M, N, K, ctypes.byref(plan), stream or None)
+                                    M, N, K, ctypes.byref(plan), flags, stream or None)
 
 
 def gemm_host(A_host, W_host, scale_host, C_host, dA, dW, dScale, dC, *, copy_weights=True,

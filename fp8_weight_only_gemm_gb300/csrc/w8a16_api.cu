@@ -151,17 +151,22 @@ void fill_simt(uint32_t M, uint32_t N, w8a16_plan_t* p) {
 }
 
 // Choose the split-K factor by a wave model: CTAs beyond the co-resident slots
-// form further waves; a CTA's time is its share of K steps plus a fixed ramp;
-// splitting adds a cluster reduction.
-uint32_t choose_split(uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps, uint32_t slots) {
+// (for that cluster size) form further waves; a CTA's time is its share of K
+// steps plus a fixed start-up (ring fill, in step units); splitting adds a
+// cluster reduction. cap[s] = co-resident CTAs in clusters of s (0 = cannot run).
+uint32_t choose_split(uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
+                      const uint32_t* cap) {
     const uint32_t max_split = ksteps < 16u ? ksteps : 16u;
     double best = 1e300;
     uint32_t best_s = 1;
     for (uint32_t s = 1; s <= max_split; ++s) {
+        const uint32_t slots = cap[s];
+        if (slots == 0) continue;
         const uint64_t ctas = static_cast<uint64_t>(row_tiles) * token_tiles * s;
         const uint64_t waves = (ctas + slots - 1) / slots;
         const double steps = static_cast<double>((ksteps + s - 1) / s);
-        const double cost = static_cast<double>(waves) * (steps + 2.0) + (s > 1 ? 1.0 + 0.1 * s : 0.0);
+        const double cost =
+            static_cast<double>(waves) * (steps + 5.0) + (s > 1 ? 0.5 + 0.1 * s : 0.0);
         if (cost < best - 1e-9) {
             best = cost;
             best_s = s;
@@ -228,22 +233,70 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
     return W8A16_OK;
 }
 
-int plan_auto(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, uint32_t cluster_slots,
+void model_capacity(uint32_t sm_count, uint32_t per_sm, uint32_t* cap) {
+    cap[0] = 0;
+    for (uint32_t c = 1; c <= 16; ++c) cap[c] = ((sm_count ? sm_count : 152u) * per_sm / c) * c;
+}
+
+// Pure planner: token tile by M, stage count by token tile, split from the
+// wave model over `cap` (NULL: every cluster size fills every SM slot).
+int plan_core(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, const uint32_t* cap,
               w8a16_plan_t* out) {
     const uint32_t tn = token_tile_for(M);
     const uint32_t stages = default_stages(tn);
     const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows);
     const uint32_t token_tiles = ceil_div(M, tn);
     const uint32_t ksteps = K / w8a16::kKStep;
-    const uint32_t per_sm = tc_ctas_per_sm(tn, stages);
-    uint32_t slots = cluster_slots ? cluster_slots : (sm_count ? sm_count : 152u) * per_sm;
-    if (slots < 1) slots = 1;
-    const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, slots);
+    uint32_t model[17];
+    if (!cap) {
+        model_capacity(sm_count, tc_ctas_per_sm(tn, stages), model);
+        cap = model;
+    }
+    const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, cap);
     fill_tc(M, N, tn, stages, split, out);
     return W8A16_OK;
 }
 
-int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, cudaStream_t stream) {
+// Live capacity table of the current device for (tn, stages), cached.
+int live_capacity(uint32_t tn, uint32_t stages, uint32_t* cap, std::string* err) {
+    static std::mutex mu;
+    struct Entry { int dev; uint32_t tn, stages; uint32_t cap[17]; };
+    static Entry cache[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].dev == dev && cache[i].tn == tn && cache[i].stages == stages) {
+                std::memcpy(cap, cache[i].cap, sizeof(uint32_t) * 17);
+                return W8A16_OK;
+            }
+    }
+    Entry e{dev, tn, stages, {0}};
+    for (uint32_t c = 1; c <= 16; ++c) {
+        int rc = w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
+        if (rc) return rc;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (used < 64) cache[used++] = e;
+    std::memcpy(cap, e.cap, sizeof(uint32_t) * 17);
+    return W8A16_OK;
+}
+
+int plan_live(uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& info, w8a16_plan_t* out,
+              std::string* err) {
+    const uint32_t tn = token_tile_for(M);
+    uint32_t cap[17];
+    int rc = live_capacity(tn, default_stages(tn), cap, err);
+    if (rc) return rc;
+    return plan_core(M, N, K, static_cast<uint32_t>(info.sm_count), cap, out);
+}
+
+int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
+        cudaStream_t stream) {
+    if (flags & ~static_cast<uint32_t>(W8A16_FLAG_PDL))
+        return fail(W8A16_ERR_ARG, "w8a16_gemm: unknown flag bits " + u(flags));
     int rc = check_sizes(g.lda, g.ldc, g.M, g.N, g.K);
     if (rc) return rc;
     rc = check_ptrs(g.A, g.W, g.scale, g.C);
@@ -261,14 +314,16 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, cudaStream_t strea
     rc = current_device_info(&info, &err);
     if (rc) return fail(rc, err);
     w8a16_plan_t plan;
-    if (forced)
+    if (forced) {
         plan = *forced;
-    else
-        plan_auto(g.M, g.N, g.K, static_cast<uint32_t>(info.sm_count), 0, &plan);
+    } else {
+        rc = plan_live(g.M, g.N, g.K, info, &plan, &err);
+        if (rc) return fail(rc, err);
+    }
     if (plan.variant == W8A16_VARIANT_SIMT)
-        rc = w8a16::launch_simt(g, plan, stream, &err);
+        rc = w8a16::launch_simt(g, plan, stream, flags, &err);
     else
-        rc = w8a16::launch_tc(g, plan, stream, ts.ns, &err);
+        rc = w8a16::launch_tc(g, plan, stream, ts.ns, flags, &err);
     if (rc) return fail(rc, err);
     return ok();
 }
@@ -290,12 +345,39 @@ int w8a16_check_args(const void* A, uint32_t a_row_stride, const void* W, const 
     return ok();
 }
 
-int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, uint32_t cluster_slots,
-                   w8a16_plan_t* out) {
+int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
+                   const uint32_t* cluster_ctas, w8a16_plan_t* out) {
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_for: NULL plan pointer");
     int rc = check_sizes(K, N, M, N, K);
     if (rc) return rc;
-    plan_auto(M, N, K, sm_count, cluster_slots, out);
+    plan_core(M, N, K, sm_count, cluster_ctas, out);
+    return ok();
+}
+
+int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t* out) {
+    if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_current: NULL plan pointer");
+    int rc = check_sizes(K, N, M, N, K);
+    if (rc) return rc;
+    DeviceInfo info;
+    std::string err;
+    rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    rc = plan_live(M, N, K, info, out, &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
+int w8a16_cluster_capacity(uint32_t token_tile, uint32_t stages, uint32_t out[17]) {
+    if (!out) return fail(W8A16_ERR_NULL, "w8a16_cluster_capacity: NULL output");
+    if (!w8a16::tc_supported_stages(token_tile, stages))
+        return fail(W8A16_ERR_PLAN, "w8a16_cluster_capacity: no kernel instance for token_tile=" +
+                                        u(token_tile) + " stages=" + u(stages));
+    DeviceInfo info;
+    std::string err;
+    int rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    rc = live_capacity(token_tile, stages, out, &err);
+    if (rc) return fail(rc, err);
     return ok();
 }
 
@@ -306,12 +388,12 @@ int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint
     if (rc) return rc;
     w8a16_plan_t p;
     if (variant == W8A16_VARIANT_AUTO) {
-        plan_auto(M, N, K, sm_count, 0, &p);
+        plan_core(M, N, K, sm_count, nullptr, &p);
     } else if (variant == W8A16_VARIANT_SIMT) {
         fill_simt(M, N, &p);
     } else if (variant == W8A16_VARIANT_TC) {
         w8a16_plan_t a;
-        plan_auto(M, N, K, sm_count, 0, &a);
+        plan_core(M, N, K, sm_count, nullptr, &a);
         const uint32_t tn = a.token_tile;
         const uint32_t st = stages ? stages : a.stages;
         const uint32_t sp = split_k ? split_k : a.split_k;
@@ -328,7 +410,14 @@ int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint
 int w8a16_gemm(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale,
                void* C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
                w8a16_stream_t stream) {
-    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, nullptr,
+    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, nullptr, 0,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w8a16_gemm_ex(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale,
+                  void* C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
+                  uint32_t flags, w8a16_stream_t stream) {
+    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, nullptr, flags,
                reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -339,9 +428,10 @@ int w8a16_gemm_contiguous(const void* A, const void* W, const float* block_scale
 
 int w8a16_gemm_with_plan(const void* A, uint32_t a_row_stride, const void* W,
                          const float* block_scale, void* C, uint32_t c_row_stride, uint32_t M,
-                         uint32_t N, uint32_t K, const w8a16_plan_t* plan, w8a16_stream_t stream) {
+                         uint32_t N, uint32_t K, const w8a16_plan_t* plan, uint32_t flags,
+                         w8a16_stream_t stream) {
     if (!plan) return fail(W8A16_ERR_NULL, "w8a16_gemm_with_plan: NULL plan pointer");
-    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, plan,
+    return run({A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K}, plan, flags,
                reinterpret_cast<cudaStream_t>(stream));
 }
 

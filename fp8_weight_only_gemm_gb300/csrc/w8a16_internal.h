@@ -43,15 +43,19 @@ constexpr uint32_t tc_tmem_cols(uint32_t tn) {
 // Kernel launchers (implemented in the kernel translation units). They assume
 // the arguments and plan were validated; they return a W8A16_* code and, on
 // failure, a message in *err.
-int launch_simt(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, std::string* err);
+int launch_simt(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint32_t flags,
+                std::string* err);
 int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
-              std::string* err);
+              uint32_t flags, std::string* err);
+// CTAs of the TC instance (tn, stages) that can be co-resident on the current
+// device when launched in clusters of `cluster` CTAs.
+int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+                        std::string* err);
 int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, std::string* err);
 
 // Device status of the TC translation unit (the only one with waits).
 cudaError_t tc_status_read(StatusWord* out, bool clear, cudaStream_t s);
 
-// Host cache of TMA descriptors (implemented with the TC launcher).
 bool tc_supported_token_tile(uint32_t tn);
 bool tc_supported_stages(uint32_t tn, uint32_t stages);
 

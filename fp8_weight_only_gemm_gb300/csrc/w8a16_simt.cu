@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "w8a16_internal.h"
 
 namespace w8a16 {
@@ -49,6 +51,10 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
                       uint32_t K) {
     __shared__ float lut[256];
     for (uint32_t i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = e4m3_value(i);
+    // Under a programmatic launch, wait for the previous grid before touching
+    // memory it may write (a no-op otherwise), and let the next one be scheduled.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,20 +109,27 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
 
 }  // namespace
 
-int launch_simt(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, std::string* err) {
-    dim3 grid(p.grid[0], p.grid[1], 1), block(p.block[0], 1, 1);
-    w8a16_simt_kernel<<<grid, block, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(g.A), g.lda, static_cast<const uint8_t*>(g.W), g.scale,
-        static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K);
-    const cudaError_t e = cudaGetLastError();
+int launch_simt(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint32_t flags,
+                std::string* err) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
+    cfg.blockDim = dim3(p.block[0], 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, w8a16_simt_kernel, static_cast<const __nv_bfloat16*>(g.A),
+                                       g.lda, static_cast<const uint8_t*>(g.W), g.scale,
+                                       static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K);
     if (e != cudaSuccess) {
+        cudaGetLastError();
         *err = std::string("SIMT kernel launch failed: ") + cudaGetErrorString(e);
         return W8A16_ERR_LAUNCH;
     }
     return W8A16_OK;
 }
-
-uint32_t simt_rows_per_cta() { return kSimtWarps; }
-uint32_t simt_tokens_per_cta() { return kSimtTokens; }
 
 }  // namespace w8a16

@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Dependents may be scheduled from here on: this CTA holds its TMEM already.
+    if (threadIdx.x == 0) grid_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const uint32_t tA = tmem_base;                    // 2 x 64 columns: BF16 weight tiles
     const uint32_t tP = tmem_base + 2 * kABufCols;    // 2 x TN columns: FP32 step products
@@ -180,11 +182,29 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();   // W is streamed once
             const uint64_t pol_a = l2_policy_evict_last();    // A is re-read by every tile
-            uint32_t issued = 0;
-            for (uint32_t i = 0; i < nsteps; ++i) {
+            // The first ring's weight tiles are requested before waiting on the
+            // previous grid in the stream (under a programmatic launch the caller
+            // guarantees that grid does not write W); A is only read after the
+            // wait. Without a programmatic launch the wait returns at once.
+            const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
+            for (uint32_t i = 0; i < npre; ++i) {
+                mbar_arrive_expect_tx(full_bar(i), Cfg::kStageBytes);
+                tma_load_2d(smem_u32(sW + i * kWTileBytes), &tmW, full_bar(i),
+                            static_cast<int32_t>((s_begin + i) * kKStep),
+                            static_cast<int32_t>(tile * kTcRows), pol_w);
+            }
+            grid_dependency_wait();
+            for (uint32_t i = 0; i < npre; ++i) {
+                const int32_t k = static_cast<int32_t>((s_begin + i) * kKStep);
+                const uint32_t a_dst = smem_u32(sA + i * Cfg::kActBytes);
+                tma_load_2d(a_dst, &tmA, full_bar(i), k, static_cast<int32_t>(token0), pol_a);
+                tma_load_2d(a_dst + TN * 128, &tmA, full_bar(i), k + 64,
+                            static_cast<int32_t>(token0), pol_a);
+            }
+            uint32_t issued = npre;
+            for (uint32_t i = npre; i < nsteps; ++i) {
                 const uint32_t s = i % STAGES, round = i / STAGES;
-                if (round > 0 &&
-                    !mbar_wait(empty_bar(s), (round - 1) & 1, deadline, abort_flag, &g_tc_status,
+                if (!mbar_wait(empty_bar(s), (round - 1) & 1, deadline, abort_flag, &g_tc_status,
                                kWaitEmpty))
                     break;
                 mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
@@ -434,52 +454,47 @@ bool get_map(const MapKey& key, int device, CUtensorMap* out, std::string* err) 
     return true;
 }
 
-template <uint32_t TN, uint32_t STAGES>
-int launch_tc_t(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
-                std::string* err) {
-    auto kern = w8a16_tc_kernel<TN, STAGES>;
-    const uint32_t smem = tc_smem_bytes(TN, STAGES);
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    });
-    if (attr_err != cudaSuccess) {
-        *err = std::string("TC kernel attribute setup failed: ") + cudaGetErrorString(attr_err);
-        return W8A16_ERR_LAUNCH;
-    }
-    int dev = 0;
-    cudaGetDevice(&dev);
-    CUtensorMap mw, ma;
-    if (!get_map({reinterpret_cast<uint64_t>(g.W), g.N, g.K, g.K, kTcRows, 0}, dev, &mw, err) ||
-        !get_map({reinterpret_cast<uint64_t>(g.A), g.M, g.K, static_cast<uint64_t>(g.lda) * 2, TN, 1},
-                 dev, &ma, err))
-        return W8A16_ERR_LAUNCH;
+using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*, uint32_t,
+                           uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.split_k;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, kern, mw, ma, g.scale, static_cast<__nv_bfloat16*>(g.C), g.ldc,
-                           g.M, g.N, g.K, p.split_k, timeout_ns);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        *err = std::string("TC kernel launch failed: ") + cudaGetErrorString(e);
-        return W8A16_ERR_LAUNCH;
-    }
-    return W8A16_OK;
+struct TcInstance {
+    uint32_t tn, stages;
+    TcKernelFn fn;
+};
+
+#define W8A16_TC_INST(TN_, ST_) {TN_, ST_, &w8a16_tc_kernel<TN_, ST_>}
+const TcInstance kTcInstances[] = {
+    W8A16_TC_INST(16, 4), W8A16_TC_INST(16, 6), W8A16_TC_INST(16, 8),
+    W8A16_TC_INST(32, 4), W8A16_TC_INST(32, 6), W8A16_TC_INST(32, 8),
+    W8A16_TC_INST(64, 3), W8A16_TC_INST(64, 4), W8A16_TC_INST(64, 6),
+    W8A16_TC_INST(128, 4),
+};
+#undef W8A16_TC_INST
+constexpr int kNumTcInstances = sizeof(kTcInstances) / sizeof(kTcInstances[0]);
+
+int find_instance(uint32_t tn, uint32_t stages) {
+    for (int i = 0; i < kNumTcInstances; ++i)
+        if (kTcInstances[i].tn == tn && kTcInstances[i].stages == stages) return i;
+    return -1;
+}
+
+// Function attributes (dynamic shared memory above 48 KiB, cluster sizes above
+// 8) are per device: set once per (device, instance).
+cudaError_t ensure_attributes(int inst, int device) {
+    static std::mutex mu;
+    static bool done[64][kNumTcInstances] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (done[device][inst]) return cudaSuccess;
+    const TcInstance& k = kTcInstances[inst];
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(tc_smem_bytes(k.tn, k.stages)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) done[device][inst] = true;
+    return e;
 }
 
 }  // namespace
@@ -488,26 +503,90 @@ bool tc_supported_token_tile(uint32_t tn) {
     return tn == 16 || tn == 32 || tn == 64 || tn == 128;
 }
 
-bool tc_supported_stages(uint32_t tn, uint32_t stages) {
-    if (!tc_supported_token_tile(tn)) return false;
-    if (tn == 128) return stages == 4;
-    if (tn == 64) return stages == 3 || stages == 4 || stages == 6;
-    return stages == 4 || stages == 6 || stages == 8;
-}
+bool tc_supported_stages(uint32_t tn, uint32_t stages) { return find_instance(tn, stages) >= 0; }
 
 int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
-              std::string* err) {
-    const uint32_t tn = p.token_tile, st = p.stages;
-#define W8A16_TC_CASE(TN_, ST_) \
-    if (tn == TN_ && st == ST_) return launch_tc_t<TN_, ST_>(g, p, s, timeout_ns, err);
-    W8A16_TC_CASE(16, 4) W8A16_TC_CASE(16, 6) W8A16_TC_CASE(16, 8)
-    W8A16_TC_CASE(32, 4) W8A16_TC_CASE(32, 6) W8A16_TC_CASE(32, 8)
-    W8A16_TC_CASE(64, 3) W8A16_TC_CASE(64, 4) W8A16_TC_CASE(64, 6)
-    W8A16_TC_CASE(128, 4)
-#undef W8A16_TC_CASE
-    *err = "no TC kernel instance for token_tile=" + std::to_string(tn) +
-           " stages=" + std::to_string(st);
-    return W8A16_ERR_PLAN;
+              uint32_t flags, std::string* err) {
+    const int inst = find_instance(p.token_tile, p.stages);
+    if (inst < 0) {
+        *err = "no TC kernel instance for token_tile=" + std::to_string(p.token_tile) +
+               " stages=" + std::to_string(p.stages);
+        return W8A16_ERR_PLAN;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = ensure_attributes(inst, dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("TC kernel attribute setup failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    CUtensorMap mw, ma;
+    if (!get_map({reinterpret_cast<uint64_t>(g.W), g.N, g.K, g.K, kTcRows, 0}, dev, &mw, err) ||
+        !get_map({reinterpret_cast<uint64_t>(g.A), g.M, g.K, static_cast<uint64_t>(g.lda) * 2,
+                  p.token_tile, 1},
+                 dev, &ma, err))
+        return W8A16_ERR_LAUNCH;
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = tc_smem_bytes(p.token_tile, p.stages);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.split_k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kTcInstances[inst].fn, mw, ma, g.scale,
+                           static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, p.split_k,
+                           timeout_ns);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("TC kernel launch failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    return W8A16_OK;
+}
+
+int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+                        std::string* err) {
+    const int inst = find_instance(tn, stages);
+    if (inst < 0 || cluster < 1 || cluster > 16) {
+        *err = "no TC kernel instance, or cluster size outside 1..16";
+        return W8A16_ERR_PLAN;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = ensure_attributes(inst, dev);
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(cluster * 64, 1, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = tc_smem_bytes(tn, stages);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kTcInstances[inst].fn),
+                                           &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("cudaOccupancyMaxActiveClusters failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_DEVICE;
+    }
+    *ctas = static_cast<uint32_t>(n) * cluster;
+    return W8A16_OK;
 }
 
 int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, std::string* err) {

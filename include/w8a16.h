@@ -77,6 +77,17 @@ enum {
     W8A16_STATUS_WAIT_TIMEOUT = 1  /* a bounded in-kernel wait ran out; output undefined */
 };
 
+/* Call flags (w8a16_gemm_ex). */
+enum {
+    /* Programmatic dependent launch: the kernel may start while the work queued
+     * before it on the stream is still running, and streams its first weight
+     * tiles before waiting for that work to finish; A, block_scale and C are only
+     * touched after the wait. Consecutive calls then overlap one call's start-up
+     * with the previous call's tail. Contract: no work queued earlier on the
+     * stream may write W (weights are read-only in inference). */
+    W8A16_FLAG_PDL = 1u
+};
+
 /* Kernel variants. */
 enum {
     W8A16_VARIANT_AUTO = 0,  /* the planner's choice (w8a16_plan) */
@@ -110,6 +121,11 @@ W8A16_API int w8a16_gemm(const void *A, uint32_t a_row_stride, const void *W, co
  * `w8a16_gemm_pipelined_m32`, which calls the strided launcher with pitches (k, n)). */
 W8A16_API int w8a16_gemm_contiguous(const void *A, const void *W, const float *block_scale, void *C,
                           uint32_t M, uint32_t N, uint32_t K, w8a16_stream_t stream);
+
+/* w8a16_gemm with call flags (W8A16_FLAG_*; 0 = the same as w8a16_gemm). */
+W8A16_API int w8a16_gemm_ex(const void *A, uint32_t a_row_stride, const void *W,
+                            const float *block_scale, void *C, uint32_t c_row_stride, uint32_t M,
+                            uint32_t N, uint32_t K, uint32_t flags, w8a16_stream_t stream);
 
 /*
  * w8a16_gemm_host -- the same operation on HOST buffers: queues on `stream` the
@@ -149,21 +165,31 @@ W8A16_API int w8a16_check_args(const void *A, uint32_t a_row_stride, const void 
                      const float *block_scale, const void *C, uint32_t c_row_stride, uint32_t M,
                      uint32_t N, uint32_t K);
 
-/* The plan w8a16_gemm would use for (M, N, K) on a GPU with `sm_count` SMs of
- * which `cluster_slots` CTAs can be co-resident in clusters (0 = assume sm_count). */
+/* The plan for (M, N, K) on a GPU with `sm_count` SMs (pure: no device work).
+ * cluster_ctas, if not NULL, has 17 entries: cluster_ctas[s] = how many CTAs of
+ * the plan's kernel can be co-resident when launched in clusters of s CTAs
+ * (s = 1..16; 0 = that cluster size cannot run), as w8a16_cluster_capacity
+ * reports; NULL assumes every size fills every SM slot. */
 W8A16_API int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
-                   uint32_t cluster_slots, w8a16_plan_t *out);
+                             const uint32_t *cluster_ctas, w8a16_plan_t *out);
+
+/* The plan w8a16_gemm uses for (M, N, K) on the current device. */
+W8A16_API int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t *out);
+
+/* Co-resident CTAs of the TC kernel for a token tile and stage count on the
+ * current device, per cluster size: out[s] for s = 1..16 (out[0] = 0). */
+W8A16_API int w8a16_cluster_capacity(uint32_t token_tile, uint32_t stages, uint32_t out[17]);
 
 /* Build the plan for an explicit variant / split / stage count (0 = planner's
  * choice for that field). Returns W8A16_ERR_PLAN if it cannot run this shape. */
 W8A16_API int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint32_t split_k,
                        uint32_t stages, uint32_t sm_count, w8a16_plan_t *out);
 
-/* w8a16_gemm with a plan from w8a16_plan_variant (for tests and tuning sweeps). */
+/* w8a16_gemm_ex with a plan from w8a16_plan_variant (for tests and tuning sweeps). */
 W8A16_API int w8a16_gemm_with_plan(const void *A, uint32_t a_row_stride, const void *W,
-                         const float *block_scale, void *C, uint32_t c_row_stride, uint32_t M,
-                         uint32_t N, uint32_t K, const w8a16_plan_t *plan,
-                         w8a16_stream_t stream);
+                                   const float *block_scale, void *C, uint32_t c_row_stride,
+                                   uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t *plan,
+                                   uint32_t flags, w8a16_stream_t stream);
 
 /* ---- errors and status -------------------------------------------------- */
 

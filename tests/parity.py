@@ -28,7 +28,7 @@ def bf16_to_f64(codes: np.ndarray) -> np.ndarray:
 
 
 def ulp_bf16(x: np.ndarray) -> np.ndarray:
-    a = np.abs(x)
+    a = np.nan_to_num(np.abs(x), nan=1.0, posinf=1.0)
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
     return np.ldexp(1.0, (e - 7).astype(np.int64))
 

@@ -162,3 +162,38 @@ def test_bounded_wait_times_out_and_context_survives():
     ref, exact, absum = oracle_full(case)
     compare(case, got, ref, exact, absum, label="after-timeout")
     assert binding.device_status()[0] == 0
+
+
+def test_programmatic_launch_chain_is_ordered():
+    """Four dependent calls (each call's A is the previous call's C, N = K) queued
+    with the programmatic-launch flag give the same bits as without it, and the
+    first link matches the oracle."""
+    import fp8_weight_only_gemm_gb300 as w8
+    K = 1024
+    cases = [workloads.make_case("decode_gemv_m1_n4096_k4096", M=8, N=K, K=K, seed=300 + i)
+             for i in range(4)]
+    Ws = [c.W.cuda() for c in cases]
+    Ss = [c.scale.cuda() for c in cases]
+    x0 = cases[0].A.cuda()
+
+    def chain(flags):
+        x = x0
+        for W, S in zip(Ws, Ss):
+            x = w8.gemm(x, W, S, flags=flags)
+        torch.cuda.synchronize()
+        return x.view(torch.int16).cpu().numpy()
+
+    ref_bits = chain(0)
+    for _ in range(3):
+        assert np.array_equal(chain(w8.FLAG_PDL), ref_bits)
+    first = run_gpu(cases[0])
+    ref, exact, absum = oracle_full(cases[0])
+    compare(cases[0], first, ref, exact, absum, split_k=16, label="pdl-chain-first")
+
+
+def test_live_plan_and_capacity():
+    import fp8_weight_only_gemm_gb300 as w8
+    cap = w8.cluster_capacity(16, 4)
+    assert cap[0] == 0 and cap[1] >= torch.cuda.get_device_properties(0).multi_processor_count
+    p = w8.plan_current(1, 4096, 4096)
+    assert p["grid"][0] * p["grid"][1] <= cap[p["split_k"]], (p, cap)

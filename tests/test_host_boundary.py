@@ -33,6 +33,7 @@ def test_header_constants_match_binding():
     assert val("W8A16_VARIANT_SIMT") == binding.VARIANT_SIMT
     assert val("W8A16_VARIANT_TC") == binding.VARIANT_TC
     assert val("W8A16_STATUS_WAIT_TIMEOUT") == binding.STATUS_WAIT_TIMEOUT
+    assert int(re.search(r"W8A16_FLAG_PDL\s*=\s*(\d+)u", text).group(1)) == binding.FLAG_PDL
 
 
 ERR = dict(M_ZERO=-1, K_BLOCK=-2, PITCH=-3, A_PITCH_ALIGN=-4, N_ZERO=-5, NULL=-6, ALIGN=-7,
@@ -117,6 +118,20 @@ def test_planner_fills_the_gpu_for_decode(lib):
     ctas = p["grid"][0] * p["grid"][1]
     assert ctas >= 152
     assert ctas <= 152 * p["ctas_per_sm"]
+
+
+def test_planner_uses_cluster_capacity(lib):
+    # A device where clusters of 8 only fit 15 at a time (120 CTAs) while 4-CTA
+    # clusters fill 2 CTAs per SM: the 32-tile decode GEMV must not be split 8
+    # ways (three waves of clusters); it picks a split whose clusters fit at once.
+    cap = [0] + [304] * 4 + [300, 300, 294, 120] + [0] * 8
+    p = binding.plan_for(1, 4096, 4096, sm_count=152, cluster_ctas=cap)
+    s = p["split_k"]
+    assert 32 * s <= cap[s], p
+    assert s >= 4
+    # a cluster size the device cannot run is never chosen
+    cap2 = [0, 304, 0, 0, 0, 0, 0, 0, 0] + [0] * 8
+    assert binding.plan_for(1, 4096, 4096, sm_count=152, cluster_ctas=cap2)["split_k"] == 1
 
 
 def test_plan_variant_validation(lib):
