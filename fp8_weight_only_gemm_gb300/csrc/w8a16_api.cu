@@ -104,13 +104,16 @@ uint32_t token_tile_for(uint32_t M) {
     return 128;
 }
 
-uint32_t default_stages(uint32_t tn) { return tn == 64 ? 3 : 4; }
+uint32_t default_stages(uint32_t tn) { return tn == 16 ? 8 : tn == 32 ? 6 : tn == 64 ? 6 : 4; }
 
-uint32_t tc_ctas_per_sm(uint32_t tn, uint32_t stages) {
-    const uint32_t smem = w8a16::tc_smem_bytes(tn, stages);
-    uint32_t by_smem = (232448u) / (smem + 1024u);            // 227 KiB usable per SM
+// CTAs of one TC plan that fit on an SM: shared memory (228 KiB per SM, 1 KiB
+// reserved per CTA), TMEM (512 columns), and registers (the kernel's launch
+// bounds allow 2 CTAs of 320 threads or 1 of 576).
+uint32_t tc_ctas_per_sm(uint32_t tn, uint32_t stages, uint32_t split) {
+    const uint32_t smem = w8a16::tc_smem_bytes(tn, stages, split);
+    uint32_t by_smem = 233472u / (smem + 1024u);
     uint32_t by_tmem = 512u / w8a16::tc_tmem_cols(tn);
-    uint32_t by_regs = tn <= 64 ? 2u : 1u;                    // launch bounds of the kernel
+    uint32_t by_regs = 1u;                                   // launch bounds: 1 CTA per SM
     uint32_t c = by_smem < by_tmem ? by_smem : by_tmem;
     return c < by_regs ? c : by_regs;
 }
@@ -123,15 +126,15 @@ void fill_tc(uint32_t M, uint32_t N, uint32_t tn, uint32_t stages, uint32_t spli
     p->token_tile = tn;
     p->split_k = split;
     p->stages = stages;
-    p->ctas_per_sm = tc_ctas_per_sm(tn, stages);
+    p->ctas_per_sm = tc_ctas_per_sm(tn, stages, split);
     p->grid[0] = ceil_div(N, w8a16::kTcRows) * split;
     p->grid[1] = ceil_div(M, tn);
     p->grid[2] = 1;
-    p->block[0] = w8a16::kTcThreads;
+    p->block[0] = w8a16::tc_threads(tn);
     p->block[1] = p->block[2] = 1;
     p->cluster[0] = split;
     p->cluster[1] = p->cluster[2] = 1;
-    p->smem_bytes = w8a16::tc_smem_bytes(tn, stages);
+    p->smem_bytes = w8a16::tc_smem_bytes(tn, stages, split);
     p->tmem_cols = w8a16::tc_tmem_cols(tn);
 }
 
@@ -230,6 +233,10 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
     if (p.grid[0] != ref.grid[0] || p.grid[1] != ref.grid[1] || p.cluster[0] != ref.cluster[0])
         return fail(W8A16_ERR_PLAN, "TC plan grid does not match the shape");
     if (ref.grid[1] > 65535u) return fail(W8A16_ERR_RANGE, "TC plan: too many token tiles");
+    if (ref.smem_bytes > w8a16::kMaxDynSmem)
+        return fail(W8A16_ERR_PLAN, "TC plan: token_tile=" + u(p.token_tile) + " stages=" +
+                                        u(p.stages) + " split_k=" + u(p.split_k) + " needs " +
+                                        u(ref.smem_bytes) + " bytes of shared memory");
     return W8A16_OK;
 }
 
@@ -249,10 +256,13 @@ int plan_core(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, const uint3
     const uint32_t ksteps = K / w8a16::kKStep;
     uint32_t model[17];
     if (!cap) {
-        model_capacity(sm_count, tc_ctas_per_sm(tn, stages), model);
+        model_capacity(sm_count, tc_ctas_per_sm(tn, stages, 1), model);
         cap = model;
     }
-    const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, cap);
+    uint32_t usable[17];
+    for (uint32_t c = 0; c <= 16; ++c)   // splits whose shared memory does not fit are out
+        usable[c] = (c >= 1 && w8a16::tc_smem_bytes(tn, stages, c) <= w8a16::kMaxDynSmem) ? cap[c] : 0u;
+    const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, usable);
     fill_tc(M, N, tn, stages, split, out);
     return W8A16_OK;
 }

@@ -27,17 +27,42 @@ struct StatusWord {
 // Tiling constants of the tensor-core variant.
 constexpr uint32_t kTcRows = 128;      // weight rows per tile (tcgen05 MMA M)
 constexpr uint32_t kKStep = 128;       // K per pipeline stage == one scale block
-constexpr uint32_t kTcConvWarps = 8;   // converter / fold warps
-constexpr uint32_t kTcThreads = 64 + 32 * kTcConvWarps;
 constexpr uint32_t kTcMaxTokenTile = 128;
+constexpr uint32_t kMaxDynSmem = 232448;   // per-CTA dynamic shared memory limit (227 KiB)
 
-// Shared-memory bytes the TC kernel needs for a token tile and stage count.
-constexpr uint32_t tc_smem_bytes(uint32_t tn, uint32_t stages) {
-    return 1024 /* alignment slack */ + stages * (kTcRows * kKStep + tn * kKStep * 2) +
-           /* barriers, tmem slot, flags */ 256;
+// Warp roles per CTA: a weight-tile TMA producer, the MMA issuer, an
+// activation-tile TMA producer, 8 converter warps (E4M3 -> BF16 into TMEM) and
+// fold warps (step products -> FP32 accumulators).
+constexpr uint32_t tc_conv_warps(uint32_t tn) { return tn <= 32 ? 16u : 8u; }
+constexpr uint32_t tc_fold_warps(uint32_t tn) { return tn <= 32 ? 4u : 8u; }
+constexpr uint32_t tc_threads(uint32_t tn) {
+    return 96u + 32u * (tc_conv_warps(tn) + tc_fold_warps(tn));
 }
-constexpr uint32_t tc_tmem_cols(uint32_t tn) {
-    return (2 * (kKStep / 2) + 2 * tn) <= 256 ? 256u : 512u;
+// Activation ring depth per token tile (its slots are held until the MMA that
+// reads them completes; the weight ring's are released as soon as converted).
+constexpr uint32_t tc_act_stages(uint32_t tn) {
+    return tn == 16 ? 8u : tn == 32 ? 4u : tn == 64 ? 3u : 2u;
+}
+// TMEM: NA operand buffers of 64 columns (one BF16 128x128 weight tile) and NP
+// product buffers of TN FP32 columns.
+constexpr uint32_t tc_tmem_cols(uint32_t tn) { return tn <= 64 ? 256u : 512u; }
+constexpr uint32_t tc_p_bufs(uint32_t tn) { return tn == 16 ? 4u : 2u; }
+constexpr uint32_t tc_a_bufs(uint32_t tn) {
+    return (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u > 4u
+               ? 4u
+               : (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u;
+}
+// Split-K receive buffer of one CTA: a slot per cluster rank holding the rows
+// this CTA owns (at most ceil(128/split)) x TN FP32 partials.
+constexpr uint32_t tc_red_rows(uint32_t split) { return (kTcRows + split - 1) / split; }
+constexpr uint32_t tc_red_bytes(uint32_t tn, uint32_t split) {
+    return split <= 1 ? 0u : split * tc_red_rows(split) * tn * 4u;
+}
+// Dynamic shared memory: 1 KiB alignment slack, the weight ring (`stages`
+// 16 KiB slots), the activation ring, the receive buffer, barriers and flags.
+constexpr uint32_t tc_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
+    return 1024u + stages * kTcRows * kKStep + tc_act_stages(tn) * tn * kKStep * 2u +
+           tc_red_bytes(tn, split) + 1024u;
 }
 
 // Kernel launchers (implemented in the kernel translation units). They assume

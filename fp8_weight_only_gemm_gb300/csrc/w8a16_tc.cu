@@ -52,21 +52,38 @@ constexpr uint32_t kABufCols = kKStep / 2;            // TMEM columns of one BF1
 // Wait-detail codes (which barrier a timed-out wait was on).
 enum : uint32_t {
     kWaitFull = 1, kWaitEmpty = 2, kWaitAFull = 3, kWaitAEmpty = 4, kWaitPFull = 5,
-    kWaitPEmpty = 6, kWaitMmaDone = 7, kWaitDrain = 8
+    kWaitPEmpty = 6, kWaitMmaDone = 7, kWaitDrain = 8, kWaitRed = 9
 };
 
 template <uint32_t TN, uint32_t STAGES>
 struct TcCfg {
-    static constexpr uint32_t kActBytes = TN * kKStep * 2;   // BF16, two 64-K boxes
-    static constexpr uint32_t kStageBytes = kWTileBytes + kActBytes;
+    static constexpr uint32_t SA = tc_act_stages(TN);          // activation ring depth
+    static constexpr uint32_t kActBytes = TN * kKStep * 2;     // BF16, two 64-K boxes
     static constexpr uint32_t kTmemCols = tc_tmem_cols(TN);
-    static constexpr uint32_t kHalf = TN / 2;                 // tokens per converter warp
-    static constexpr uint32_t kNumBars = 2 * STAGES + 9;
+    static constexpr uint32_t NC = tc_conv_warps(TN);
+    static constexpr uint32_t kKPerConv = kKStep * 4 / NC;     // K of a step per converter warp
+    static constexpr uint32_t ND = SA > 4 ? SA : 4;            // MMA-completion barriers
+    static constexpr uint32_t NF = tc_fold_warps(TN);
+    static constexpr uint32_t NA = tc_a_bufs(TN);
+    static constexpr uint32_t NP = tc_p_bufs(TN);
+    static constexpr uint32_t kThreads = tc_threads(TN);
+    static constexpr uint32_t kConv0 = 3;                       // first converter warp
+    static constexpr uint32_t kFold0 = kConv0 + NC;             // first fold warp
+    static constexpr uint32_t kTokPerFold = TN * 4 / NF;        // tokens per fold thread
+    // barriers: wfull/wempty[S], xfull[SA], tfull[NA], mdone[ND], pempty[NP], done, red
+    static constexpr uint32_t kNumBars = 2 * STAGES + SA + NA + ND + NP + 2;
+    static_assert(NA >= 2 && NA * 64 + NP * TN <= kTmemCols, "TMEM budget");
+    static_assert(ND >= SA && ND >= NA && ND >= NP, "a completion barrier is never lapped");
+    static_assert(kKPerConv == 32 || kKPerConv == 64, "converter K slice");
+    static_assert(kTokPerFold % 8 == 0, "fold loads are whole x8 column groups");
+    static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
 };
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
@@ -75,10 +92,23 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+// One FP32 register into another CTA's shared memory, counted on that CTA's
+// mbarrier as completed transaction bytes.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, uint32_t remote_bar, float a) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr),
+        "f"(a), "r"(remote_bar)
+        : "memory");
+}
+
+template <uint32_t NREG>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[NREG]) {
+    if constexpr (NREG == 32) {
+        tmem_st_32x32b_x32(taddr, r);
+    } else {
+        static_assert(NREG == 16, "16 or 32 columns per converter store");
+        tmem_st_32x32b_x16(taddr, r);
+    }
 }
 
 // Warp-uniform bounded wait: every lane polls; the warp proceeds only if all did.
@@ -88,24 +118,24 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <uint32_t N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
-    if constexpr (N == 8) {
-        tmem_ld_32x32b_x8(taddr, v);
-    } else {
-        static_assert(N % 16 == 0, "token half must be 8 or a multiple of 16");
-#pragma unroll
-        for (uint32_t c = 0; c < N / 16; ++c) {
-            float t[16];
-            tmem_ld_32x32b_x16(taddr + 16 * c, t);
-#pragma unroll
-            for (uint32_t i = 0; i < 16; ++i) v[16 * c + i] = t[i];
-        }
+// First row of the weight tile owned by cluster rank r when split_k CTAs share it.
+__device__ __forceinline__ uint32_t owned_row0(uint32_t r, uint32_t split_k) {
+    return r * kTcRows / split_k;
+}
+
+// Wait until the last `depth` copies a producer issued into a ring have landed.
+__device__ __forceinline__ void drain_ring(uint32_t bar_base, uint32_t depth, uint32_t issued,
+                                           uint64_t timeout_ns) {
+    const uint64_t dl = globaltimer_ns() + timeout_ns;
+    for (uint32_t j = issued > depth ? issued - depth : 0; j < issued; ++j) {
+        volatile int never = 0;
+        mbar_wait(bar_base + 8u * (j % depth), (j / depth) & 1, dl, &never, &g_tc_status,
+                  kWaitDrain);
     }
 }
 
 template <uint32_t TN, uint32_t STAGES>
-__global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
+__global__ void __launch_bounds__(tc_threads(TN), 1)
     w8a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                     const float* __restrict__ scale, __nv_bfloat16* __restrict__ C, uint32_t ldc,
                     uint32_t M, uint32_t N, uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
@@ -113,20 +143,24 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* sW = smem;                                   // STAGES x 16 KiB
-    uint8_t* sA = smem + STAGES * kWTileBytes;            // STAGES x kActBytes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sA + STAGES * Cfg::kActBytes);
+    uint8_t* sW = smem;                                    // STAGES x 16 KiB of E4M3 codes
+    uint8_t* sX = smem + STAGES * kWTileBytes;             // SA x TN x 128 BF16 activations
+    float* sRed = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kActBytes);   // split-K slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sRed) +
+                                                 tc_red_bytes(TN, split_k));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+    // mdone[i % ND] completes when the MMAs of step i have: it frees activation
+    // slot i % SA, TMEM operand buffer i % NA, and fills product buffer i % NP.
     const uint32_t bar0 = smem_u32(bars);
-    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
-    auto afull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto aempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    auto pfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 4 + b); };
-    auto pempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 6 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 8);
+    const uint32_t wfull0 = bar0, wempty0 = wfull0 + 8u * STAGES;
+    const uint32_t xfull0 = wempty0 + 8u * STAGES;
+    const uint32_t tfull0 = xfull0 + 8u * Cfg::SA;
+    const uint32_t mdone0 = tfull0 + 8u * Cfg::NA;
+    const uint32_t pempty0 = mdone0 + 8u * Cfg::ND;
+    const uint32_t done_bar = pempty0 + 8u * Cfg::NP;
+    const uint32_t red_bar = done_bar + 8u;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t tile = blockIdx.x / split_k;     // cluster = split_k consecutive CTAs
@@ -137,22 +171,39 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
     const uint32_t s_end = static_cast<uint32_t>(static_cast<uint64_t>(rank + 1) * ksteps / split_k);
     const uint32_t nsteps = s_end - s_begin;
     const uint64_t deadline = globaltimer_ns() + timeout_ns;
+    const uint32_t my_row0 = owned_row0(rank, split_k);
+    const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
+    const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
 
-    if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kTcConvWarps + 1);
+    if (warp == 0) {
+        // barrier b is initialised by lane b % 32 (arrival counts by kind)
+        for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
+            const uint32_t addr = bar0 + 8u * b;
+            uint32_t count = 1;
+            if (addr >= wempty0 && addr < xfull0) count = Cfg::NC;        // converters
+            else if (addr >= tfull0 && addr < mdone0) count = Cfg::NC;    // converters
+            else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF; // fold warps
+            mbar_init(addr, count);
         }
-        for (uint32_t b = 0; b < 2; ++b) {
-            mbar_init(afull_bar(b), kTcConvWarps);
-            mbar_init(aempty_bar(b), 1);
-            mbar_init(pfull_bar(b), 1);
-            mbar_init(pempty_bar(b), kTcConvWarps);
-        }
-        mbar_init(done_bar, 1);
-        *abort_flag = 0;
+        if (lane == 0) *abort_flag = 0;
         fence_barrier_init();
-        tma_prefetch_desc(&tmW);
+        __syncwarp();
+    }
+    if (threadIdx.x == 0) {
+        if (split_k > 1)   // every rank pushes its partials of my rows here
+            mbar_arrive_expect_tx(red_bar, split_k * my_rows * TN * 4u);
+        // The first ring's weight tiles go out before anything else (TMEM
+        // allocation, the CTA barrier), so their HBM latency overlaps the set-up.
+        // Weights are requested before waiting on the previous grid in the
+        // stream: under a programmatic launch the caller guarantees that grid
+        // does not write W.
+        const uint64_t pol_w = l2_policy_evict_first();
+        for (uint32_t i = 0; i < npre; ++i) {
+            mbar_arrive_expect_tx(wfull0 + 8u * i, kWTileBytes);
+            tma_load_2d(smem_u32(sW + i * kWTileBytes), &tmW, wfull0 + 8u * i,
+                        static_cast<int32_t>((s_begin + i) * kKStep),
+                        static_cast<int32_t>(tile * kTcRows), pol_w);
+        }
         tma_prefetch_desc(&tmA);
     }
     if (warp == 1) {
@@ -162,95 +213,91 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Peers may push into this CTA's receive buffer once the cluster barrier
+    // completes; arrive now, wait only before the first push.
+    if (split_k > 1) cluster_arrive();
     // Dependents may be scheduled from here on: this CTA holds its TMEM already.
     if (threadIdx.x == 0) grid_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tA = tmem_base;                    // 2 x 64 columns: BF16 weight tiles
-    const uint32_t tP = tmem_base + 2 * kABufCols;    // 2 x TN columns: FP32 step products
-
-    float acc[Cfg::kHalf];
-#pragma unroll
-    for (uint32_t t = 0; t < Cfg::kHalf; ++t) acc[t] = 0.f;
-    const uint32_t cw = warp - 2;                     // converter index 0..7
-    const uint32_t quarter = warp & 3;                // TMEM lanes this warp may access
-    const uint32_t khalf = cw >> 2;                   // which 64 K of a step / which token half
-    const uint32_t row = quarter * 32 + lane;         // weight row within the tile
+    const uint32_t tA = tmem_base;                         // NA x 64 columns: BF16 weight tiles
+    const uint32_t tP = tmem_base + Cfg::NA * kABufCols;   // NP x TN columns: FP32 products
+    const uint32_t quarter = warp & 3;                     // TMEM lanes this warp may access
+    const uint32_t row = quarter * 32 + lane;              // weight row within the tile
     const uint32_t lane_bits = (quarter * 32) << 16;
+    const bool is_conv = warp >= Cfg::kConv0 && warp < Cfg::kFold0;
+    const bool is_fold = warp >= Cfg::kFold0;
+    const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
+    const uint32_t toks_valid = min(TN, M - token0);
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------------- weight producer (TMA)
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();   // W is streamed once
-            const uint64_t pol_a = l2_policy_evict_last();    // A is re-read by every tile
-            // The first ring's weight tiles are requested before waiting on the
-            // previous grid in the stream (under a programmatic launch the caller
-            // guarantees that grid does not write W); A is only read after the
-            // wait. Without a programmatic launch the wait returns at once.
-            const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
-            for (uint32_t i = 0; i < npre; ++i) {
-                mbar_arrive_expect_tx(full_bar(i), Cfg::kStageBytes);
-                tma_load_2d(smem_u32(sW + i * kWTileBytes), &tmW, full_bar(i),
+            uint32_t issued = npre;                            // issued at set-up
+            for (uint32_t i = npre; i < nsteps; ++i) {
+                const uint32_t s = i % STAGES;
+                if (!mbar_wait(wempty0 + 8u * s, ((i / STAGES) - 1) & 1, deadline, abort_flag,
+                               &g_tc_status, kWaitEmpty))
+                    break;
+                mbar_arrive_expect_tx(wfull0 + 8u * s, kWTileBytes);
+                tma_load_2d(smem_u32(sW + s * kWTileBytes), &tmW, wfull0 + 8u * s,
                             static_cast<int32_t>((s_begin + i) * kKStep),
                             static_cast<int32_t>(tile * kTcRows), pol_w);
+                issued = i + 1;
             }
+            // every issued copy lands before the CTA may exit
+            drain_ring(wfull0, STAGES, issued, timeout_ns);
+        }
+    } else if (warp == 2) {
+        // --------------------------------------- activation producer (TMA)
+        if (lane == 0) {
+            const uint64_t pol_a = l2_policy_evict_last();    // A is re-read by every tile
+            // A may be written by the previous grid in the stream: wait for it
+            // (returns at once unless launched as a programmatic dependent).
             grid_dependency_wait();
-            for (uint32_t i = 0; i < npre; ++i) {
+            uint32_t issued = 0;
+            for (uint32_t i = 0; i < nsteps; ++i) {
+                const uint32_t j = i % Cfg::SA;
+                if (i >= Cfg::SA) {   // slot j last held step i - SA: wait for its MMAs
+                    const uint32_t q = i - Cfg::SA;
+                    if (!mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline,
+                                   abort_flag, &g_tc_status, kWaitEmpty))
+                        break;
+                }
+                mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kActBytes);
                 const int32_t k = static_cast<int32_t>((s_begin + i) * kKStep);
-                const uint32_t a_dst = smem_u32(sA + i * Cfg::kActBytes);
-                tma_load_2d(a_dst, &tmA, full_bar(i), k, static_cast<int32_t>(token0), pol_a);
-                tma_load_2d(a_dst + TN * 128, &tmA, full_bar(i), k + 64,
-                            static_cast<int32_t>(token0), pol_a);
-            }
-            uint32_t issued = npre;
-            for (uint32_t i = npre; i < nsteps; ++i) {
-                const uint32_t s = i % STAGES, round = i / STAGES;
-                if (!mbar_wait(empty_bar(s), (round - 1) & 1, deadline, abort_flag, &g_tc_status,
-                               kWaitEmpty))
-                    break;
-                mbar_arrive_expect_tx(full_bar(s), Cfg::kStageBytes);
-                const int32_t k = static_cast<int32_t>((s_begin + i) * kKStep);
-                tma_load_2d(smem_u32(sW + s * kWTileBytes), &tmW, full_bar(s), k,
-                            static_cast<int32_t>(tile * kTcRows), pol_w);
-                const uint32_t a_dst = smem_u32(sA + s * Cfg::kActBytes);
-                tma_load_2d(a_dst, &tmA, full_bar(s), k, static_cast<int32_t>(token0), pol_a);
-                tma_load_2d(a_dst + TN * 128, &tmA, full_bar(s), k + 64,
+                const uint32_t dst = smem_u32(sX + j * Cfg::kActBytes);
+                tma_load_2d(dst, &tmA, xfull0 + 8u * j, k, static_cast<int32_t>(token0), pol_a);
+                tma_load_2d(dst + TN * 128, &tmA, xfull0 + 8u * j, k + 64,
                             static_cast<int32_t>(token0), pol_a);
                 issued = i + 1;
             }
-            // Every issued copy must land before the CTA may exit or reuse its
-            // shared memory (on the normal path they already have).
-            const uint64_t drain_deadline = globaltimer_ns() + timeout_ns;
-            for (uint32_t j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j) {
-                volatile int never = 0;
-                mbar_wait(full_bar(j % STAGES), (j / STAGES) & 1, drain_deadline, &never,
-                          &g_tc_status, kWaitDrain);
-            }
+            drain_ring(xfull0, Cfg::SA, issued, timeout_ns);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kTcRows, TN);
             for (uint32_t i = 0; i < nsteps; ++i) {
-                const uint32_t b = i & 1, use = i >> 1, s = i % STAGES;
-                if (!mbar_wait(afull_bar(b), use & 1, deadline, abort_flag, &g_tc_status, kWaitAFull))
+                const uint32_t a = i % Cfg::NA, p = i % Cfg::NP, j = i % Cfg::SA;
+                if (!mbar_wait(tfull0 + 8u * a, (i / Cfg::NA) & 1, deadline, abort_flag,
+                               &g_tc_status, kWaitAFull))
                     break;
-                if (!mbar_wait(full_bar(s), (i / STAGES) & 1, deadline, abort_flag, &g_tc_status,
-                               kWaitFull))
+                if (!mbar_wait(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag,
+                               &g_tc_status, kWaitFull))
                     break;
-                if (use > 0 && !mbar_wait(pempty_bar(b), (use - 1) & 1, deadline, abort_flag,
-                                          &g_tc_status, kWaitPEmpty))
+                if (i >= Cfg::NP && !mbar_wait(pempty0 + 8u * p, ((i / Cfg::NP) - 1) & 1, deadline,
+                                               abort_flag, &g_tc_status, kWaitPEmpty))
                     break;
                 tc_fence_after();
-                const uint32_t act = smem_u32(sA + s * Cfg::kActBytes);
+                const uint32_t act = smem_u32(sX + j * Cfg::kActBytes);
 #pragma unroll
-                for (uint32_t j = 0; j < kKStep / 16; ++j) {
+                for (uint32_t kk = 0; kk < kKStep / 16; ++kk) {
                     const uint64_t bdesc =
-                        smem_desc_kmajor_sw128(act + (j >> 2) * (TN * 128) + (j & 3) * 32);
-                    tc_mma_a_tmem(tP + b * TN, tA + b * kABufCols + j * 8, bdesc, idesc, j > 0);
+                        smem_desc_kmajor_sw128(act + (kk >> 2) * (TN * 128) + (kk & 3) * 32);
+                    tc_mma_a_tmem(tP + p * TN, tA + a * kABufCols + kk * 8, bdesc, idesc, kk > 0);
                 }
-                tc_commit(pfull_bar(b));
-                tc_commit(aempty_bar(b));
-                tc_commit(empty_bar(s));
+                tc_commit(mdone0 + 8u * (i % Cfg::ND));
             }
             // All MMAs this thread issued must finish before TMEM is released.
             tc_commit(done_bar);
@@ -258,67 +305,109 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
             mbar_wait(done_bar, 0, globaltimer_ns() + timeout_ns, &never, &g_tc_status,
                       kWaitMmaDone);
         }
-    } else {
-        // ------------------------------------------- converters and scale fold
-        const float* srow = scale + static_cast<size_t>(tile) * ksteps + s_begin;
-        auto fold = [&](uint32_t j) -> bool {
-            const uint32_t b = j & 1;
-            if (!warp_wait(pfull_bar(b), (j >> 1) & 1, deadline, abort_flag, kWaitPFull))
-                return false;
-            tc_fence_after();
-            float p[Cfg::kHalf];
-            tmem_ld_cols<Cfg::kHalf>(tP + lane_bits + b * TN + khalf * Cfg::kHalf, p);
-            tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pempty_bar(b));
-            const float sc = __ldg(srow + j);
-#pragma unroll
-            for (uint32_t t = 0; t < Cfg::kHalf; ++t) acc[t] = fmaf(sc, p[t], acc[t]);
-            return true;
-        };
-
-        bool ok = true;
+    } else if (is_conv) {
+        // -------------------------------------- converters: E4M3 -> BF16 in TMEM
+        // The NC/4 converter warps of one TMEM lane quarter split each step's K
+        // into slices of kKPerConv codes (32 or 64) per row.
+        const uint32_t slice = (warp - Cfg::kConv0) >> 2;
+        constexpr uint32_t kChunks = Cfg::kKPerConv / 16;           // 16-byte chunks per row
         const uint32_t swz = row & 7;
-        for (uint32_t i = 0; i < nsteps && ok; ++i) {
-            const uint32_t b = i & 1, use = i >> 1, s = i % STAGES;
-            if (!warp_wait(full_bar(s), (i / STAGES) & 1, deadline, abort_flag, kWaitFull)) {
-                ok = false;
-                break;
-            }
-            // This thread's 64 codes: row `row`, K [64 khalf, 64 khalf + 64) of the
-            // step, stored as 16-byte chunks 4 khalf + c at chunk (4 khalf + c) ^ (row & 7)
-            // (TMA's 128-byte swizzle).
+        for (uint32_t i = 0; i < nsteps; ++i) {
+            const uint32_t a = i % Cfg::NA, s = i % STAGES;
+            if (!warp_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, kWaitFull)) break;
+            // Row `row`'s codes of this slice sit in 16-byte chunks slice*kChunks.., chunk
+            // c at position c ^ (row & 7) (TMA's 128-byte swizzle).
             const uint8_t* rp = sW + s * kWTileBytes + row * 128;
-            uint4 q[4];
+            uint4 q[kChunks];
 #pragma unroll
-            for (uint32_t c = 0; c < 4; ++c)
-                q[c] = *reinterpret_cast<const uint4*>(rp + (((4 * khalf + c) ^ swz) << 4));
+            for (uint32_t c = 0; c < kChunks; ++c)
+                q[c] = *reinterpret_cast<const uint4*>(rp + (((slice * kChunks + c) ^ swz) << 4));
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(s));
-
-            uint32_t w[32];
+            if (lane == 0) mbar_arrive(wempty0 + 8u * s);   // the codes are in registers
+            uint32_t w[kChunks * 8];
 #pragma unroll
-            for (uint32_t c = 0; c < 4; ++c) {
+            for (uint32_t c = 0; c < kChunks; ++c) {
                 uint32_t o[8];
                 e4m3x16_to_bf16x16(q[c], o);
 #pragma unroll
                 for (uint32_t t = 0; t < 8; ++t) w[8 * c + t] = o[t];
             }
-            if (use > 0 &&
-                !warp_wait(aempty_bar(b), (use - 1) & 1, deadline, abort_flag, kWaitAEmpty)) {
-                ok = false;
-                break;
+            if (i >= Cfg::NA) {   // buffer a last held step i - NA: wait for its MMAs
+                const uint32_t q2 = i - Cfg::NA;
+                if (!warp_wait(mdone0 + 8u * (q2 % Cfg::ND), (q2 / Cfg::ND) & 1, deadline, abort_flag,
+                               kWaitAEmpty))
+                    break;
             }
             tc_fence_after();
-            tmem_st_32x32b_x32(tA + lane_bits + b * kABufCols + khalf * 32, w);
+            tmem_st_cols<kChunks * 8>(tA + lane_bits + a * kABufCols + slice * (kChunks * 8), w);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull_bar(b));
-            if (i > 0 && !fold(i - 1)) ok = false;
+            if (lane == 0) mbar_arrive(tfull0 + 8u * a);
         }
-        if (ok && nsteps > 0) ok = fold(nsteps - 1);
+    } else if (is_fold) {
+        // ------------------------------- fold: acc += scale(step) * P(step)
+        const uint32_t fh = (warp - Cfg::kFold0) >> 2;   // token group of this fold warp
+        float acc[Cfg::kTokPerFold];
+#pragma unroll
+        for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) acc[t] = 0.f;
+        const float* srow = scale + static_cast<size_t>(tile) * ksteps + s_begin;
+        for (uint32_t i = 0; i < nsteps; ++i) {
+            const uint32_t p = i % Cfg::NP;
+            if (!warp_wait(mdone0 + 8u * (i % Cfg::ND), (i / Cfg::ND) & 1, deadline, abort_flag,
+                           kWaitPFull))
+                break;
+            tc_fence_after();
+            const float sc = __ldg(srow + i);
+            const uint32_t pcol = tP + lane_bits + p * TN + fh * Cfg::kTokPerFold;
+            // up to 32 columns per wait (16 when the accumulators are wide, to
+            // bound register use)
+            constexpr uint32_t kChunk = Cfg::kTokPerFold > 32 ? 16u : 32u;
+#pragma unroll
+            for (uint32_t c = 0; c < Cfg::kTokPerFold; c += kChunk) {
+                float v0[16], v1[16];
+                tmem_ld_32x32b_x16(pcol + c, v0);
+                if (kChunk == 32 && c + 16 < Cfg::kTokPerFold) tmem_ld_32x32b_x16(pcol + c + 16, v1);
+                tc_wait_ld();
+#pragma unroll
+                for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sc, v0[t], acc[c + t]);
+                if (kChunk == 32 && c + 16 < Cfg::kTokPerFold) {
+#pragma unroll
+                    for (uint32_t t = 0; t < 16; ++t) acc[c + 16 + t] = fmaf(sc, v1[t], acc[c + 16 + t]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pempty0 + 8u * p);
+        }
+        if (split_k == 1) {
+            if (row < rows_valid) {
+                const uint32_t n = tile * kTcRows + row;
+#pragma unroll
+                for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) {
+                    const uint32_t m = fh * Cfg::kTokPerFold + t;
+                    if (m < toks_valid)
+                        C[static_cast<size_t>(token0 + m) * ldc + n] = __float2bfloat16_rn(acc[t]);
+                }
+            }
+        } else {
+            // Split-K: push this row's partial to the rank owning the row (slot =
+            // this CTA's rank). No CTA reads another's shared memory, so none has
+            // to wait for the others before it exits.
+            cluster_wait();
+            uint32_t owner = 0;
+            while (owner + 1 < split_k && owned_row0(owner + 1, split_k) <= row) ++owner;
+            const uint32_t lrow = row - owned_row0(owner, split_k);
+            // receive layout [slot][token][row]: a warp's 32 rows land in 32
+            // consecutive words, and the owner reads them back the same way
+            const uint32_t off =
+                ((rank * TN + fh * Cfg::kTokPerFold) * tc_red_rows(split_k) + lrow) * 4u;
+            const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
+            const uint32_t dbar = dsmem_map(red_bar, owner);
+#pragma unroll
+            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)
+                st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+        }
     }
 
     // ------------------------------------------------------------ teardown
@@ -328,46 +417,22 @@ __global__ void __launch_bounds__(kTcThreads, TN <= 64 ? 2 : 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
+    if (split_k == 1) return;
 
-    const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
-    const uint32_t toks_valid = min(TN, M - token0);
-    if (split_k == 1) {
-        if (warp >= 2 && row < rows_valid) {
-            const uint32_t n = tile * kTcRows + row;
-#pragma unroll
-            for (uint32_t t = 0; t < Cfg::kHalf; ++t) {
-                const uint32_t m = khalf * Cfg::kHalf + t;
-                if (m < toks_valid)
-                    C[static_cast<size_t>(token0 + m) * ldc + n] = __float2bfloat16_rn(acc[t]);
-            }
-        }
-        return;
-    }
-
-    // Split-K: partials to shared memory as red[token][row] (over the drained
-    // ring), then every CTA of the cluster sums its slice of the outputs over
-    // ranks 0..split_k-1 in order.
-    float* red = reinterpret_cast<float*>(smem);
-    if (warp >= 2) {
-#pragma unroll
-        for (uint32_t t = 0; t < Cfg::kHalf; ++t) red[(khalf * Cfg::kHalf + t) * kTcRows + row] = acc[t];
-    }
-    cluster_sync_all();
-    {
-        const uint32_t total = toks_valid * kTcRows;
-        const uint32_t beg = static_cast<uint32_t>(static_cast<uint64_t>(rank) * total / split_k);
-        const uint32_t end = static_cast<uint32_t>(static_cast<uint64_t>(rank + 1) * total / split_k);
-        const uint32_t red_local = smem_u32(red);
-        for (uint32_t idx = beg + threadIdx.x; idx < end; idx += kTcThreads) {
-            const uint32_t tok = idx / kTcRows, r = idx % kTcRows;
+    // Each rank sums the rows it owns over the slots in rank (= K) order.
+    const bool got = warp_wait(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+    if (got) {
+        const uint32_t total = my_rows * toks_valid;
+        for (uint32_t idx = threadIdx.x; idx < total; idx += Cfg::kThreads) {
+            const uint32_t tok = idx / my_rows, lr = idx % my_rows;
+            const uint32_t r = my_row0 + lr;
             if (r >= rows_valid) continue;
             float v = 0.f;
             for (uint32_t src = 0; src < split_k; ++src)
-                v += dsmem_ld_f32(dsmem_map(red_local + 4u * idx, src));
+                v += sRed[(src * TN + tok) * tc_red_rows(split_k) + lr];
             C[static_cast<size_t>(token0 + tok) * ldc + tile * kTcRows + r] = __float2bfloat16_rn(v);
         }
     }
-    cluster_sync_all();   // no CTA leaves while others still read its shared memory
 }
 
 // One CTA, one thread: waits on an mbarrier nothing arrives on, so the bounded
@@ -464,10 +529,10 @@ struct TcInstance {
 
 #define W8A16_TC_INST(TN_, ST_) {TN_, ST_, &w8a16_tc_kernel<TN_, ST_>}
 const TcInstance kTcInstances[] = {
-    W8A16_TC_INST(16, 4), W8A16_TC_INST(16, 6), W8A16_TC_INST(16, 8),
-    W8A16_TC_INST(32, 4), W8A16_TC_INST(32, 6), W8A16_TC_INST(32, 8),
-    W8A16_TC_INST(64, 3), W8A16_TC_INST(64, 4), W8A16_TC_INST(64, 6),
-    W8A16_TC_INST(128, 4),
+    W8A16_TC_INST(16, 4),  W8A16_TC_INST(16, 6),  W8A16_TC_INST(16, 8), W8A16_TC_INST(16, 10),
+    W8A16_TC_INST(32, 3),  W8A16_TC_INST(32, 4),  W8A16_TC_INST(32, 6), W8A16_TC_INST(32, 8),
+    W8A16_TC_INST(64, 4),  W8A16_TC_INST(64, 6),  W8A16_TC_INST(64, 8),
+    W8A16_TC_INST(128, 4), W8A16_TC_INST(128, 6),
 };
 #undef W8A16_TC_INST
 constexpr int kNumTcInstances = sizeof(kTcInstances) / sizeof(kTcInstances[0]);
@@ -487,9 +552,15 @@ cudaError_t ensure_attributes(int inst, int device) {
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (done[device][inst]) return cudaSuccess;
     const TcInstance& k = kTcInstances[inst];
+    // the largest request any split of this instance makes (capped at the limit)
+    uint32_t most = 0;
+    for (uint32_t sp = 1; sp <= 16; ++sp) {
+        const uint32_t b = tc_smem_bytes(k.tn, k.stages, sp);
+        if (b <= kMaxDynSmem && b > most) most = b;
+    }
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(tc_smem_bytes(k.tn, k.stages)));
+                                         static_cast<int>(most));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -531,8 +602,8 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
-    cfg.dynamicSmemBytes = tc_smem_bytes(p.token_tile, p.stages);
+    cfg.blockDim = dim3(tc_threads(p.token_tile), 1, 1);
+    cfg.dynamicSmemBytes = tc_smem_bytes(p.token_tile, p.stages, p.split_k);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -567,8 +638,12 @@ int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(cluster * 64, 1, 1);
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
-    cfg.dynamicSmemBytes = tc_smem_bytes(tn, stages);
+    cfg.blockDim = dim3(tc_threads(tn), 1, 1);
+    cfg.dynamicSmemBytes = tc_smem_bytes(tn, stages, cluster);
+    if (cfg.dynamicSmemBytes > kMaxDynSmem) {
+        *ctas = 0;
+        return W8A16_OK;
+    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster;

@@ -68,16 +68,18 @@ def test_forced_splits(split_k, M):
     assert np.array_equal(got, again), "same plan, different bits: not deterministic"
 
 
-@pytest.mark.parametrize("M,stages", [(4, 4), (4, 6), (4, 8), (24, 6), (24, 8), (48, 3), (48, 4),
-                                      (48, 6), (100, 4)])
-def test_stage_instances(M, stages):
+@pytest.mark.parametrize("M,stages,split", [(4, 4, 2), (4, 6, 2), (4, 8, 2), (4, 10, 3), (24, 3, 2),
+                                            (24, 4, 2), (24, 6, 2), (24, 8, 3), (48, 4, 2),
+                                            (48, 6, 2), (48, 8, 3), (100, 4, 2), (100, 6, 1),
+                                            (100, 6, 2)])
+def test_stage_instances(M, stages, split):
     from fp8_weight_only_gemm_gb300 import binding
     case = workloads.make_case("decode_gemv_m1_n4096_k4096", M=M, N=384, K=1536, seed=200 + M)
     wl = case.wl
-    p = _plan(wl.M, wl.N, wl.K, binding.VARIANT_TC, split_k=2, stages=stages)
+    p = _plan(wl.M, wl.N, wl.K, binding.VARIANT_TC, split_k=split, stages=stages)
     got = run_gpu(case, plan=p)
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=2, label=f"stages{stages}/M{M}")
+    compare(case, got, ref, exact, absum, split_k=split, label=f"stages{stages}/M{M}")
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldc", [

@@ -107,7 +107,7 @@ def test_plans_for_the_workloads(lib, M, N, K, tn):
     assert p["grid"][0] == -(-N // 128) * p["split_k"]
     assert p["grid"][1] == -(-M // tn)
     assert p["cluster"][0] == p["split_k"]
-    assert p["block"][0] == 320
+    assert p["block"][0] == (736 if tn <= 32 else 608)
     assert p["tmem_cols"] * p["ctas_per_sm"] <= 512
     assert p["smem_bytes"] * p["ctas_per_sm"] <= 232448
 
@@ -116,8 +116,8 @@ def test_planner_fills_the_gpu_for_decode(lib):
     # a 32-tile decode GEMV must split K so that most SMs get work
     p = binding.plan_for(1, 4096, 4096, sm_count=152)
     ctas = p["grid"][0] * p["grid"][1]
-    assert ctas >= 152
-    assert ctas <= 152 * p["ctas_per_sm"]
+    assert ctas >= 0.8 * 152                 # most SMs stream weights
+    assert ctas <= 152 * p["ctas_per_sm"]    # in one wave
 
 
 def test_planner_uses_cluster_capacity(lib):
@@ -136,12 +136,19 @@ def test_planner_uses_cluster_capacity(lib):
 
 def test_plan_variant_validation(lib):
     p = binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=4, stages=6)
+    assert p.token_tile == 16
     assert p.split_k == 4 and p.stages == 6 and p.grid[0] == 8 * 4
     with pytest.raises(binding.W8A16Error) as e:
         binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=9)   # > K/128 = 8
     assert e.value.code == ERR["PLAN"]
     with pytest.raises(binding.W8A16Error):
         binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, stages=5)    # no instance
+    # the widest token tile's 6-slot ring leaves room for small split-K receive
+    # buffers only
+    assert binding.plan_variant(100, 1024, 2048, binding.VARIANT_TC, split_k=2, stages=6).stages == 6
+    with pytest.raises(binding.W8A16Error) as e:
+        binding.plan_variant(100, 1024, 2048, binding.VARIANT_TC, split_k=14, stages=6)
+    assert "shared memory" in str(e.value)
     s = binding.plan_variant(8, 1024, 1024, binding.VARIANT_SIMT)
     assert s.variant == binding.VARIANT_SIMT and s.grid[0] == 128
     with pytest.raises(binding.W8A16Error):
