@@ -5,12 +5,14 @@ scale per 128x128 block)^T, computed by hand-written tcgen05/TMA kernels in
 ``libw8a16.so`` behind a C ABI (include/w8a16.h). This package is the thin
 Python binding: torch provides device memory and streams only.
 """
-from .binding import (FLAG_PDL, Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, W8A16Error,
+from .binding import (FLAG_PDL, Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8,
+                      W8A16Error,
                       check_args, cluster_capacity, device_status, gemm, gemm_host, gemm_ptr,
                       header_functions, last_error, load, plan_current, plan_for, plan_variant,
                       selftest_wait_timeout, strerror, version)
 
-__all__ = ["FLAG_PDL", "Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "W8A16Error",
+__all__ = ["FLAG_PDL", "Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "VARIANT_TC8",
+           "W8A16Error",
            "check_args", "cluster_capacity", "device_status", "gemm", "gemm_host", "gemm_ptr",
            "header_functions", "last_error", "load", "plan_current", "plan_for", "plan_variant",
            "selftest_wait_timeout", "strerror", "version"]

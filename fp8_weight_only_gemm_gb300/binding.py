@@ -18,7 +18,7 @@ HEADER = PKG.parent / "include" / "w8a16.h"
 # Values mirrored from include/w8a16.h (checked against the header by the tests).
 W8A16_OK = 0
 FLAG_PDL = 1
-VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC = 0, 1, 2
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8 = 0, 1, 2, 3
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
 
 
@@ -52,7 +52,7 @@ _SIGS = {
     "w8a16_check_args": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32]),
     "w8a16_plan_for": (_INT, [_U32, _U32, _U32, _U32, ctypes.POINTER(_U32), ctypes.POINTER(Plan)]),
     "w8a16_plan_current": (_INT, [_U32, _U32, _U32, ctypes.POINTER(Plan)]),
-    "w8a16_cluster_capacity": (_INT, [_U32, _U32, ctypes.POINTER(_U32)]),
+    "w8a16_cluster_capacity": (_INT, [_I32, _U32, _U32, ctypes.POINTER(_U32)]),
     "w8a16_plan_variant": (_INT, [_U32, _U32, _U32, _I32, _U32, _U32, _U32, ctypes.POINTER(Plan)]),
     "w8a16_gemm_with_plan": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32,
                                     ctypes.POINTER(Plan), _U32, _VP]),
@@ -136,9 +136,9 @@ def plan_current(M, N, K) -> dict:
     return p.as_dict()
 
 
-def cluster_capacity(token_tile, stages) -> list[int]:
+def cluster_capacity(token_tile, stages, variant=VARIANT_TC) -> list[int]:
     out = (_U32 * 17)()
-    _check(load().w8a16_cluster_capacity(token_tile, stages, out))
+    _check(load().w8a16_cluster_capacity(variant, token_tile, stages, out))
     return list(out)
 
 

@@ -104,38 +104,62 @@ uint32_t token_tile_for(uint32_t M) {
     return 128;
 }
 
-uint32_t default_stages(uint32_t tn) { return tn == 16 ? 8 : tn == 32 ? 6 : tn == 64 ? 6 : 4; }
+// Tensor-core variants: TC (BF16 datapath) and TC8 (FP8 datapath, token tiles
+// up to 64). Per-variant sizes come from the shared constants.
+bool is_tc_variant(int32_t v) { return v == W8A16_VARIANT_TC || v == W8A16_VARIANT_TC8; }
+uint32_t max_token_tile(int32_t v) { return v == W8A16_VARIANT_TC8 ? 64u : 128u; }
+uint32_t v_threads(int32_t v, uint32_t tn) {
+    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_threads(tn) : w8a16::tc_threads(tn);
+}
+uint32_t v_smem(int32_t v, uint32_t tn, uint32_t st, uint32_t split) {
+    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_smem_bytes(tn, st, split)
+                                  : w8a16::tc_smem_bytes(tn, st, split);
+}
+uint32_t v_tmem(int32_t v, uint32_t tn) {
+    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_tmem_cols(tn) : w8a16::tc_tmem_cols(tn);
+}
+bool v_supported(int32_t v, uint32_t tn, uint32_t st) {
+    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_supported_stages(tn, st)
+                                  : w8a16::tc_supported_stages(tn, st);
+}
+uint32_t default_stages(int32_t v, uint32_t tn) {
+    if (v == W8A16_VARIANT_TC8) return tn == 16 ? 4 : tn == 32 ? 6 : 4;   // 16: two CTAs per SM
+    return tn == 16 ? 8 : tn == 32 ? 6 : tn == 64 ? 6 : 4;
+}
+// The variant the planner uses for a token count.
+int32_t auto_variant(uint32_t M) { return M <= 32 ? W8A16_VARIANT_TC8 : W8A16_VARIANT_TC; }
 
-// CTAs of one TC plan that fit on an SM: shared memory (228 KiB per SM, 1 KiB
-// reserved per CTA), TMEM (512 columns), and registers (the kernel's launch
-// bounds allow 2 CTAs of 320 threads or 1 of 576).
-uint32_t tc_ctas_per_sm(uint32_t tn, uint32_t stages, uint32_t split) {
-    const uint32_t smem = w8a16::tc_smem_bytes(tn, stages, split);
-    uint32_t by_smem = 233472u / (smem + 1024u);
-    uint32_t by_tmem = 512u / w8a16::tc_tmem_cols(tn);
-    uint32_t by_regs = 1u;                                   // launch bounds: 1 CTA per SM
+// CTAs of one tensor-core plan that fit on an SM: shared memory (228 KiB per
+// SM, 1 KiB reserved per CTA), TMEM (512 columns), threads (2048), and the
+// kernels' launch bounds (registers sized for one CTA per SM).
+uint32_t tc_ctas_per_sm(int32_t v, uint32_t tn, uint32_t stages, uint32_t split) {
+    const uint32_t smem = v_smem(v, tn, stages, split);
+    const uint32_t by_smem = 233472u / (smem + 1024u);
+    const uint32_t by_tmem = 512u / v_tmem(v, tn);
+    const uint32_t by_threads = 2048u / v_threads(v, tn);
     uint32_t c = by_smem < by_tmem ? by_smem : by_tmem;
-    return c < by_regs ? c : by_regs;
+    c = c < by_threads ? c : by_threads;
+    return c < 1u ? 1u : c;
 }
 
-// Fill a TC plan for a given token tile, stage count and split.
-void fill_tc(uint32_t M, uint32_t N, uint32_t tn, uint32_t stages, uint32_t split,
+// Fill a tensor-core plan for a given variant, token tile, stage count and split.
+void fill_tc(int32_t v, uint32_t M, uint32_t N, uint32_t tn, uint32_t stages, uint32_t split,
              w8a16_plan_t* p) {
     std::memset(p, 0, sizeof *p);
-    p->variant = W8A16_VARIANT_TC;
+    p->variant = v;
     p->token_tile = tn;
     p->split_k = split;
     p->stages = stages;
-    p->ctas_per_sm = tc_ctas_per_sm(tn, stages, split);
+    p->ctas_per_sm = tc_ctas_per_sm(v, tn, stages, split);
     p->grid[0] = ceil_div(N, w8a16::kTcRows) * split;
     p->grid[1] = ceil_div(M, tn);
     p->grid[2] = 1;
-    p->block[0] = w8a16::tc_threads(tn);
+    p->block[0] = v_threads(v, tn);
     p->block[1] = p->block[2] = 1;
     p->cluster[0] = split;
     p->cluster[1] = p->cluster[2] = 1;
-    p->smem_bytes = w8a16::tc_smem_bytes(tn, stages, split);
-    p->tmem_cols = w8a16::tc_tmem_cols(tn);
+    p->smem_bytes = v_smem(v, tn, stages, split);
+    p->tmem_cols = v_tmem(v, tn);
 }
 
 void fill_simt(uint32_t M, uint32_t N, w8a16_plan_t* p) {
@@ -220,16 +244,17 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
             return fail(W8A16_ERR_PLAN, "SIMT plan does not match the shape");
         return W8A16_OK;
     }
-    if (p.variant != W8A16_VARIANT_TC)
+    if (!is_tc_variant(p.variant))
         return fail(W8A16_ERR_PLAN, "unknown variant " + std::to_string(p.variant));
-    if (!w8a16::tc_supported_stages(p.token_tile, p.stages))
+    if (!v_supported(p.variant, p.token_tile, p.stages))
         return fail(W8A16_ERR_PLAN, "TC plan: token_tile=" + u(p.token_tile) + " stages=" +
-                                        u(p.stages) + " has no kernel instance");
+                                        u(p.stages) + " has no kernel instance for variant " +
+                                        std::to_string(p.variant));
     if (p.split_k < 1 || p.split_k > 16 || p.split_k > ksteps)
         return fail(W8A16_ERR_PLAN, "TC plan: split_k=" + u(p.split_k) +
                                         " must be in 1..min(16, K/128=" + u(ksteps) + ")");
     w8a16_plan_t ref;
-    fill_tc(M, N, p.token_tile, p.stages, p.split_k, &ref);
+    fill_tc(p.variant, M, N, p.token_tile, p.stages, p.split_k, &ref);
     if (p.grid[0] != ref.grid[0] || p.grid[1] != ref.grid[1] || p.cluster[0] != ref.cluster[0])
         return fail(W8A16_ERR_PLAN, "TC plan grid does not match the shape");
     if (ref.grid[1] > 65535u) return fail(W8A16_ERR_RANGE, "TC plan: too many token tiles");
@@ -245,62 +270,72 @@ void model_capacity(uint32_t sm_count, uint32_t per_sm, uint32_t* cap) {
     for (uint32_t c = 1; c <= 16; ++c) cap[c] = ((sm_count ? sm_count : 152u) * per_sm / c) * c;
 }
 
-// Pure planner: token tile by M, stage count by token tile, split from the
-// wave model over `cap` (NULL: every cluster size fills every SM slot).
-int plan_core(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, const uint32_t* cap,
-              w8a16_plan_t* out) {
+uint32_t token_tile_for(int32_t v, uint32_t M) {
     const uint32_t tn = token_tile_for(M);
-    const uint32_t stages = default_stages(tn);
+    return tn > max_token_tile(v) ? max_token_tile(v) : tn;
+}
+
+// Pure planner: variant by M (or as given), token tile by M, stage count by
+// token tile, split from the wave model over `cap` (NULL: every cluster size
+// fills every SM slot).
+int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
+              const uint32_t* cap, w8a16_plan_t* out) {
+    if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
+    const uint32_t tn = token_tile_for(v, M);
+    const uint32_t stages = default_stages(v, tn);
     const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows);
     const uint32_t token_tiles = ceil_div(M, tn);
     const uint32_t ksteps = K / w8a16::kKStep;
     uint32_t model[17];
     if (!cap) {
-        model_capacity(sm_count, tc_ctas_per_sm(tn, stages, 1), model);
+        model_capacity(sm_count, tc_ctas_per_sm(v, tn, stages, 1), model);
         cap = model;
     }
     uint32_t usable[17];
     for (uint32_t c = 0; c <= 16; ++c)   // splits whose shared memory does not fit are out
-        usable[c] = (c >= 1 && w8a16::tc_smem_bytes(tn, stages, c) <= w8a16::kMaxDynSmem) ? cap[c] : 0u;
+        usable[c] = (c >= 1 && v_smem(v, tn, stages, c) <= w8a16::kMaxDynSmem) ? cap[c] : 0u;
     const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, usable);
-    fill_tc(M, N, tn, stages, split, out);
+    fill_tc(v, M, N, tn, stages, split, out);
     return W8A16_OK;
 }
 
-// Live capacity table of the current device for (tn, stages), cached.
-int live_capacity(uint32_t tn, uint32_t stages, uint32_t* cap, std::string* err) {
+// Live capacity table of the current device for (variant, tn, stages), cached.
+int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::string* err) {
     static std::mutex mu;
-    struct Entry { int dev; uint32_t tn, stages; uint32_t cap[17]; };
-    static Entry cache[64];
+    struct Entry { int dev; int32_t v; uint32_t tn, stages; uint32_t cap[17]; };
+    static Entry cache[128];
     static int used = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     {
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < used; ++i)
-            if (cache[i].dev == dev && cache[i].tn == tn && cache[i].stages == stages) {
+            if (cache[i].dev == dev && cache[i].v == v && cache[i].tn == tn &&
+                cache[i].stages == stages) {
                 std::memcpy(cap, cache[i].cap, sizeof(uint32_t) * 17);
                 return W8A16_OK;
             }
     }
-    Entry e{dev, tn, stages, {0}};
+    Entry e{dev, v, tn, stages, {0}};
     for (uint32_t c = 1; c <= 16; ++c) {
-        int rc = w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
+        int rc = v == W8A16_VARIANT_TC8 ? w8a16::tc8_cluster_capacity(tn, stages, c, &e.cap[c], err)
+                                        : w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
         if (rc) return rc;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (used < 64) cache[used++] = e;
+    if (used < 128) cache[used++] = e;
     std::memcpy(cap, e.cap, sizeof(uint32_t) * 17);
     return W8A16_OK;
 }
 
 int plan_live(uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& info, w8a16_plan_t* out,
               std::string* err) {
-    const uint32_t tn = token_tile_for(M);
+    const int32_t v = auto_variant(M);
+    const uint32_t tn = token_tile_for(v, M);
     uint32_t cap[17];
-    int rc = live_capacity(tn, default_stages(tn), cap, err);
+    int rc = live_capacity(v, tn, default_stages(v, tn), cap, err);
     if (rc) return rc;
-    return plan_core(M, N, K, static_cast<uint32_t>(info.sm_count), cap, out);
+    return plan_core(v, M, N, K, static_cast<uint32_t>(info.sm_count), cap, out);
 }
 
 int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
@@ -332,6 +367,8 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
     }
     if (plan.variant == W8A16_VARIANT_SIMT)
         rc = w8a16::launch_simt(g, plan, stream, flags, &err);
+    else if (plan.variant == W8A16_VARIANT_TC8)
+        rc = w8a16::launch_tc8(g, plan, stream, ts.ns, flags, &err);
     else
         rc = w8a16::launch_tc(g, plan, stream, ts.ns, flags, &err);
     if (rc) return fail(rc, err);
@@ -360,7 +397,7 @@ int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_for: NULL plan pointer");
     int rc = check_sizes(K, N, M, N, K);
     if (rc) return rc;
-    plan_core(M, N, K, sm_count, cluster_ctas, out);
+    plan_core(W8A16_VARIANT_AUTO, M, N, K, sm_count, cluster_ctas, out);
     return ok();
 }
 
@@ -377,16 +414,18 @@ int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t* out) {
     return ok();
 }
 
-int w8a16_cluster_capacity(uint32_t token_tile, uint32_t stages, uint32_t out[17]) {
+int w8a16_cluster_capacity(int32_t variant, uint32_t token_tile, uint32_t stages,
+                           uint32_t out[17]) {
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_cluster_capacity: NULL output");
-    if (!w8a16::tc_supported_stages(token_tile, stages))
-        return fail(W8A16_ERR_PLAN, "w8a16_cluster_capacity: no kernel instance for token_tile=" +
-                                        u(token_tile) + " stages=" + u(stages));
+    if (!is_tc_variant(variant) || !v_supported(variant, token_tile, stages))
+        return fail(W8A16_ERR_PLAN, "w8a16_cluster_capacity: no kernel instance for variant " +
+                                        std::to_string(variant) + " token_tile=" + u(token_tile) +
+                                        " stages=" + u(stages));
     DeviceInfo info;
     std::string err;
     int rc = current_device_info(&info, &err);
     if (rc) return fail(rc, err);
-    rc = live_capacity(token_tile, stages, out, &err);
+    rc = live_capacity(variant, token_tile, stages, out, &err);
     if (rc) return fail(rc, err);
     return ok();
 }
@@ -398,16 +437,15 @@ int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint
     if (rc) return rc;
     w8a16_plan_t p;
     if (variant == W8A16_VARIANT_AUTO) {
-        plan_core(M, N, K, sm_count, nullptr, &p);
+        plan_core(W8A16_VARIANT_AUTO, M, N, K, sm_count, nullptr, &p);
     } else if (variant == W8A16_VARIANT_SIMT) {
         fill_simt(M, N, &p);
-    } else if (variant == W8A16_VARIANT_TC) {
+    } else if (is_tc_variant(variant)) {
         w8a16_plan_t a;
-        plan_core(M, N, K, sm_count, nullptr, &a);
-        const uint32_t tn = a.token_tile;
+        plan_core(variant, M, N, K, sm_count, nullptr, &a);
         const uint32_t st = stages ? stages : a.stages;
         const uint32_t sp = split_k ? split_k : a.split_k;
-        fill_tc(M, N, tn, st, sp, &p);
+        fill_tc(variant, M, N, a.token_tile, st, sp, &p);
     } else {
         return fail(W8A16_ERR_PLAN, "w8a16_plan_variant: unknown variant " + std::to_string(variant));
     }
@@ -504,8 +542,11 @@ const char* w8a16_strerror(int code) {
 
 int w8a16_device_status(w8a16_stream_t stream, int clear, uint32_t* status, uint32_t* where,
                         uint32_t* detail) {
-    w8a16::StatusWord w{0, 0, 0};
-    const cudaError_t e = w8a16::tc_status_read(&w, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+    w8a16::StatusWord w{0, 0, 0}, w8{0, 0, 0};
+    cudaError_t e = w8a16::tc_status_read(&w, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess)
+        e = w8a16::tc8_status_read(&w8, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+    if (w.code == 0) w = w8;
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(W8A16_ERR_DEVICE, std::string("w8a16_device_status: ") + cudaGetErrorString(e));

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <string>
 
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
 #include "w8a16.h"
@@ -65,6 +66,25 @@ constexpr uint32_t tc_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
            tc_red_bytes(tn, split) + 1024u;
 }
 
+// FP8-datapath variant (TC8): E4M3 weights straight from the TMA ring into
+// kind::f8f6f4 MMAs, activations as two E4M3 terms (2 TN MMA columns).
+constexpr uint32_t tc8_act_stages(uint32_t tn) { return tn <= 32 ? 4u : 2u; }
+constexpr uint32_t tc8_b_stages(uint32_t tn) { return tn <= 32 ? 4u : 2u; }
+constexpr uint32_t tc8_p_bufs(uint32_t) { return 4u; }
+constexpr uint32_t tc8_split_warps(uint32_t tn) { return tn <= 32 ? 4u : 8u; }
+constexpr uint32_t tc8_fold_warps(uint32_t tn) { return tn <= 32 ? 4u : 8u; }
+constexpr uint32_t tc8_threads(uint32_t tn) {
+    return 96u + 32u * (tc8_split_warps(tn) + tc8_fold_warps(tn));
+}
+constexpr uint32_t tc8_tmem_cols(uint32_t tn) {
+    return tc8_p_bufs(tn) * 2u * tn <= 128u ? 128u : tc8_p_bufs(tn) * 2u * tn <= 256u ? 256u : 512u;
+}
+constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
+    return 1024u + stages * kTcRows * kKStep + tc8_b_stages(tn) * 2u * tn * kKStep +
+           tc8_act_stages(tn) * tn * kKStep * 2u + tc8_p_bufs(tn) * tn * 4u +
+           tc_red_bytes(tn, split) + 1024u;
+}
+
 // Kernel launchers (implemented in the kernel translation units). They assume
 // the arguments and plan were validated; they return a W8A16_* code and, on
 // failure, a message in *err.
@@ -76,10 +96,22 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
 // device when launched in clusters of `cluster` CTAs.
 int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
                         std::string* err);
+int launch_tc8(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+               uint32_t flags, std::string* err);
+int tc8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+                         std::string* err);
+bool tc8_supported_stages(uint32_t tn, uint32_t stages);
 int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, std::string* err);
 
-// Device status of the TC translation unit (the only one with waits).
+// TMA descriptors of W ([N][K] E4M3, 128x128 boxes) and A ([M][K] BF16 at the
+// caller's pitch, 64 x token_tile boxes), 128-byte swizzle; cached per device.
+bool tc_tensor_map_w(const GemmArgs& g, int device, CUtensorMap* out, std::string* err);
+bool tc_tensor_map_a(const GemmArgs& g, uint32_t token_tile, int device, CUtensorMap* out,
+                     std::string* err);
+
+// Device status of the translation units whose kernels wait.
 cudaError_t tc_status_read(StatusWord* out, bool clear, cudaStream_t s);
+cudaError_t tc8_status_read(StatusWord* out, bool clear, cudaStream_t s);
 
 bool tc_supported_token_tile(uint32_t tn);
 bool tc_supported_stages(uint32_t tn, uint32_t stages);

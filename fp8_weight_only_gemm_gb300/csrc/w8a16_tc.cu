@@ -625,6 +625,17 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
     return W8A16_OK;
 }
 
+bool tc_tensor_map_w(const GemmArgs& g, int device, CUtensorMap* out, std::string* err) {
+    return get_map({reinterpret_cast<uint64_t>(g.W), g.N, g.K, g.K, kTcRows, 0}, device, out, err);
+}
+
+bool tc_tensor_map_a(const GemmArgs& g, uint32_t token_tile, int device, CUtensorMap* out,
+                     std::string* err) {
+    return get_map({reinterpret_cast<uint64_t>(g.A), g.M, g.K, static_cast<uint64_t>(g.lda) * 2,
+                    token_tile, 1},
+                   device, out, err);
+}
+
 int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
                         std::string* err) {
     const int inst = find_instance(tn, stages);

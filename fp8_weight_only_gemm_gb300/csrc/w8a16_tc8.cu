@@ -1,0 +1,599 @@
+// FP8-datapath tensor-core W8A16 kernel for sm_103a (tcgen05.mma kind::f8f6f4 + TMA).
+//
+// Same operation, checks and reduction order as the BF16 tensor-core kernel
+// (page "metrale_model_layers/layers/ops/w8a16_gemm_pipelined_m32.rs": one
+// FP32 fold of the block scale per 128-K step, split-K partials added in step
+// order), with the E4M3 weights fed to the tensor core as they arrive:
+//
+//   * the weight tile TMA lands in shared memory (128 rows x 128 K, 128-byte
+//     swizzle) is the MMA's A operand as is: the tensor core decodes E4M3
+//     exactly, so there is no conversion work and no TMEM operand traffic, and
+//     one K=32 MMA covers twice the weights of a BF16 K=16 MMA;
+//   * each BF16 activation row of a 128-K block is written as two E4M3 terms,
+//     x = a * 2^(7-E) = hi + lo / 32 with E the exponent of the block's largest
+//     |a| (hi = e4m3_rne(x), lo = e4m3_rne(32 (x - hi))): exact for every a with
+//     |a| >= 2^-14 max|a|, and within 2^-22 max|a| otherwise. The two terms are
+//     the MMA's B rows [0, TN) and [TN, 2 TN), so one MMA of N = 2 TN computes
+//     both products;
+//   * the fold recombines them in FP32: acc += scale * 2^(E-7) * (P_hi + P_lo / 32).
+// A non-finite activation makes its token's outputs NaN (E4M3 has no infinity).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "w8a16_device.cuh"
+#include "w8a16_internal.h"
+
+namespace w8a16 {
+
+__device__ DeviceStatus g_tc8_status;
+
+namespace {
+
+constexpr uint32_t kWTileBytes = kTcRows * kKStep;   // 16 KiB of E4M3 per stage
+
+enum : uint32_t {
+    kWaitW = 11, kWaitX = 12, kWaitXEmpty = 13, kWaitB = 14, kWaitMdone = 15, kWaitPEmpty = 16,
+    kWaitDone = 17, kWaitDrain = 18, kWaitRed = 19
+};
+
+template <uint32_t TN, uint32_t STAGES>
+struct T8Cfg {
+    static constexpr uint32_t SA = tc8_act_stages(TN);     // BF16 activation staging ring
+    static constexpr uint32_t SB = tc8_b_stages(TN);       // E4M3 two-term activation ring
+    static constexpr uint32_t NP = tc8_p_bufs(TN);         // TMEM product buffers (2 TN cols)
+    static constexpr uint32_t NS = tc8_split_warps(TN);
+    static constexpr uint32_t NF = tc8_fold_warps(TN);
+    static constexpr uint32_t kThreads = tc8_threads(TN);
+    static constexpr uint32_t kTmemCols = tc8_tmem_cols(TN);
+    static constexpr uint32_t kXBytes = TN * kKStep * 2;
+    static constexpr uint32_t kBBytes = 2 * TN * kKStep;
+    static constexpr uint32_t kSplit0 = 3;                 // first splitter warp
+    static constexpr uint32_t kFold0 = kSplit0 + NS;       // first fold warp
+    static constexpr uint32_t kTokPerFold = TN * 4 / NF;
+    static constexpr uint32_t ND = STAGES > SB ? (STAGES > NP ? STAGES : NP) : (SB > NP ? SB : NP);
+    // barriers: wfull[S], xfull[SA], xempty[SA], bfull[SB], mdone[ND], pempty[NP], done, red
+    static constexpr uint32_t kNumBars = STAGES + 2 * SA + SB + ND + NP + 2;
+    static_assert(NP * 2 * TN <= kTmemCols, "TMEM budget");
+    static_assert(kTokPerFold % 16 == 0, "fold loads whole x16 column groups");
+    static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
+};
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, uint32_t remote_bar, float a) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr),
+        "f"(a), "r"(remote_bar)
+        : "memory");
+}
+// Generic-proxy shared-memory writes become visible to the tensor core's reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ bool warp_wait8(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                           volatile int* abort_flag, uint32_t detail) {
+    const bool ok = mbar_wait(bar, parity, deadline, abort_flag, &g_tc8_status, detail);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__device__ __forceinline__ uint32_t owned_row0(uint32_t r, uint32_t split_k) {
+    return r * kTcRows / split_k;
+}
+
+__device__ __forceinline__ void drain_ring8(uint32_t bar_base, uint32_t depth, uint32_t issued,
+                                            uint64_t timeout_ns) {
+    const uint64_t dl = globaltimer_ns() + timeout_ns;
+    for (uint32_t j = issued > depth ? issued - depth : 0; j < issued; ++j) {
+        volatile int never = 0;
+        mbar_wait(bar_base + 8u * (j % depth), (j / depth) & 1, dl, &never, &g_tc8_status, kWaitDrain);
+    }
+}
+
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B, FP32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two FP32 values to E4M3 (round to nearest even, saturating): lo in byte 0.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Two E4M3 codes (byte 0 and 1) back to FP32.
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float& hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(codes)));
+    const __half2 v = *reinterpret_cast<const __half2*>(&h2);
+    lo = __low2float(v);
+    hi = __high2float(v);
+}
+
+template <uint32_t TN, uint32_t STAGES>
+__global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
+    w8a16_tc8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                     const float* __restrict__ scale, __nv_bfloat16* __restrict__ C, uint32_t ldc,
+                     uint32_t M, uint32_t N, uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
+    using Cfg = T8Cfg<TN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sW = smem;                                   // STAGES x 16 KiB E4M3 weights
+    uint8_t* sB = sW + STAGES * kWTileBytes;              // SB x 2TN x 128 E4M3 activation terms
+    uint8_t* sX = sB + Cfg::SB * Cfg::kBBytes;            // SA x TN x 128 BF16 activations
+    float* sInv = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kXBytes);   // NP x TN factors
+    float* sRed = sInv + Cfg::NP * TN;                    // split-K receive slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sRed) +
+                                                 tc_red_bytes(TN, split_k));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    // mdone[i % ND] completes when the MMAs of step i have: it frees weight slot
+    // i % STAGES and term slot i % SB, and fills product buffer i % NP.
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t wfull0 = bar0;
+    const uint32_t xfull0 = wfull0 + 8u * STAGES, xempty0 = xfull0 + 8u * Cfg::SA;
+    const uint32_t bfull0 = xempty0 + 8u * Cfg::SA;
+    const uint32_t mdone0 = bfull0 + 8u * Cfg::SB;
+    const uint32_t pempty0 = mdone0 + 8u * Cfg::ND;
+    const uint32_t done_bar = pempty0 + 8u * Cfg::NP;
+    const uint32_t red_bar = done_bar + 8u;
+
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t tile = blockIdx.x / split_k;
+    const uint32_t rank = blockIdx.x % split_k;
+    const uint32_t token0 = blockIdx.y * TN;
+    const uint32_t ksteps = K / kKStep;
+    const uint32_t s_begin = static_cast<uint32_t>(static_cast<uint64_t>(rank) * ksteps / split_k);
+    const uint32_t s_end = static_cast<uint32_t>(static_cast<uint64_t>(rank + 1) * ksteps / split_k);
+    const uint32_t nsteps = s_end - s_begin;
+    const uint64_t deadline = globaltimer_ns() + timeout_ns;
+    const uint32_t my_row0 = owned_row0(rank, split_k);
+    const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
+    const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
+    const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
+    const uint32_t toks_valid = min(TN, M - token0);
+
+    if (warp == 0) {
+        for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
+            const uint32_t addr = bar0 + 8u * b;
+            uint32_t count = 1;
+            if (addr >= xempty0 && addr < mdone0) count = Cfg::NS;          // splitters
+            else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;   // fold warps
+            mbar_init(addr, count);
+        }
+        if (lane == 0) *abort_flag = 0;
+        fence_barrier_init();
+        __syncwarp();
+    }
+    if (threadIdx.x == 0) {
+        if (split_k > 1) mbar_arrive_expect_tx(red_bar, split_k * my_rows * TN * 4u);
+        // First weight tiles before anything else; weights are requested before
+        // waiting on the previous grid (under a programmatic launch the caller
+        // guarantees that grid does not write W).
+        const uint64_t pol_w = l2_policy_evict_first();
+        for (uint32_t i = 0; i < npre; ++i) {
+            mbar_arrive_expect_tx(wfull0 + 8u * i, kWTileBytes);
+            tma_load_2d(smem_u32(sW + i * kWTileBytes), &tmW, wfull0 + 8u * i,
+                        static_cast<int32_t>((s_begin + i) * kKStep),
+                        static_cast<int32_t>(tile * kTcRows), pol_w);
+        }
+        tma_prefetch_desc(&tmA);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (split_k > 1) cluster_arrive();
+    if (threadIdx.x == 0) grid_launch_dependents();
+    const uint32_t tP = *tmem_slot;                 // NP x 2TN columns: FP32 products
+    const uint32_t quarter = warp & 3;
+    const uint32_t row = quarter * 32 + lane;
+    const uint32_t lane_bits = (quarter * 32) << 16;
+    const bool is_split = warp >= Cfg::kSplit0 && warp < Cfg::kFold0;
+    const bool is_fold = warp >= Cfg::kFold0;
+
+    if (warp == 0) {
+        // ------------------------------------------------ weight producer (TMA)
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            uint32_t issued = npre;
+            for (uint32_t i = npre; i < nsteps; ++i) {
+                const uint32_t s = i % STAGES, q = i - STAGES;   // slot s last held step q
+                if (!mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline, abort_flag,
+                               &g_tc8_status, kWaitMdone))
+                    break;
+                mbar_arrive_expect_tx(wfull0 + 8u * s, kWTileBytes);
+                tma_load_2d(smem_u32(sW + s * kWTileBytes), &tmW, wfull0 + 8u * s,
+                            static_cast<int32_t>((s_begin + i) * kKStep),
+                            static_cast<int32_t>(tile * kTcRows), pol_w);
+                issued = i + 1;
+            }
+            drain_ring8(wfull0, STAGES, issued, timeout_ns);
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------- activation producer (TMA)
+        if (lane == 0) {
+            const uint64_t pol_a = l2_policy_evict_last();
+            grid_dependency_wait();   // A may be written by the previous grid in the stream
+            uint32_t issued = 0;
+            for (uint32_t i = 0; i < nsteps; ++i) {
+                const uint32_t j = i % Cfg::SA;
+                if (i >= Cfg::SA && !mbar_wait(xempty0 + 8u * j, ((i / Cfg::SA) - 1) & 1, deadline,
+                                               abort_flag, &g_tc8_status, kWaitXEmpty))
+                    break;
+                mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kXBytes);
+                const int32_t k = static_cast<int32_t>((s_begin + i) * kKStep);
+                const uint32_t dst = smem_u32(sX + j * Cfg::kXBytes);
+                tma_load_2d(dst, &tmA, xfull0 + 8u * j, k, static_cast<int32_t>(token0), pol_a);
+                tma_load_2d(dst + TN * 128, &tmA, xfull0 + 8u * j, k + 64,
+                            static_cast<int32_t>(token0), pol_a);
+                issued = i + 1;
+            }
+            drain_ring8(xfull0, Cfg::SA, issued, timeout_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, 2 * TN);
+            for (uint32_t i = 0; i < nsteps; ++i) {
+                const uint32_t s = i % STAGES, b = i % Cfg::SB, p = i % Cfg::NP;
+                if (!mbar_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, &g_tc8_status,
+                               kWaitW))
+                    break;
+                if (!mbar_wait(bfull0 + 8u * b, (i / Cfg::SB) & 1, deadline, abort_flag,
+                               &g_tc8_status, kWaitB))
+                    break;
+                if (i >= Cfg::NP && !mbar_wait(pempty0 + 8u * p, ((i / Cfg::NP) - 1) & 1, deadline,
+                                               abort_flag, &g_tc8_status, kWaitPEmpty))
+                    break;
+                tc_fence_after();
+                const uint32_t wa = smem_u32(sW + s * kWTileBytes);
+                const uint32_t ba = smem_u32(sB + b * Cfg::kBBytes);
+#pragma unroll
+                for (uint32_t kk = 0; kk < kKStep / 32; ++kk)
+                    tc_mma_ss_f8(tP + p * 2 * TN, smem_desc_kmajor_sw128(wa + kk * 32),
+                                 smem_desc_kmajor_sw128(ba + kk * 32), idesc, kk > 0);
+                tc_commit(mdone0 + 8u * (i % Cfg::ND));
+            }
+            tc_commit(done_bar);
+            volatile int never = 0;
+            mbar_wait(done_bar, 0, globaltimer_ns() + timeout_ns, &never, &g_tc8_status, kWaitDone);
+        }
+    } else if (is_split) {
+        // ---------------- splitters: BF16 activations -> two E4M3 terms per value
+        // Work item = (token, group of 4 consecutive K); a token's 32 groups are
+        // the 32 lanes of one warp, which reduce the token's block maximum.
+        const uint32_t sw = warp - Cfg::kSplit0;
+        for (uint32_t i = 0; i < nsteps; ++i) {
+            const uint32_t j = i % Cfg::SA, b = i % Cfg::SB, f = i % Cfg::NP;
+            if (!warp_wait8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
+            if (i >= Cfg::SB) {   // term slot b last held step i - SB
+                const uint32_t q = i - Cfg::SB;
+                if (!warp_wait8(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline, abort_flag,
+                                kWaitMdone))
+                    break;
+            }
+            if (i >= Cfg::NP && !warp_wait8(pempty0 + 8u * f, ((i / Cfg::NP) - 1) & 1, deadline,
+                                            abort_flag, kWaitPEmpty))
+                break;   // factor slot f is read by the fold of step i - NP
+            const uint8_t* xs = sX + j * Cfg::kXBytes;
+            uint8_t* bs = sB + b * Cfg::kBBytes;
+            for (uint32_t t = sw; t < toks_valid; t += Cfg::NS) {
+                // K group 4*lane.. of token t: BF16 box lane / 16, 16-byte chunk
+                // (lane % 16) / 2 of row t (swizzled), 8-byte half lane % 2
+                const uint32_t g = lane & 15;
+                const uint8_t* xr = xs + (lane >> 4) * (TN * 128) + t * 128;
+                const uint2 av = *reinterpret_cast<const uint2*>(
+                    xr + (((g >> 1) ^ (t & 7)) << 4) + ((g & 1) << 3));
+                float v[4] = {__uint_as_float(av.x << 16), __uint_as_float(av.x & 0xFFFF0000u),
+                              __uint_as_float(av.y << 16), __uint_as_float(av.y & 0xFFFF0000u)};
+                float mx = 0.f;
+                bool bad = false;
+#pragma unroll
+                for (uint32_t e = 0; e < 4; ++e) {
+                    const float a = fabsf(v[e]);
+                    if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
+                    else bad = true;       // NaN or infinity
+                }
+#pragma unroll
+                for (uint32_t o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                // E = floor(log2(mx)) from the bits (mx may be a subnormal)
+                const uint32_t mb = __float_as_uint(mx);
+                const int ef = static_cast<int>(mb >> 23);
+                const int E = ef != 0 ? ef - 127 : (mb != 0 ? -118 - __clz(mb) : 0);
+                // x = a * 2^(7 - E) in two exact power-of-two steps (7 - E in -120..156)
+                const int e1 = (7 - E) / 2, e2 = (7 - E) - e1;
+                const float p1 = __int_as_float((127 + e1) << 23), p2 = __int_as_float((127 + e2) << 23);
+                float x[4];
+#pragma unroll
+                for (uint32_t e = 0; e < 4; ++e) x[e] = (v[e] * p1) * p2;
+                const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
+                float hf[4];
+                e4m3x2_to_f32x2(h01, hf[0], hf[1]);
+                e4m3x2_to_f32x2(h23, hf[2], hf[3]);
+                const uint32_t l01 = f32x2_to_e4m3x2((x[0] - hf[0]) * 32.f, (x[1] - hf[1]) * 32.f);
+                const uint32_t l23 = f32x2_to_e4m3x2((x[2] - hf[2]) * 32.f, (x[3] - hf[3]) * 32.f);
+                uint32_t hw = h01 | (h23 << 16);
+                const uint32_t lw = l01 | (l23 << 16);
+                if (bad) hw = 0x7F7F7F7Fu;   // a non-finite value: NaN codes
+                // E4M3 row t (hi) and TN + t (lo): 4 bytes at K 4*lane of the 128-byte
+                // row, i.e. chunk lane / 4 (swizzled), byte (lane % 4) * 4
+                const uint32_t pos = (((lane >> 2) ^ (t & 7)) << 4) + ((lane & 3) << 2);
+                *reinterpret_cast<uint32_t*>(bs + t * 128 + pos) = hw;
+                *reinterpret_cast<uint32_t*>(bs + (TN + t) * 128 + pos) = lw;
+                if (lane == 0) {
+                    // 2^(E-7) as FP32 (subnormal or zero for very small blocks)
+                    const int ie = E - 7;
+                    float inv = 0.f;
+                    if (mx > 0.f)
+                        inv = ie >= -126 ? __int_as_float((127 + ie) << 23)
+                                         : (ie >= -149 ? __int_as_float(1 << (ie + 149)) : 0.f);
+                    sInv[f * TN + t] = inv;
+                }
+            }
+            fence_proxy_async_smem();   // the tensor core reads these terms
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(xempty0 + 8u * j);
+                mbar_arrive(bfull0 + 8u * b);
+            }
+        }
+    } else if (is_fold) {
+        // --------- fold: acc += scale * 2^(E-7) * (P_hi + P_lo / 32) per token
+        const uint32_t fh = (warp - Cfg::kFold0) >> 2;
+        float acc[Cfg::kTokPerFold];
+#pragma unroll
+        for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) acc[t] = 0.f;
+        const float* srow = scale + static_cast<size_t>(tile) * ksteps + s_begin;
+        for (uint32_t i = 0; i < nsteps; ++i) {
+            const uint32_t p = i % Cfg::NP;
+            if (!warp_wait8(mdone0 + 8u * (i % Cfg::ND), (i / Cfg::ND) & 1, deadline, abort_flag,
+                            kWaitMdone))
+                break;
+            tc_fence_after();
+            const float sc = __ldg(srow + i);
+            const uint32_t pcol = tP + lane_bits + p * 2 * TN + fh * Cfg::kTokPerFold;
+            const float* inv = sInv + p * TN + fh * Cfg::kTokPerFold;
+#pragma unroll
+            for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
+                float vh[16], vl[16];
+                tmem_ld_32x32b_x16(pcol + c, vh);
+                tmem_ld_32x32b_x16(pcol + TN + c, vl);
+                tc_wait_ld();
+#pragma unroll
+                for (uint32_t t = 0; t < 16; ++t) {
+                    const float pt = fmaf(vl[t], 0.03125f, vh[t]) * inv[c + t];
+                    acc[c + t] = fmaf(sc, pt, acc[c + t]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pempty0 + 8u * p);
+        }
+        if (split_k == 1) {
+            if (row < rows_valid) {
+                const uint32_t n = tile * kTcRows + row;
+#pragma unroll
+                for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) {
+                    const uint32_t m = fh * Cfg::kTokPerFold + t;
+                    if (m < toks_valid)
+                        C[static_cast<size_t>(token0 + m) * ldc + n] = __float2bfloat16_rn(acc[t]);
+                }
+            }
+        } else {
+            cluster_wait();
+            uint32_t owner = 0;
+            while (owner + 1 < split_k && owned_row0(owner + 1, split_k) <= row) ++owner;
+            const uint32_t lrow = row - owned_row0(owner, split_k);
+            const uint32_t off =
+                ((rank * TN + fh * Cfg::kTokPerFold) * tc_red_rows(split_k) + lrow) * 4u;
+            const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
+            const uint32_t dbar = dsmem_map(red_bar, owner);
+#pragma unroll
+            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)
+                st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tP, Cfg::kTmemCols);
+    }
+    if (split_k == 1) return;
+
+    const bool got = warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+    if (got) {
+        const uint32_t total = my_rows * toks_valid;
+        for (uint32_t idx = threadIdx.x; idx < total; idx += Cfg::kThreads) {
+            const uint32_t tok = idx / my_rows, lr = idx % my_rows;
+            const uint32_t r = my_row0 + lr;
+            if (r >= rows_valid) continue;
+            float v = 0.f;
+            for (uint32_t src = 0; src < split_k; ++src)
+                v += sRed[(src * TN + tok) * tc_red_rows(split_k) + lr];
+            C[static_cast<size_t>(token0 + tok) * ldc + tile * kTcRows + r] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
+using Tc8KernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*, uint32_t,
+                             uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+struct Tc8Instance {
+    uint32_t tn, stages;
+    Tc8KernelFn fn;
+};
+#define W8A16_TC8_INST(TN_, ST_) {TN_, ST_, &w8a16_tc8_kernel<TN_, ST_>}
+const Tc8Instance kTc8Instances[] = {
+    W8A16_TC8_INST(16, 4), W8A16_TC8_INST(16, 6), W8A16_TC8_INST(16, 8),
+    W8A16_TC8_INST(32, 4), W8A16_TC8_INST(32, 6), W8A16_TC8_INST(32, 8),
+    W8A16_TC8_INST(64, 4), W8A16_TC8_INST(64, 6),
+};
+#undef W8A16_TC8_INST
+constexpr int kNumTc8 = sizeof(kTc8Instances) / sizeof(kTc8Instances[0]);
+
+int find_tc8(uint32_t tn, uint32_t stages) {
+    for (int i = 0; i < kNumTc8; ++i)
+        if (kTc8Instances[i].tn == tn && kTc8Instances[i].stages == stages) return i;
+    return -1;
+}
+
+cudaError_t ensure_attributes8(int inst, int device) {
+    static std::mutex mu;
+    static bool done[64][kNumTc8] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (done[device][inst]) return cudaSuccess;
+    const Tc8Instance& k = kTc8Instances[inst];
+    uint32_t most = 0;
+    for (uint32_t sp = 1; sp <= 16; ++sp) {
+        const uint32_t b = tc8_smem_bytes(k.tn, k.stages, sp);
+        if (b <= kMaxDynSmem && b > most) most = b;
+    }
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(most));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) done[device][inst] = true;
+    return e;
+}
+
+}  // namespace
+
+bool tc8_supported_stages(uint32_t tn, uint32_t stages) { return find_tc8(tn, stages) >= 0; }
+
+int launch_tc8(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+               uint32_t flags, std::string* err) {
+    const int inst = find_tc8(p.token_tile, p.stages);
+    if (inst < 0) {
+        *err = "no TC8 kernel instance for token_tile=" + std::to_string(p.token_tile) +
+               " stages=" + std::to_string(p.stages);
+        return W8A16_ERR_PLAN;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = ensure_attributes8(inst, dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("TC8 kernel attribute setup failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    CUtensorMap mw, ma;
+    if (!tc_tensor_map_w(g, dev, &mw, err) || !tc_tensor_map_a(g, p.token_tile, dev, &ma, err))
+        return W8A16_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
+    cfg.blockDim = dim3(tc8_threads(p.token_tile), 1, 1);
+    cfg.dynamicSmemBytes = tc8_smem_bytes(p.token_tile, p.stages, p.split_k);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.split_k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kTc8Instances[inst].fn, mw, ma, g.scale,
+                           static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, p.split_k,
+                           timeout_ns);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("TC8 kernel launch failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    return W8A16_OK;
+}
+
+int tc8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+                         std::string* err) {
+    const int inst = find_tc8(tn, stages);
+    if (inst < 0 || cluster < 1 || cluster > 16) {
+        *err = "no TC8 kernel instance, or cluster size outside 1..16";
+        return W8A16_ERR_PLAN;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = ensure_attributes8(inst, dev);
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(cluster * 64, 1, 1);
+    cfg.blockDim = dim3(tc8_threads(tn), 1, 1);
+    cfg.dynamicSmemBytes = tc8_smem_bytes(tn, stages, cluster);
+    if (cfg.dynamicSmemBytes > kMaxDynSmem) {
+        *ctas = 0;
+        return W8A16_OK;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kTc8Instances[inst].fn),
+                                           &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("cudaOccupancyMaxActiveClusters failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_DEVICE;
+    }
+    *ctas = static_cast<uint32_t>(n) * cluster;
+    return W8A16_OK;
+}
+
+cudaError_t tc8_status_read(StatusWord* out, bool clear, cudaStream_t s) {
+    DeviceStatus st;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&st, g_tc8_status, sizeof st, 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    out->code = st.code;
+    out->where = st.where;
+    out->detail = st.detail;
+    if (clear) {
+        const DeviceStatus zero{0, 0, 0};
+        e = cudaMemcpyToSymbolAsync(g_tc8_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
+}  // namespace w8a16

@@ -92,8 +92,13 @@ enum {
 enum {
     W8A16_VARIANT_AUTO = 0,  /* the planner's choice (w8a16_plan) */
     W8A16_VARIANT_SIMT = 1,  /* CUDA-core kernel: one warp per weight row, no tensor cores */
-    W8A16_VARIANT_TC = 2     /* TMA weight ring + in-register E4M3->BF16 + tcgen05 MMA
+    W8A16_VARIANT_TC = 2,    /* TMA weight ring + in-register E4M3->BF16 + tcgen05 MMA
                                 (weight rows = MMA M, tokens = MMA N), cluster split-K */
+    W8A16_VARIANT_TC8 = 3    /* FP8 tensor datapath: the E4M3 weight tiles feed tcgen05
+                                kind::f8f6f4 MMAs as loaded; each BF16 activation enters
+                                as two E4M3 terms (exact for |a| >= 2^-14 of its token's
+                                128-K block maximum, within 2^-22 of it otherwise); a
+                                non-finite activation makes its token's outputs NaN */
 };
 
 /*
@@ -176,9 +181,10 @@ W8A16_API int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_cou
 /* The plan w8a16_gemm uses for (M, N, K) on the current device. */
 W8A16_API int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t *out);
 
-/* Co-resident CTAs of the TC kernel for a token tile and stage count on the
- * current device, per cluster size: out[s] for s = 1..16 (out[0] = 0). */
-W8A16_API int w8a16_cluster_capacity(uint32_t token_tile, uint32_t stages, uint32_t out[17]);
+/* Co-resident CTAs of a tensor-core variant's kernel for a token tile and stage
+ * count on the current device, per cluster size: out[s] for s = 1..16 (out[0] = 0). */
+W8A16_API int w8a16_cluster_capacity(int32_t variant, uint32_t token_tile, uint32_t stages,
+                                     uint32_t out[17]);
 
 /* Build the plan for an explicit variant / split / stage count (0 = planner's
  * choice for that field). Returns W8A16_ERR_PLAN if it cannot run this shape. */

@@ -10,7 +10,11 @@ Tolerances:
     GPU's FP32 value differs from the exact sum by at most
         (K/128 + 256 + split_k) * 2^-23 * sum_k |A * W * scale|
     (tensor-core step sums, one fold per step, the cluster reduction), and
-    rounding to BF16 adds half an ulp of the result.
+    rounding to BF16 adds half an ulp of the result. The FP8-datapath variant
+    (TC8) represents each activation as two E4M3 terms, exact for values at
+    least 2^-14 of their 128-K block maximum and within 2^-22 of it otherwise,
+    which adds at most 2^-22 * max|A[m, :]| * sum_k |W[n, k] * scale| (the
+    tests allow twice that).
 """
 from __future__ import annotations
 
@@ -56,7 +60,7 @@ def oracle_full(case: workloads.Case):
 
 def stated_tolerance(case: workloads.Case, ref: np.ndarray) -> np.ndarray:
     wl = case.wl
-    a = case.A[:, :wl.K].to(torch.float64).abs().max().item()
+    a = case.A[:, :wl.K].to(torch.float64).abs().nan_to_num(0.0, posinf=0.0).max().item()
     w = case.W.view(torch.float8_e4m3fn).to(torch.float64).abs().nan_to_num(0.0)
     s = case.scale.to(torch.float64)
     nb = s.shape[0]
@@ -67,8 +71,19 @@ def stated_tolerance(case: workloads.Case, ref: np.ndarray) -> np.ndarray:
     return 2.0 ** -7 * np.abs(ref) + 1e-3 * math.sqrt(wl.K) * a * ws
 
 
+def split_term_bound(case: workloads.Case) -> np.ndarray:
+    """2^-21 * max_k |A[m, k]| * sum_k |W[n, k] * scale|  ([M, N])."""
+    wl = case.wl
+    a = case.A[:, :wl.K].to(torch.float64).abs().nan_to_num(0.0, posinf=0.0).amax(dim=1).numpy()
+    w = case.W.view(torch.float8_e4m3fn).to(torch.float64).abs().nan_to_num(0.0)
+    s = case.scale.to(torch.float64).repeat_interleave(128, dim=0)[:wl.N]
+    s = s.repeat_interleave(128, dim=1)
+    wabs = (w * s).sum(dim=1).numpy()
+    return 2.0 ** -21 * a[:, None] * wabs[None, :]
+
+
 def compare(case: workloads.Case, got: np.ndarray, ref_C: np.ndarray, exact: np.ndarray,
-            absum: np.ndarray, split_k: int = 1, label: str = ""):
+            absum: np.ndarray, split_k: int = 1, label: str = "", variant: int = 2):
     """Element-by-element comparison of a GPU result with the oracle; asserts."""
     wl = case.wl
     M, N = wl.M, wl.N
@@ -87,7 +102,8 @@ def compare(case: workloads.Case, got: np.ndarray, ref_C: np.ndarray, exact: np.
     assert not bad.any(), (f"{label}: {bad.sum()} outputs outside the stated tolerance; first at "
                            f"{np.argwhere(bad)[0]}: gpu={g[bad][0]} ref={r[bad][0]} tol={tol[bad][0]}")
     gamma = (wl.K / 128 + 256 + split_k) * 2.0 ** -23
-    tight = gamma * absum + 0.5 * ulp_bf16(np.abs(exact) + gamma * absum) + 2.0 ** -133
+    extra = split_term_bound(case) if variant == 3 else 0.0
+    tight = gamma * absum + extra + 0.5 * ulp_bf16(np.abs(exact) + gamma * absum + extra) + 2.0 ** -133
     err2 = np.abs(g - exact)
     bad2 = fin & ~(err2 <= tight)
     assert not bad2.any(), (f"{label}: {bad2.sum()} outputs outside the arithmetic error bound; first "

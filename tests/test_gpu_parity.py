@@ -31,6 +31,9 @@ def _plan(M, N, K, variant, split_k=0, stages=0):
     return binding.plan_variant(M, N, K, variant, split_k, stages, sms)
 
 
+TC_VARIANTS = [2, 3]   # BF16 datapath, FP8 datapath
+
+
 @pytest.mark.parametrize("name", workloads.CONFIG_ORDER)
 def test_workload_auto_plan(name):
     case = workloads.make_case(name)
@@ -38,10 +41,20 @@ def test_workload_auto_plan(name):
     ref, exact, absum = oracle_full(case)
     from fp8_weight_only_gemm_gb300 import binding
     wl = case.wl
-    p = binding.plan_for(wl.M, wl.N, wl.K, torch.cuda.get_device_properties(0).multi_processor_count)
-    compare(case, got, ref, exact, absum, split_k=p["split_k"], label=name)
+    p = binding.plan_current(wl.M, wl.N, wl.K)
+    compare(case, got, ref, exact, absum, split_k=p["split_k"], label=name, variant=p["variant"])
     # every output of the used region was written (no sentinel left)
     assert not np.any(got.reshape(wl.M, wl.ldc)[:, :wl.N] == workloads.C_USED_SENTINEL)
+
+
+@pytest.mark.parametrize("variant", TC_VARIANTS)
+@pytest.mark.parametrize("name", workloads.CONFIG_ORDER[:4])
+def test_workload_each_tc_variant(name, variant):
+    case = workloads.make_case(name)
+    wl = case.wl
+    got = run_gpu(case, plan=_plan(wl.M, wl.N, wl.K, variant))
+    ref, exact, absum = oracle_full(case)
+    compare(case, got, ref, exact, absum, split_k=16, label=f"{name}/v{variant}", variant=variant)
 
 
 @pytest.mark.parametrize("name", workloads.CONFIG_ORDER[:4])
@@ -54,32 +67,35 @@ def test_workload_simt_variant(name):
     compare(case, got, ref, exact, absum, label=name + "/simt")
 
 
+@pytest.mark.parametrize("variant", TC_VARIANTS)
 @pytest.mark.parametrize("split_k", [1, 2, 3, 5, 8, 13, 16])
 @pytest.mark.parametrize("M", [1, 8, 32])
-def test_forced_splits(split_k, M):
-    from fp8_weight_only_gemm_gb300 import binding
+def test_forced_splits(split_k, M, variant):
     case = workloads.make_case("decode_gemv_m1_n4096_k4096", M=M, N=640, K=2048, seed=100 + M)
     wl = case.wl
-    p = _plan(wl.M, wl.N, wl.K, binding.VARIANT_TC, split_k=split_k)
+    p = _plan(wl.M, wl.N, wl.K, variant, split_k=split_k)
     got = run_gpu(case, plan=p)
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=split_k, label=f"split{split_k}/M{M}")
+    compare(case, got, ref, exact, absum, split_k=split_k, label=f"split{split_k}/M{M}/v{variant}",
+            variant=variant)
     again = run_gpu(case, plan=p)
     assert np.array_equal(got, again), "same plan, different bits: not deterministic"
 
 
-@pytest.mark.parametrize("M,stages,split", [(4, 4, 2), (4, 6, 2), (4, 8, 2), (4, 10, 3), (24, 3, 2),
-                                            (24, 4, 2), (24, 6, 2), (24, 8, 3), (48, 4, 2),
-                                            (48, 6, 2), (48, 8, 3), (100, 4, 2), (100, 6, 1),
-                                            (100, 6, 2)])
-def test_stage_instances(M, stages, split):
-    from fp8_weight_only_gemm_gb300 import binding
+@pytest.mark.parametrize("variant,M,stages,split", [
+    (2, 4, 4, 2), (2, 4, 6, 2), (2, 4, 8, 2), (2, 4, 10, 3), (2, 24, 3, 2), (2, 24, 4, 2),
+    (2, 24, 6, 2), (2, 24, 8, 3), (2, 48, 4, 2), (2, 48, 6, 2), (2, 48, 8, 3), (2, 100, 4, 2),
+    (2, 100, 6, 1), (2, 100, 6, 2),
+    (3, 4, 4, 2), (3, 4, 6, 2), (3, 4, 8, 3), (3, 24, 4, 2), (3, 24, 6, 2), (3, 24, 8, 3),
+    (3, 48, 4, 2), (3, 48, 6, 3)])
+def test_stage_instances(variant, M, stages, split):
     case = workloads.make_case("decode_gemv_m1_n4096_k4096", M=M, N=384, K=1536, seed=200 + M)
     wl = case.wl
-    p = _plan(wl.M, wl.N, wl.K, binding.VARIANT_TC, split_k=split, stages=stages)
+    p = _plan(wl.M, wl.N, wl.K, variant, split_k=split, stages=stages)
     got = run_gpu(case, plan=p)
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=split, label=f"stages{stages}/M{M}")
+    compare(case, got, ref, exact, absum, split_k=split, label=f"v{variant}/stages{stages}/M{M}",
+            variant=variant)
 
 
 @pytest.mark.parametrize("M,N,K,lda,ldc", [
@@ -88,41 +104,75 @@ def test_stage_instances(M, stages, split):
     (64, 130, 256, 256, 131), (65, 257, 384, 384, 257), (127, 64, 256, 264, 64),
     (129, 300, 256, 256, 300), (200, 129, 128, 136, 133), (257, 128, 256, 256, 128),
 ])
-def test_edge_shapes(M, N, K, lda, ldc):
+@pytest.mark.parametrize("variant", [0, 2, 3])
+def test_edge_shapes(M, N, K, lda, ldc, variant):
     case = workloads.make_case("tiny_m1_n256_k256", M=M, N=N, K=K, a_row_stride=lda,
                                c_row_stride=ldc, seed=M * 1000 + N)
-    got = run_gpu(case)
+    plan = None if variant == 0 else _plan(M, N, K, variant)
+    got = run_gpu(case, plan=plan)
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=16, label=f"edge M{M} N{N} K{K}")
+    v = variant or __import__("fp8_weight_only_gemm_gb300").plan_current(M, N, K)["variant"]
+    compare(case, got, ref, exact, absum, split_k=16, label=f"edge M{M} N{N} K{K} v{variant}",
+            variant=v)
 
 
+@pytest.mark.parametrize("variant", TC_VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(3, 256, 512), (20, 384, 1024)])
-def test_every_code_and_scale_range(M, N, K):
+def test_every_code_and_scale_range(M, N, K, variant):
     """Uniform codes (subnormals, +-448, -0 included) under log-uniform scales."""
     case = workloads.random_codes_case(M, N, K, seed=M + N + K)
-    got = run_gpu(case)
+    got = run_gpu(case, plan=_plan(M, N, K, variant))
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=16, label="all-codes")
+    compare(case, got, ref, exact, absum, split_k=16, label=f"all-codes/v{variant}", variant=variant)
 
 
-def test_nan_weight_code_propagates():
+@pytest.mark.parametrize("variant", TC_VARIANTS)
+def test_nan_weight_code_propagates(variant):
     case = workloads.make_case("tiny_m1_n256_k256", M=5, N=256, K=384, seed=77)
     case.W[3, 200] = 0x7F
     case.W[130, 5] = 0xFF
-    got = run_gpu(case)
+    got = run_gpu(case, plan=_plan(5, 256, 384, variant))
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=16, label="nan")
+    compare(case, got, ref, exact, absum, split_k=16, label=f"nan/v{variant}", variant=variant)
     g = got.reshape(5, 256)
     isnan = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
     assert isnan[:, 3].all() and isnan[:, 130].all() and isnan.sum() == 10
 
 
-def test_zero_block_and_zero_scale():
+@pytest.mark.parametrize("variant", TC_VARIANTS)
+def test_nan_activation_propagates(variant):
+    case = workloads.make_case("tiny_m1_n256_k256", M=6, N=256, K=384, seed=78)
+    A = case.A.clone()
+    A[2, 300] = float("nan")
+    case.A = A
+    got = run_gpu(case, plan=_plan(6, 256, 384, variant))
+    ref, exact, absum = oracle_full(case)
+    compare(case, got, ref, exact, absum, split_k=16, label=f"nan-a/v{variant}", variant=variant)
+    g = got.reshape(6, 256)
+    isnan = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
+    assert isnan[2].all() and isnan.sum() == 256
+
+
+@pytest.mark.parametrize("variant", TC_VARIANTS)
+def test_activation_dynamic_range(variant):
+    """Activations spread over 2^+-40 within each 128-K block (tiny values next to
+    large ones): exact on the BF16 datapath, within the two-term bound on TC8."""
+    case = workloads.make_case("tiny_m1_n256_k256", M=7, N=384, K=768, seed=79)
+    g = torch.Generator().manual_seed(80)
+    e = torch.randint(-40, 40, case.A.shape, generator=g).to(torch.float32)
+    case.A = (case.A.float() * torch.pow(2.0, e)).to(torch.bfloat16)
+    got = run_gpu(case, plan=_plan(7, 384, 768, variant))
+    ref, exact, absum = oracle_full(case)
+    compare(case, got, ref, exact, absum, split_k=16, label=f"range/v{variant}", variant=variant)
+
+
+@pytest.mark.parametrize("variant", TC_VARIANTS)
+def test_zero_block_and_zero_scale(variant):
     case = workloads.make_case("skinny_qkv_m8_n12288_k4096", N=512, K=1024, zero_blocks=((2, 3),))
     assert float(case.scale[2, 3]) == 0.0
-    got = run_gpu(case)
+    got = run_gpu(case, plan=_plan(8, 512, 1024, variant))
     ref, exact, absum = oracle_full(case)
-    compare(case, got, ref, exact, absum, split_k=16, label="zero-block")
+    compare(case, got, ref, exact, absum, split_k=16, label=f"zero-block/v{variant}", variant=variant)
 
 
 def test_host_buffer_entry_point_matches_device_path():
@@ -198,4 +248,5 @@ def test_live_plan_and_capacity():
     cap = w8.cluster_capacity(16, 4)
     assert cap[0] == 0 and cap[1] >= torch.cuda.get_device_properties(0).multi_processor_count
     p = w8.plan_current(1, 4096, 4096)
+    cap = w8.cluster_capacity(p["token_tile"], p["stages"], p["variant"])
     assert p["grid"][0] * p["grid"][1] <= cap[p["split_k"]], (p, cap)

@@ -32,6 +32,7 @@ def test_header_constants_match_binding():
         return int(re.search(rf"{name}\s*=\s*(-?\d+)", text).group(1))
     assert val("W8A16_VARIANT_SIMT") == binding.VARIANT_SIMT
     assert val("W8A16_VARIANT_TC") == binding.VARIANT_TC
+    assert val("W8A16_VARIANT_TC8") == binding.VARIANT_TC8
     assert val("W8A16_STATUS_WAIT_TIMEOUT") == binding.STATUS_WAIT_TIMEOUT
     assert int(re.search(r"W8A16_FLAG_PDL\s*=\s*(\d+)u", text).group(1)) == binding.FLAG_PDL
 
@@ -100,14 +101,17 @@ def test_strerror_covers_codes(lib):
                                       (17, 1000, 1024, 32), (64, 512, 512, 64), (300, 512, 512, 128)])
 def test_plans_for_the_workloads(lib, M, N, K, tn):
     p = binding.plan_for(M, N, K, sm_count=152)
-    assert p["variant"] == binding.VARIANT_TC
+    assert p["variant"] == (binding.VARIANT_TC8 if M <= 32 else binding.VARIANT_TC)
     assert p["token_tile"] == tn
     ksteps = K // 128
     assert 1 <= p["split_k"] <= min(16, ksteps)
     assert p["grid"][0] == -(-N // 128) * p["split_k"]
     assert p["grid"][1] == -(-M // tn)
     assert p["cluster"][0] == p["split_k"]
-    assert p["block"][0] == (736 if tn <= 32 else 608)
+    if p["variant"] == binding.VARIANT_TC8:
+        assert p["block"][0] == 352
+    else:
+        assert p["block"][0] == (736 if tn <= 32 else 608)
     assert p["tmem_cols"] * p["ctas_per_sm"] <= 512
     assert p["smem_bytes"] * p["ctas_per_sm"] <= 232448
 
@@ -136,7 +140,10 @@ def test_planner_uses_cluster_capacity(lib):
 
 def test_plan_variant_validation(lib):
     p = binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=4, stages=6)
-    assert p.token_tile == 16
+    assert p.token_tile == 16 and p.variant == binding.VARIANT_TC
+    p8 = binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC8, split_k=2, stages=4)
+    assert p8.variant == binding.VARIANT_TC8 and p8.block[0] == 352 and p8.tmem_cols == 128
+    assert binding.plan_variant(100, 1024, 1024, binding.VARIANT_TC8).token_tile == 64
     assert p.split_k == 4 and p.stages == 6 and p.grid[0] == 8 * 4
     with pytest.raises(binding.W8A16Error) as e:
         binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, split_k=9)   # > K/128 = 8
