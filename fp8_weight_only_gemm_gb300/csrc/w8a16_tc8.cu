@@ -56,6 +56,11 @@ struct T8Cfg {
     static constexpr uint32_t kSplit0 = 3;                 // first splitter warp
     static constexpr uint32_t kFold0 = kSplit0 + NS;       // first fold warp
     static constexpr uint32_t kTokPerFold = TN * 4 / NF;
+    // Step-parallel splitting (few tokens): splitter warp w takes steps w, w+NS, ...
+    // Each warp then reuses its own ring slots, which needs NS to divide the
+    // activation and term rings; the factor and product rings must be at least NS.
+    static constexpr bool kStepPar = SA % NS == 0 && SB % NS == 0 && NP >= NS;
+
     static constexpr uint32_t ND = STAGES > SB ? (STAGES > NP ? STAGES : NP) : (SB > NP ? SB : NP);
     // barriers: wfull[S], xfull[SA], xempty[SA], bfull[SB], mdone[ND], pempty[NP], done, red
     static constexpr uint32_t kNumBars = STAGES + 2 * SA + SB + ND + NP + 2;
@@ -64,8 +69,12 @@ struct T8Cfg {
     static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
 };
 
+// Relaxed arrive: the only state peers touch before the matching wait is the
+// receive mbarrier, whose initialisation fence.mbarrier_init already releases to
+// the cluster. A release arrive would also wait for this CTA's in-flight weight
+// loads, holding the activation producer back by about a microsecond.
 __device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -178,12 +187,14 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
     const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
     const uint32_t toks_valid = min(TN, M - token0);
+    // up to 8 tokens: a splitter warp splits whole steps (two passes at most)
+    const bool step_par = Cfg::kStepPar && toks_valid <= 8;
 
     if (warp == 0) {
         for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
             const uint32_t addr = bar0 + 8u * b;
             uint32_t count = 1;
-            if (addr >= xempty0 && addr < mdone0) count = Cfg::NS;          // splitters
+            if (addr >= xempty0 && addr < mdone0) count = step_par ? 1u : Cfg::NS;   // splitters
             else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;   // fold warps
             mbar_init(addr, count);
         }
@@ -263,7 +274,11 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // The fold of step i - NP has freed product buffer i % NP once bfull[i]
+            // completes: the splitters of step i wait for that before arriving.
             constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, 2 * TN);
+            const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
+            const uint64_t db0 = smem_desc_kmajor_sw128(smem_u32(sB));
             for (uint32_t i = 0; i < nsteps; ++i) {
                 const uint32_t s = i % STAGES, b = i % Cfg::SB, p = i % Cfg::NP;
                 if (!mbar_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, &g_tc8_status,
@@ -272,16 +287,12 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 if (!mbar_wait(bfull0 + 8u * b, (i / Cfg::SB) & 1, deadline, abort_flag,
                                &g_tc8_status, kWaitB))
                     break;
-                if (i >= Cfg::NP && !mbar_wait(pempty0 + 8u * p, ((i / Cfg::NP) - 1) & 1, deadline,
-                                               abort_flag, &g_tc8_status, kWaitPEmpty))
-                    break;
                 tc_fence_after();
-                const uint32_t wa = smem_u32(sW + s * kWTileBytes);
-                const uint32_t ba = smem_u32(sB + b * Cfg::kBBytes);
+                const uint64_t dw = dw0 + ((s * kWTileBytes) >> 4);
+                const uint64_t db = db0 + ((b * Cfg::kBBytes) >> 4);
 #pragma unroll
-                for (uint32_t kk = 0; kk < kKStep / 32; ++kk)
-                    tc_mma_ss_f8(tP + p * 2 * TN, smem_desc_kmajor_sw128(wa + kk * 32),
-                                 smem_desc_kmajor_sw128(ba + kk * 32), idesc, kk > 0);
+                for (uint32_t kk = 0; kk < kKStep / 32; ++kk)   // 32 bytes of K per MMA
+                    tc_mma_ss_f8(tP + p * 2 * TN, dw + 2 * kk, db + 2 * kk, idesc, kk > 0);
                 tc_commit(mdone0 + 8u * (i % Cfg::ND));
             }
             tc_commit(done_bar);
@@ -290,10 +301,16 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         }
     } else if (is_split) {
         // ---------------- splitters: BF16 activations -> two E4M3 terms per value
-        // Work item = (token, group of 4 consecutive K); a token's 32 groups are
-        // the 32 lanes of one warp, which reduce the token's block maximum.
+        // A pass covers 4 tokens: 8 lanes per token, lane c holding the 16 values
+        // at K 8c..8c+7 and 64+8c..64+8c+7 (16-byte chunk c of each BF16 box, so
+        // the 8 lanes of a token read one 128-byte row without bank conflicts).
+        // Token-parallel mode: warp w takes passes w, w+NS, ... of every step.
+        // Step-parallel mode: warp w takes every pass of steps w, w+NS, ...
         const uint32_t sw = warp - Cfg::kSplit0;
-        for (uint32_t i = 0; i < nsteps; ++i) {
+        const uint32_t tt = lane >> 3, c = lane & 7;
+        const uint32_t i_first = step_par ? sw : 0u, di = step_par ? Cfg::NS : 1u;
+        const uint32_t t_first = step_par ? 0u : 4u * sw, dt = step_par ? 4u : 4u * Cfg::NS;
+        for (uint32_t i = i_first; i < nsteps; i += di) {
             const uint32_t j = i % Cfg::SA, b = i % Cfg::SB, f = i % Cfg::NP;
             if (!warp_wait8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
             if (i >= Cfg::SB) {   // term slot b last held step i - SB
@@ -304,28 +321,32 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             }
             if (i >= Cfg::NP && !warp_wait8(pempty0 + 8u * f, ((i / Cfg::NP) - 1) & 1, deadline,
                                             abort_flag, kWaitPEmpty))
-                break;   // factor slot f is read by the fold of step i - NP
+                break;   // factor slot f and product buffer f are read by the fold of step i - NP
             const uint8_t* xs = sX + j * Cfg::kXBytes;
             uint8_t* bs = sB + b * Cfg::kBBytes;
-            for (uint32_t t = sw; t < toks_valid; t += Cfg::NS) {
-                // K group 4*lane.. of token t: BF16 box lane / 16, 16-byte chunk
-                // (lane % 16) / 2 of row t (swizzled), 8-byte half lane % 2
-                const uint32_t g = lane & 15;
-                const uint8_t* xr = xs + (lane >> 4) * (TN * 128) + t * 128;
-                const uint2 av = *reinterpret_cast<const uint2*>(
-                    xr + (((g >> 1) ^ (t & 7)) << 4) + ((g & 1) << 3));
-                float v[4] = {__uint_as_float(av.x << 16), __uint_as_float(av.x & 0xFFFF0000u),
-                              __uint_as_float(av.y << 16), __uint_as_float(av.y & 0xFFFF0000u)};
+            for (uint32_t t0 = t_first; t0 < toks_valid; t0 += dt) {
+                // rows past the last token are TMA zero fill: splitting them is harmless
+                const uint32_t t = t0 + tt, sw7 = t & 7;
+                const uint8_t* xr = xs + t * 128 + ((c ^ sw7) << 4);
+                const uint4 a0 = *reinterpret_cast<const uint4*>(xr);
+                const uint4 a1 = *reinterpret_cast<const uint4*>(xr + TN * 128);
+                const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                float x[16];
+#pragma unroll
+                for (uint32_t e = 0; e < 8; ++e) {
+                    x[2 * e] = __uint_as_float(w[e] << 16);
+                    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+                }
                 float mx = 0.f;
                 bool bad = false;
 #pragma unroll
-                for (uint32_t e = 0; e < 4; ++e) {
-                    const float a = fabsf(v[e]);
+                for (uint32_t e = 0; e < 16; ++e) {
+                    const float a = fabsf(x[e]);
                     if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
                     else bad = true;       // NaN or infinity
                 }
 #pragma unroll
-                for (uint32_t o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                for (uint32_t o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
                 // E = floor(log2(mx)) from the bits (mx may be a subnormal)
                 const uint32_t mb = __float_as_uint(mx);
                 const int ef = static_cast<int>(mb >> 23);
@@ -333,24 +354,40 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 // x = a * 2^(7 - E) in two exact power-of-two steps (7 - E in -120..156)
                 const int e1 = (7 - E) / 2, e2 = (7 - E) - e1;
                 const float p1 = __int_as_float((127 + e1) << 23), p2 = __int_as_float((127 + e2) << 23);
-                float x[4];
 #pragma unroll
-                for (uint32_t e = 0; e < 4; ++e) x[e] = (v[e] * p1) * p2;
-                const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
-                float hf[4];
-                e4m3x2_to_f32x2(h01, hf[0], hf[1]);
-                e4m3x2_to_f32x2(h23, hf[2], hf[3]);
-                const uint32_t l01 = f32x2_to_e4m3x2((x[0] - hf[0]) * 32.f, (x[1] - hf[1]) * 32.f);
-                const uint32_t l23 = f32x2_to_e4m3x2((x[2] - hf[2]) * 32.f, (x[3] - hf[3]) * 32.f);
-                uint32_t hw = h01 | (h23 << 16);
-                const uint32_t lw = l01 | (l23 << 16);
-                if (bad) hw = 0x7F7F7F7Fu;   // a non-finite value: NaN codes
-                // E4M3 row t (hi) and TN + t (lo): 4 bytes at K 4*lane of the 128-byte
-                // row, i.e. chunk lane / 4 (swizzled), byte (lane % 4) * 4
-                const uint32_t pos = (((lane >> 2) ^ (t & 7)) << 4) + ((lane & 3) << 2);
-                *reinterpret_cast<uint32_t*>(bs + t * 128 + pos) = hw;
-                *reinterpret_cast<uint32_t*>(bs + (TN + t) * 128 + pos) = lw;
-                if (lane == 0) {
+                for (uint32_t e = 0; e < 16; ++e) x[e] = (x[e] * p1) * p2;
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (uint32_t q = 0; q < 4; ++q) {
+                    const uint32_t h0 = f32x2_to_e4m3x2(x[4 * q], x[4 * q + 1]);
+                    const uint32_t h1 = f32x2_to_e4m3x2(x[4 * q + 2], x[4 * q + 3]);
+                    float hf[4];   // the hi terms' values (exact)
+                    e4m3x2_to_f32x2(h0, hf[0], hf[1]);
+                    e4m3x2_to_f32x2(h1, hf[2], hf[3]);
+                    const uint32_t l0 = f32x2_to_e4m3x2((x[4 * q] - hf[0]) * 32.f, (x[4 * q + 1] - hf[1]) * 32.f);
+                    const uint32_t l1 = f32x2_to_e4m3x2((x[4 * q + 2] - hf[2]) * 32.f, (x[4 * q + 3] - hf[3]) * 32.f);
+                    hw[q] = bad ? 0x7F7F7F7Fu : (h0 | (h1 << 16));   // non-finite: NaN codes
+                    lw[q] = l0 | (l1 << 16);
+                }
+                // E4M3 rows t (hi) and TN + t (lo), 128 bytes each, 128-byte swizzle:
+                // K 8c.. is 8 bytes in chunk c/2, K 64+8c.. in chunk 4 + c/2. Odd
+                // tokens store their second half first so that the two tokens of a
+                // half-warp write disjoint banks.
+                const uint32_t posA = (((c >> 1) ^ sw7) << 4) + ((c & 1) << 3);
+                const uint32_t posB = ((((c >> 1) + 4) ^ sw7) << 4) + ((c & 1) << 3);
+                const bool odd = tt & 1;
+                const uint32_t p_1 = odd ? posB : posA, p_2 = odd ? posA : posB;
+                const uint2 h_1 = odd ? make_uint2(hw[2], hw[3]) : make_uint2(hw[0], hw[1]);
+                const uint2 h_2 = odd ? make_uint2(hw[0], hw[1]) : make_uint2(hw[2], hw[3]);
+                const uint2 l_1 = odd ? make_uint2(lw[2], lw[3]) : make_uint2(lw[0], lw[1]);
+                const uint2 l_2 = odd ? make_uint2(lw[0], lw[1]) : make_uint2(lw[2], lw[3]);
+                uint8_t* rh = bs + t * 128;
+                uint8_t* rl = bs + (TN + t) * 128;
+                *reinterpret_cast<uint2*>(rh + p_1) = h_1;
+                *reinterpret_cast<uint2*>(rh + p_2) = h_2;
+                *reinterpret_cast<uint2*>(rl + p_1) = l_1;
+                *reinterpret_cast<uint2*>(rl + p_2) = l_2;
+                if (c == 0) {
                     // 2^(E-7) as FP32 (subnormal or zero for very small blocks)
                     const int ie = E - 7;
                     float inv = 0.f;
@@ -363,8 +400,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             fence_proxy_async_smem();   // the tensor core reads these terms
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(xempty0 + 8u * j);
                 mbar_arrive(bfull0 + 8u * b);
+                mbar_arrive(xempty0 + 8u * j);
             }
         }
     } else if (is_fold) {
