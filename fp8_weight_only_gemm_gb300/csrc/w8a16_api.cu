@@ -126,8 +126,9 @@ uint32_t default_stages(int32_t v, uint32_t tn) {
     if (v == W8A16_VARIANT_TC8) return tn == 16 ? 4 : tn == 32 ? 6 : 4;   // 16: two CTAs per SM
     return tn == 16 ? 8 : tn == 32 ? 6 : tn == 64 ? 6 : 4;
 }
-// The variant the planner uses for a token count.
-int32_t auto_variant(uint32_t M) { return M <= 32 ? W8A16_VARIANT_TC8 : W8A16_VARIANT_TC; }
+// The variant the planner uses for a token count: the two-term FP8 kernel while
+// its activation split is cheap (a 16-token tile), the BF16 kernel beyond.
+int32_t auto_variant(uint32_t M) { return M <= 16 ? W8A16_VARIANT_TC8 : W8A16_VARIANT_TC; }
 
 // CTAs of one tensor-core plan that fit on an SM: shared memory (228 KiB per
 // SM, 1 KiB reserved per CTA), TMEM (512 columns), threads (2048), and the
@@ -177,10 +178,12 @@ void fill_simt(uint32_t M, uint32_t N, w8a16_plan_t* p) {
     p->cluster[0] = p->cluster[1] = p->cluster[2] = 1;
 }
 
-// Choose the split-K factor by a wave model: CTAs beyond the co-resident slots
-// (for that cluster size) form further waves; a CTA's time is its share of K
-// steps plus a fixed start-up (ring fill, in step units); splitting adds a
-// cluster reduction. cap[s] = co-resident CTAs in clusters of s (0 = cannot run).
+// Choose the split-K factor by a load model: a CTA's time is its share of K
+// steps plus a fixed start-up and drain (5 steps' worth); CTAs beyond the
+// co-resident slots for that cluster size stretch the launch in proportion (a
+// partial second wave costs only its share, since launches overlap); each rank
+// of a split adds a little reduction work. cap[s] = co-resident CTAs in clusters
+// of s (0 = cannot run).
 uint32_t choose_split(uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
                       const uint32_t* cap) {
     const uint32_t max_split = ksteps < 16u ? ksteps : 16u;
@@ -189,11 +192,10 @@ uint32_t choose_split(uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
     for (uint32_t s = 1; s <= max_split; ++s) {
         const uint32_t slots = cap[s];
         if (slots == 0) continue;
-        const uint64_t ctas = static_cast<uint64_t>(row_tiles) * token_tiles * s;
-        const uint64_t waves = (ctas + slots - 1) / slots;
+        const double ctas = static_cast<double>(row_tiles) * token_tiles * s;
+        const double load = ctas > slots ? ctas / slots : 1.0;
         const double steps = static_cast<double>((ksteps + s - 1) / s);
-        const double cost =
-            static_cast<double>(waves) * (steps + 5.0) + (s > 1 ? 0.5 + 0.1 * s : 0.0);
+        const double cost = load * (steps + 5.0) + 0.25 * s;
         if (cost < best - 1e-9) {
             best = cost;
             best_s = s;

@@ -101,7 +101,7 @@ def test_strerror_covers_codes(lib):
                                       (17, 1000, 1024, 32), (64, 512, 512, 64), (300, 512, 512, 128)])
 def test_plans_for_the_workloads(lib, M, N, K, tn):
     p = binding.plan_for(M, N, K, sm_count=152)
-    assert p["variant"] == (binding.VARIANT_TC8 if M <= 32 else binding.VARIANT_TC)
+    assert p["variant"] == (binding.VARIANT_TC8 if M <= 16 else binding.VARIANT_TC)
     assert p["token_tile"] == tn
     ksteps = K // 128
     assert 1 <= p["split_k"] <= min(16, ksteps)
