@@ -13,21 +13,25 @@
 //   * swap-AB: 128 weight rows are the MMA's M, the tokens (rows of A, padded to
 //     the token tile TN = 16..128) are its N, so a decode call wastes no MMA rows
 //     on padding and the whole token range of one tile streams W exactly once;
-//   * warp 0 (one thread) streams 128x128 E4M3 weight tiles and the TNx128 BF16
-//     activation tile of each K step with TMA (128-byte swizzle) into a ring of
-//     STAGES shared-memory slots;
-//   * 8 converter warps each take 32 weight rows x 64 K of a step, convert E4M3
-//     to BF16 in registers (exact) and write them with tcgen05.st into one of two
-//     TMEM operand buffers;
-//   * warp 1 (one thread) issues 8 tcgen05.mma (K = 16 each) per step with A in
-//     TMEM and the activations in shared memory, into one of two TMEM product
-//     buffers P, and commits to mbarriers;
-//   * the converter warps read P back (tcgen05.ld) and fold acc += scale * P in
-//     FP32 registers, one scale per (tile, step);
+//   * warp 0 (one thread) streams 128x128 E4M3 weight tiles with TMA (128-byte
+//     swizzle) into a ring of STAGES shared-memory slots; the first slots are
+//     requested before the CTA barrier, and before waiting on the previous grid
+//     (programmatic dependent launch: the caller guarantees W is not written);
+//   * warp 2 (one thread) waits on the previous grid, then streams the TNx128
+//     BF16 activation tile of each K step into its own ring;
+//   * NC converter warps (16 for TN <= 32, else 8) take 32 weight rows x a K
+//     slice of a step each, convert E4M3 to BF16 in registers (exact) and write
+//     them with tcgen05.st into one of NA TMEM operand buffers;
+//   * warp 1 (one thread) allocates TMEM and issues 8 tcgen05.mma (K = 16 each)
+//     per step with A in TMEM and the activations in shared memory, into one of
+//     NP TMEM product buffers P, committing each step to an mbarrier;
+//   * NF fold warps read P back (tcgen05.ld) and fold acc += scale * P in FP32
+//     registers, one scale per (tile, step), then store or push the partials;
 //   * split-K: a cluster of split_k CTAs shares one weight tile, each CTA on a
-//     contiguous range of K steps; partials meet in shared memory and each CTA
-//     sums a slice of the outputs over the cluster's CTAs in rank (= K) order via
-//     distributed shared memory. No global scratch, no atomics: deterministic.
+//     contiguous range of K steps; every CTA owns a slice of the tile's rows and
+//     receives the other ranks' partials of that slice in shared memory
+//     (st.async over distributed shared memory), summing them in rank (= K)
+//     order. No global scratch, no atomics: deterministic.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
