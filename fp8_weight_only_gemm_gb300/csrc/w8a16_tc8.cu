@@ -56,10 +56,11 @@ struct T8Cfg {
     static constexpr uint32_t kSplit0 = 3;                 // first splitter warp
     static constexpr uint32_t kFold0 = kSplit0 + NS;       // first fold warp
     static constexpr uint32_t kTokPerFold = TN * 4 / NF;
-    // Step-parallel splitting (few tokens): splitter warp w takes steps w, w+NS, ...
-    // Each warp then reuses its own ring slots, which needs NS to divide the
-    // activation and term rings; the factor and product rings must be at least NS.
-    static constexpr bool kStepPar = SA % NS == 0 && SB % NS == 0 && NP >= NS;
+    // Step-parallel mode (few tokens): splitter warp w takes steps w, w+NS, ... and
+    // issues their MMAs itself. Every ring then has exactly NS slots, so warp w
+    // always uses slot w of each and waits only on barriers it alone feeds or that
+    // complete once per step of its own.
+    static constexpr bool kStepPar = STAGES == NS && SA == NS && SB == NS && NP == NS;
 
     static constexpr uint32_t ND = STAGES > SB ? (STAGES > NP ? STAGES : NP) : (SB > NP ? SB : NP);
     // barriers: wfull[S], xfull[SA], xempty[SA], bfull[SB], mdone[ND], pempty[NP], done, red
@@ -143,6 +144,141 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float
     hi = __high2float(v);
 }
 
+// The four K=32 MMAs of one 128-K step: D[128 x 2TN] (FP32, TMEM) = W tile x terms.
+template <uint32_t TN>
+__device__ __forceinline__ void step_mmas(uint32_t d_tmem, uint64_t dw, uint64_t db) {
+    constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, 2 * TN);
+#pragma unroll
+    for (uint32_t kk = 0; kk < kKStep / 32; ++kk)   // 32 bytes of K per MMA
+        tc_mma_ss_f8(d_tmem, dw + 2 * kk, db + 2 * kk, idesc, kk > 0);
+}
+
+// E = floor(log2(mx)) of a block maximum from its bits (mx may be an FP32 subnormal).
+__device__ __forceinline__ int block_exponent(float mx) {
+    const uint32_t mb = __float_as_uint(mx);
+    const int ef = static_cast<int>(mb >> 23);
+    return ef != 0 ? ef - 127 : (mb != 0 ? -118 - __clz(mb) : 0);
+}
+// 2^(7-E) as two exact FP32 powers of two (7 - E spans -120..156).
+__device__ __forceinline__ void split_scales(int E, float& p1, float& p2) {
+    const int e1 = (7 - E) / 2, e2 = (7 - E) - e1;
+    p1 = __int_as_float((127 + e1) << 23);
+    p2 = __int_as_float((127 + e2) << 23);
+}
+// 2^(E-7) as FP32 (subnormal or zero for very small blocks); 0 for an all-zero block.
+__device__ __forceinline__ float fold_factor(int E, float mx) {
+    const int ie = E - 7;
+    if (!(mx > 0.f)) return 0.f;
+    return ie >= -126 ? __int_as_float((127 + ie) << 23)
+                      : (ie >= -149 ? __int_as_float(1 << (ie + 149)) : 0.f);
+}
+// hi/lo E4M3 codes of four consecutive scaled values (byte i = value i).
+__device__ __forceinline__ void two_terms4(const float* x, uint32_t& hw, uint32_t& lw) {
+    const uint32_t h0 = f32x2_to_e4m3x2(x[0], x[1]), h1 = f32x2_to_e4m3x2(x[2], x[3]);
+    float hf[4];   // the hi terms' values (exact)
+    e4m3x2_to_f32x2(h0, hf[0], hf[1]);
+    e4m3x2_to_f32x2(h1, hf[2], hf[3]);
+    const uint32_t l0 = f32x2_to_e4m3x2((x[0] - hf[0]) * 32.f, (x[1] - hf[1]) * 32.f);
+    const uint32_t l1 = f32x2_to_e4m3x2((x[2] - hf[2]) * 32.f, (x[3] - hf[3]) * 32.f);
+    hw = h0 | (h1 << 16);
+    lw = l0 | (l1 << 16);
+}
+
+// Split one token's 128-K block with the whole warp, 4 values per lane (used for
+// one or two tokens, where a lane per 4 values keeps all 32 lanes busy). Lane l
+// holds K 4l..4l+3: BF16 box l / 16, 16-byte chunk (l % 16) / 2 of row t, half l % 2.
+template <uint32_t TN>
+__device__ __forceinline__ void split_token_w32(const uint8_t* xs, uint8_t* bs, float* inv,
+                                                uint32_t t, uint32_t lane) {
+    const uint32_t g = lane & 15;
+    const uint2 av = *reinterpret_cast<const uint2*>(xs + (lane >> 4) * (TN * 128) + t * 128 +
+                                                     (((g >> 1) ^ (t & 7)) << 4) + ((g & 1) << 3));
+    float x[4] = {__uint_as_float(av.x << 16), __uint_as_float(av.x & 0xFFFF0000u),
+                  __uint_as_float(av.y << 16), __uint_as_float(av.y & 0xFFFF0000u)};
+    float mx = 0.f;
+    bool bad = false;
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) {
+        const float a = fabsf(x[e]);
+        if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
+        else bad = true;   // NaN or infinity
+    }
+#pragma unroll
+    for (uint32_t o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    const int E = block_exponent(mx);
+    float p1, p2;
+    split_scales(E, p1, p2);
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) x[e] = (x[e] * p1) * p2;
+    uint32_t hw, lw;
+    two_terms4(x, hw, lw);
+    if (bad) hw = 0x7F7F7F7Fu;   // a non-finite value: NaN codes
+    // E4M3 rows t (hi) and TN + t (lo): 4 bytes at K 4l, chunk l / 4 (swizzled), byte 4 (l % 4)
+    const uint32_t pos = (((lane >> 2) ^ (t & 7)) << 4) + ((lane & 3) << 2);
+    *reinterpret_cast<uint32_t*>(bs + t * 128 + pos) = hw;
+    *reinterpret_cast<uint32_t*>(bs + (TN + t) * 128 + pos) = lw;
+    if (lane == 0) inv[t] = fold_factor(E, mx);
+}
+
+// Split four tokens' blocks (t0..t0+3), 8 lanes per token, 16 values per lane:
+// lane c of a token holds K 8c..8c+7 and 64+8c..64+8c+7 (16-byte chunk c of each
+// BF16 box, so the 8 lanes of a token read one 128-byte row without conflicts).
+template <uint32_t TN>
+__device__ __forceinline__ void split_tokens_w8(const uint8_t* xs, uint8_t* bs, float* inv,
+                                                uint32_t t0, uint32_t lane) {
+    const uint32_t tt = lane >> 3, c = lane & 7;
+    const uint32_t t = t0 + tt, sw7 = t & 7;
+    const uint8_t* xr = xs + t * 128 + ((c ^ sw7) << 4);
+    const uint4 a0 = *reinterpret_cast<const uint4*>(xr);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(xr + TN * 128);
+    const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    float x[16];
+#pragma unroll
+    for (uint32_t e = 0; e < 8; ++e) {
+        x[2 * e] = __uint_as_float(w[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+    float mx = 0.f;
+    bool bad = false;
+#pragma unroll
+    for (uint32_t e = 0; e < 16; ++e) {
+        const float a = fabsf(x[e]);
+        if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
+        else bad = true;   // NaN or infinity
+    }
+#pragma unroll
+    for (uint32_t o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    const int E = block_exponent(mx);
+    float p1, p2;
+    split_scales(E, p1, p2);
+#pragma unroll
+    for (uint32_t e = 0; e < 16; ++e) x[e] = (x[e] * p1) * p2;
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (uint32_t q = 0; q < 4; ++q) {
+        two_terms4(x + 4 * q, hw[q], lw[q]);
+        if (bad) hw[q] = 0x7F7F7F7Fu;   // a non-finite value: NaN codes
+    }
+    // E4M3 rows t (hi) and TN + t (lo), 128 bytes each, 128-byte swizzle: K 8c.. is
+    // 8 bytes in chunk c/2, K 64+8c.. in chunk 4 + c/2. Odd tokens store their
+    // second half first so that the two tokens of a half-warp write disjoint banks.
+    const uint32_t posA = (((c >> 1) ^ sw7) << 4) + ((c & 1) << 3);
+    const uint32_t posB = ((((c >> 1) + 4) ^ sw7) << 4) + ((c & 1) << 3);
+    const bool odd = tt & 1;
+    const uint32_t p_1 = odd ? posB : posA, p_2 = odd ? posA : posB;
+    const uint2 h_1 = odd ? make_uint2(hw[2], hw[3]) : make_uint2(hw[0], hw[1]);
+    const uint2 h_2 = odd ? make_uint2(hw[0], hw[1]) : make_uint2(hw[2], hw[3]);
+    const uint2 l_1 = odd ? make_uint2(lw[2], lw[3]) : make_uint2(lw[0], lw[1]);
+    const uint2 l_2 = odd ? make_uint2(lw[0], lw[1]) : make_uint2(lw[2], lw[3]);
+    uint8_t* rh = bs + t * 128;
+    uint8_t* rl = bs + (TN + t) * 128;
+    *reinterpret_cast<uint2*>(rh + p_1) = h_1;
+    *reinterpret_cast<uint2*>(rh + p_2) = h_2;
+    *reinterpret_cast<uint2*>(rl + p_1) = l_1;
+    *reinterpret_cast<uint2*>(rl + p_2) = l_2;
+    if (c == 0) inv[t] = fold_factor(E, mx);
+}
+
 template <uint32_t TN, uint32_t STAGES>
 __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     w8a16_tc8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
@@ -196,6 +332,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             uint32_t count = 1;
             if (addr >= xempty0 && addr < mdone0) count = step_par ? 1u : Cfg::NS;   // splitters
             else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;   // fold warps
+            else if (addr == done_bar) count = step_par ? Cfg::NS : 1u;      // MMA issuers
             mbar_init(addr, count);
         }
         if (lane == 0) *abort_flag = 0;
@@ -273,13 +410,13 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // (token-parallel mode; in step-parallel mode the splitters issue)
         if (lane == 0) {
             // The fold of step i - NP has freed product buffer i % NP once bfull[i]
             // completes: the splitters of step i wait for that before arriving.
-            constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, 2 * TN);
             const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
             const uint64_t db0 = smem_desc_kmajor_sw128(smem_u32(sB));
-            for (uint32_t i = 0; i < nsteps; ++i) {
+            for (uint32_t i = 0; i < (step_par ? 0u : nsteps); ++i) {
                 const uint32_t s = i % STAGES, b = i % Cfg::SB, p = i % Cfg::NP;
                 if (!mbar_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, &g_tc8_status,
                                kWaitW))
@@ -290,26 +427,25 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 tc_fence_after();
                 const uint64_t dw = dw0 + ((s * kWTileBytes) >> 4);
                 const uint64_t db = db0 + ((b * Cfg::kBBytes) >> 4);
-#pragma unroll
-                for (uint32_t kk = 0; kk < kKStep / 32; ++kk)   // 32 bytes of K per MMA
-                    tc_mma_ss_f8(tP + p * 2 * TN, dw + 2 * kk, db + 2 * kk, idesc, kk > 0);
+                step_mmas<TN>(tP + p * 2 * TN, dw, db);
                 tc_commit(mdone0 + 8u * (i % Cfg::ND));
             }
-            tc_commit(done_bar);
+            if (!step_par) tc_commit(done_bar);
             volatile int never = 0;
             mbar_wait(done_bar, 0, globaltimer_ns() + timeout_ns, &never, &g_tc8_status, kWaitDone);
         }
     } else if (is_split) {
         // ---------------- splitters: BF16 activations -> two E4M3 terms per value
-        // A pass covers 4 tokens: 8 lanes per token, lane c holding the 16 values
-        // at K 8c..8c+7 and 64+8c..64+8c+7 (16-byte chunk c of each BF16 box, so
-        // the 8 lanes of a token read one 128-byte row without bank conflicts).
-        // Token-parallel mode: warp w takes passes w, w+NS, ... of every step.
-        // Step-parallel mode: warp w takes every pass of steps w, w+NS, ...
+        // Token-parallel mode: warp w takes 4-token passes w, w+NS, ... of every
+        // step. Step-parallel mode (up to 8 tokens): warp w takes every pass of
+        // steps w, w+NS, ...; with one or two tokens a pass is one token on all
+        // 32 lanes.
         const uint32_t sw = warp - Cfg::kSplit0;
-        const uint32_t tt = lane >> 3, c = lane & 7;
         const uint32_t i_first = step_par ? sw : 0u, di = step_par ? Cfg::NS : 1u;
         const uint32_t t_first = step_par ? 0u : 4u * sw, dt = step_par ? 4u : 4u * Cfg::NS;
+        const bool whole_warp = step_par && toks_valid <= 2;
+        const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
+        const uint64_t db0 = smem_desc_kmajor_sw128(smem_u32(sB));
         for (uint32_t i = i_first; i < nsteps; i += di) {
             const uint32_t j = i % Cfg::SA, b = i % Cfg::SB, f = i % Cfg::NP;
             if (!warp_wait8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
@@ -324,86 +460,38 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 break;   // factor slot f and product buffer f are read by the fold of step i - NP
             const uint8_t* xs = sX + j * Cfg::kXBytes;
             uint8_t* bs = sB + b * Cfg::kBBytes;
-            for (uint32_t t0 = t_first; t0 < toks_valid; t0 += dt) {
+            float* inv = sInv + f * TN;
+            if (whole_warp) {
+                for (uint32_t t = 0; t < toks_valid; ++t) split_token_w32<TN>(xs, bs, inv, t, lane);
+            } else {
                 // rows past the last token are TMA zero fill: splitting them is harmless
-                const uint32_t t = t0 + tt, sw7 = t & 7;
-                const uint8_t* xr = xs + t * 128 + ((c ^ sw7) << 4);
-                const uint4 a0 = *reinterpret_cast<const uint4*>(xr);
-                const uint4 a1 = *reinterpret_cast<const uint4*>(xr + TN * 128);
-                const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                float x[16];
-#pragma unroll
-                for (uint32_t e = 0; e < 8; ++e) {
-                    x[2 * e] = __uint_as_float(w[e] << 16);
-                    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-                }
-                float mx = 0.f;
-                bool bad = false;
-#pragma unroll
-                for (uint32_t e = 0; e < 16; ++e) {
-                    const float a = fabsf(x[e]);
-                    if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
-                    else bad = true;       // NaN or infinity
-                }
-#pragma unroll
-                for (uint32_t o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-                // E = floor(log2(mx)) from the bits (mx may be a subnormal)
-                const uint32_t mb = __float_as_uint(mx);
-                const int ef = static_cast<int>(mb >> 23);
-                const int E = ef != 0 ? ef - 127 : (mb != 0 ? -118 - __clz(mb) : 0);
-                // x = a * 2^(7 - E) in two exact power-of-two steps (7 - E in -120..156)
-                const int e1 = (7 - E) / 2, e2 = (7 - E) - e1;
-                const float p1 = __int_as_float((127 + e1) << 23), p2 = __int_as_float((127 + e2) << 23);
-#pragma unroll
-                for (uint32_t e = 0; e < 16; ++e) x[e] = (x[e] * p1) * p2;
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (uint32_t q = 0; q < 4; ++q) {
-                    const uint32_t h0 = f32x2_to_e4m3x2(x[4 * q], x[4 * q + 1]);
-                    const uint32_t h1 = f32x2_to_e4m3x2(x[4 * q + 2], x[4 * q + 3]);
-                    float hf[4];   // the hi terms' values (exact)
-                    e4m3x2_to_f32x2(h0, hf[0], hf[1]);
-                    e4m3x2_to_f32x2(h1, hf[2], hf[3]);
-                    const uint32_t l0 = f32x2_to_e4m3x2((x[4 * q] - hf[0]) * 32.f, (x[4 * q + 1] - hf[1]) * 32.f);
-                    const uint32_t l1 = f32x2_to_e4m3x2((x[4 * q + 2] - hf[2]) * 32.f, (x[4 * q + 3] - hf[3]) * 32.f);
-                    hw[q] = bad ? 0x7F7F7F7Fu : (h0 | (h1 << 16));   // non-finite: NaN codes
-                    lw[q] = l0 | (l1 << 16);
-                }
-                // E4M3 rows t (hi) and TN + t (lo), 128 bytes each, 128-byte swizzle:
-                // K 8c.. is 8 bytes in chunk c/2, K 64+8c.. in chunk 4 + c/2. Odd
-                // tokens store their second half first so that the two tokens of a
-                // half-warp write disjoint banks.
-                const uint32_t posA = (((c >> 1) ^ sw7) << 4) + ((c & 1) << 3);
-                const uint32_t posB = ((((c >> 1) + 4) ^ sw7) << 4) + ((c & 1) << 3);
-                const bool odd = tt & 1;
-                const uint32_t p_1 = odd ? posB : posA, p_2 = odd ? posA : posB;
-                const uint2 h_1 = odd ? make_uint2(hw[2], hw[3]) : make_uint2(hw[0], hw[1]);
-                const uint2 h_2 = odd ? make_uint2(hw[0], hw[1]) : make_uint2(hw[2], hw[3]);
-                const uint2 l_1 = odd ? make_uint2(lw[2], lw[3]) : make_uint2(lw[0], lw[1]);
-                const uint2 l_2 = odd ? make_uint2(lw[0], lw[1]) : make_uint2(lw[2], lw[3]);
-                uint8_t* rh = bs + t * 128;
-                uint8_t* rl = bs + (TN + t) * 128;
-                *reinterpret_cast<uint2*>(rh + p_1) = h_1;
-                *reinterpret_cast<uint2*>(rh + p_2) = h_2;
-                *reinterpret_cast<uint2*>(rl + p_1) = l_1;
-                *reinterpret_cast<uint2*>(rl + p_2) = l_2;
-                if (c == 0) {
-                    // 2^(E-7) as FP32 (subnormal or zero for very small blocks)
-                    const int ie = E - 7;
-                    float inv = 0.f;
-                    if (mx > 0.f)
-                        inv = ie >= -126 ? __int_as_float((127 + ie) << 23)
-                                         : (ie >= -149 ? __int_as_float(1 << (ie + 149)) : 0.f);
-                    sInv[f * TN + t] = inv;
-                }
+                for (uint32_t t0 = t_first; t0 < toks_valid; t0 += dt)
+                    split_tokens_w8<TN>(xs, bs, inv, t0, lane);
             }
             fence_proxy_async_smem();   // the tensor core reads these terms
             __syncwarp();
-            if (lane == 0) {
+            if (step_par) {
+                // This warp issues step i's MMAs: slot b = i % NS also holds step i's
+                // weights, and step i - NS's MMAs (this warp's, awaited above) freed it.
+                bool ok = true;
+                if (lane == 0) {
+                    mbar_arrive(xempty0 + 8u * j);
+                    ok = mbar_wait(wfull0 + 8u * b, (i / STAGES) & 1, deadline, abort_flag,
+                                   &g_tc8_status, kWaitW);
+                    if (ok) {
+                        tc_fence_after();
+                        step_mmas<TN>(tP + f * 2 * TN, dw0 + ((b * kWTileBytes) >> 4),
+                                      db0 + ((b * Cfg::kBBytes) >> 4));
+                        tc_commit(mdone0 + 8u * (i % Cfg::ND));
+                    }
+                }
+                if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) break;
+            } else if (lane == 0) {
                 mbar_arrive(bfull0 + 8u * b);
                 mbar_arrive(xempty0 + 8u * j);
             }
         }
+        if (step_par && lane == 0) tc_commit(done_bar);   // after this warp's last MMAs
     } else if (is_fold) {
         // --------- fold: acc += scale * 2^(E-7) * (P_hi + P_lo / 32) per token
         const uint32_t fh = (warp - Cfg::kFold0) >> 2;
