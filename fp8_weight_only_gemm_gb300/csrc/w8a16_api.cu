@@ -330,13 +330,21 @@ int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::s
     return W8A16_OK;
 }
 
+// The live table decides which cluster sizes can run at all; the slot counts are
+// the model's (SMs x CTAs per SM), because the cluster occupancy query reports one
+// CTA per SM even where two co-reside (launches of two-per-SM plans do run all
+// their CTAs at once).
 int plan_live(uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& info, w8a16_plan_t* out,
               std::string* err) {
     const int32_t v = auto_variant(M);
     const uint32_t tn = token_tile_for(v, M);
+    const uint32_t stages = default_stages(v, tn);
     uint32_t cap[17];
-    int rc = live_capacity(v, tn, default_stages(v, tn), cap, err);
+    int rc = live_capacity(v, tn, stages, cap, err);
     if (rc) return rc;
+    uint32_t model[17];
+    model_capacity(static_cast<uint32_t>(info.sm_count), tc_ctas_per_sm(v, tn, stages, 1), model);
+    for (uint32_t c = 1; c <= 16; ++c) cap[c] = cap[c] == 0 ? 0u : model[c];
     return plan_core(v, M, N, K, static_cast<uint32_t>(info.sm_count), cap, out);
 }
 

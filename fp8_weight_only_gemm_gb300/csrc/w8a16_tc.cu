@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     const uint32_t my_row0 = owned_row0(rank, split_k);
     const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
     const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
+    const uint32_t toks_valid = min(TN, M - token0);
 
     if (warp == 0) {
         // barrier b is initialised by lane b % 32 (arrival counts by kind)
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     }
     if (threadIdx.x == 0) {
         if (split_k > 1)   // every rank pushes its partials of my rows here
-            mbar_arrive_expect_tx(red_bar, split_k * my_rows * TN * 4u);
+            mbar_arrive_expect_tx(red_bar, split_k * my_rows * toks_valid * 4u);
         // The first ring's weight tiles go out before anything else (TMEM
         // allocation, the CTA barrier), so their HBM latency overlaps the set-up.
         // Weights are requested before waiting on the previous grid in the
@@ -235,7 +236,6 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     const bool is_conv = warp >= Cfg::kConv0 && warp < Cfg::kFold0;
     const bool is_fold = warp >= Cfg::kFold0;
     const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
-    const uint32_t toks_valid = min(TN, M - token0);
 
     if (warp == 0) {
         // ------------------------------------------- weight producer (TMA)
@@ -413,8 +413,9 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
             const uint32_t dbar = dsmem_map(red_bar, owner);
 #pragma unroll
-            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)
-                st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)   // tokens past M are not sent
+                if (fh * Cfg::kTokPerFold + t < toks_valid)
+                    st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
         }
     }
 

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         __syncwarp();
     }
     if (threadIdx.x == 0) {
-        if (split_k > 1) mbar_arrive_expect_tx(red_bar, split_k * my_rows * TN * 4u);
+        if (split_k > 1) mbar_arrive_expect_tx(red_bar, split_k * my_rows * toks_valid * 4u);
         // First weight tiles before anything else; weights are requested before
         // waiting on the previous grid (under a programmatic launch the caller
         // guarantees that grid does not write W).
@@ -544,8 +544,9 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
             const uint32_t dbar = dsmem_map(red_bar, owner);
 #pragma unroll
-            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)
-                st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)   // tokens past M are not sent
+                if (fh * Cfg::kTokPerFold + t < toks_valid)
+                    st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
         }
     }
 
