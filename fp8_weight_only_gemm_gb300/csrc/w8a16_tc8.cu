@@ -186,13 +186,10 @@ __device__ __forceinline__ void two_terms4(const float* x, uint32_t& hw, uint32_
 
 // Split one token's 128-K block with the whole warp, 4 values per lane (used for
 // one or two tokens, where a lane per 4 values keeps all 32 lanes busy). Lane l
-// holds K 4l..4l+3: BF16 box l / 16, 16-byte chunk (l % 16) / 2 of row t, half l % 2.
+// holds K 4l..4l+3 (av: 4 BF16 values, lowest K first).
 template <uint32_t TN>
-__device__ __forceinline__ void split_token_w32(const uint8_t* xs, uint8_t* bs, float* inv,
-                                                uint32_t t, uint32_t lane) {
-    const uint32_t g = lane & 15;
-    const uint2 av = *reinterpret_cast<const uint2*>(xs + (lane >> 4) * (TN * 128) + t * 128 +
-                                                     (((g >> 1) ^ (t & 7)) << 4) + ((g & 1) << 3));
+__device__ __forceinline__ void split_token_w32(uint2 av, uint8_t* bs, float* inv, uint32_t t,
+                                                uint32_t lane) {
     float x[4] = {__uint_as_float(av.x << 16), __uint_as_float(av.x & 0xFFFF0000u),
                   __uint_as_float(av.y << 16), __uint_as_float(av.y & 0xFFFF0000u)};
     float mx = 0.f;
@@ -283,7 +280,8 @@ template <uint32_t TN, uint32_t STAGES>
 __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     w8a16_tc8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                      const float* __restrict__ scale, __nv_bfloat16* __restrict__ C, uint32_t ldc,
-                     uint32_t M, uint32_t N, uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
+                     const uint16_t* __restrict__ A, uint32_t lda, uint32_t M, uint32_t N,
+                     uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
     using Cfg = T8Cfg<TN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -325,6 +323,10 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     const uint32_t toks_valid = min(TN, M - token0);
     // up to 8 tokens: a splitter warp splits whole steps (two passes at most)
     const bool step_par = Cfg::kStepPar && toks_valid <= 8;
+    // one or two tokens: the splitters read A straight from global memory (the
+    // tensor-memory-access unit is busy with weight tiles, and a 256-byte row
+    // waits behind them), so the activation producer has nothing to do
+    const bool direct_x = step_par && toks_valid <= 2;
 
     if (warp == 0) {
         for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         }
     } else if (warp == 2) {
         // -------------------------------------------- activation producer (TMA)
-        if (lane == 0) {
+        if (lane == 0 && !direct_x) {
             const uint64_t pol_a = l2_policy_evict_last();
             grid_dependency_wait();   // A may be written by the previous grid in the stream
             uint32_t issued = 0;
@@ -443,12 +445,28 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         const uint32_t sw = warp - Cfg::kSplit0;
         const uint32_t i_first = step_par ? sw : 0u, di = step_par ? Cfg::NS : 1u;
         const uint32_t t_first = step_par ? 0u : 4u * sw, dt = step_par ? 4u : 4u * Cfg::NS;
-        const bool whole_warp = step_par && toks_valid <= 2;
         const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
         const uint64_t db0 = smem_desc_kmajor_sw128(smem_u32(sB));
+        // direct_x: lane l's 4 values at K 4l of tokens 0 and 1, one step ahead
+        const uint16_t* arow = A + static_cast<size_t>(token0) * lda + 4u * lane;
+        auto load_x = [&](uint32_t i, uint2* v) {
+            const uint16_t* src = arow + static_cast<size_t>(s_begin + i) * kKStep;
+            v[0] = *reinterpret_cast<const uint2*>(src);
+            v[1] = toks_valid > 1 ? *reinterpret_cast<const uint2*>(src + lda) : make_uint2(0u, 0u);
+        };
+        uint2 xnext[2] = {make_uint2(0u, 0u), make_uint2(0u, 0u)};
+        if (direct_x) {
+            grid_dependency_wait();   // A may be written by the previous grid in the stream
+            if (i_first < nsteps) load_x(i_first, xnext);
+        }
         for (uint32_t i = i_first; i < nsteps; i += di) {
             const uint32_t j = i % Cfg::SA, b = i % Cfg::SB, f = i % Cfg::NP;
-            if (!warp_wait8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
+            uint2 xcur[2] = {xnext[0], xnext[1]};
+            if (direct_x) {
+                if (i + di < nsteps) load_x(i + di, xnext);
+            } else if (!warp_wait8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) {
+                break;
+            }
             if (i >= Cfg::SB) {   // term slot b last held step i - SB
                 const uint32_t q = i - Cfg::SB;
                 if (!warp_wait8(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline, abort_flag,
@@ -461,8 +479,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             const uint8_t* xs = sX + j * Cfg::kXBytes;
             uint8_t* bs = sB + b * Cfg::kBBytes;
             float* inv = sInv + f * TN;
-            if (whole_warp) {
-                for (uint32_t t = 0; t < toks_valid; ++t) split_token_w32<TN>(xs, bs, inv, t, lane);
+            if (direct_x) {
+                for (uint32_t t = 0; t < toks_valid; ++t) split_token_w32<TN>(xcur[t], bs, inv, t, lane);
             } else {
                 // rows past the last token are TMA zero fill: splitting them is harmless
                 for (uint32_t t0 = t_first; t0 < toks_valid; t0 += dt)
@@ -475,7 +493,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 // weights, and step i - NS's MMAs (this warp's, awaited above) freed it.
                 bool ok = true;
                 if (lane == 0) {
-                    mbar_arrive(xempty0 + 8u * j);
+                    if (!direct_x) mbar_arrive(xempty0 + 8u * j);
                     ok = mbar_wait(wfull0 + 8u * b, (i / STAGES) & 1, deadline, abort_flag,
                                    &g_tc8_status, kWaitW);
                     if (ok) {
@@ -575,7 +593,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
 }
 
 using Tc8KernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*, uint32_t,
-                             uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+                             const uint16_t*, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t,
+                             uint64_t);
 struct Tc8Instance {
     uint32_t tn, stages;
     Tc8KernelFn fn;
@@ -656,7 +675,8 @@ int launch_tc8(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kTc8Instances[inst].fn, mw, ma, g.scale,
-                           static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, p.split_k,
+                           static_cast<__nv_bfloat16*>(g.C), g.ldc,
+                           static_cast<const uint16_t*>(g.A), g.lda, g.M, g.N, g.K, p.split_k,
                            timeout_ns);
     if (e != cudaSuccess) {
         cudaGetLastError();
