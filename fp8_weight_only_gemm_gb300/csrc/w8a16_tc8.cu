@@ -200,8 +200,8 @@ __device__ __forceinline__ void split_token_w32(uint2 av, uint8_t* bs, float* in
         if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
         else bad = true;   // NaN or infinity
     }
-#pragma unroll
-    for (uint32_t o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    // the block maximum: |x| >= 0 orders as its bit pattern, one warp reduction
+    mx = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mx)));
     const int E = block_exponent(mx);
     float p1, p2;
     split_scales(E, p1, p2);
@@ -554,8 +554,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             }
         } else {
             cluster_wait();
-            uint32_t owner = 0;
-            while (owner + 1 < split_k && owned_row0(owner + 1, split_k) <= row) ++owner;
+            // the last rank r with r * 128 / split_k <= row (no division by split_k)
+            const uint32_t owner = ((row + 1) * split_k - 1) / kTcRows;
             const uint32_t lrow = row - owned_row0(owner, split_k);
             const uint32_t off =
                 ((rank * TN + fh * Cfg::kTokPerFold) * tc_red_rows(split_k) + lrow) * 4u;
@@ -580,13 +580,20 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     const bool got = warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
     if (got) {
         const uint32_t total = my_rows * toks_valid;
+        const uint32_t red_rows = tc_red_rows(split_k);
         for (uint32_t idx = threadIdx.x; idx < total; idx += Cfg::kThreads) {
             const uint32_t tok = idx / my_rows, lr = idx % my_rows;
             const uint32_t r = my_row0 + lr;
             if (r >= rows_valid) continue;
+            // all ranks' partials are loaded at once, then added in rank order
+            float part[16];
+#pragma unroll
+            for (uint32_t src = 0; src < 16; ++src)
+                part[src] = src < split_k ? sRed[(src * TN + tok) * red_rows + lr] : 0.f;
             float v = 0.f;
-            for (uint32_t src = 0; src < split_k; ++src)
-                v += sRed[(src * TN + tok) * tc_red_rows(split_k) + lr];
+#pragma unroll
+            for (uint32_t src = 0; src < 16; ++src)
+                if (src < split_k) v += part[src];
             C[static_cast<size_t>(token0 + tok) * ldc + tile * kTcRows + r] = __float2bfloat16_rn(v);
         }
     }
