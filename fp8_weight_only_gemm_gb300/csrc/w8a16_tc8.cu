@@ -517,13 +517,22 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
 #pragma unroll
         for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) acc[t] = 0.f;
         const float* srow = scale + static_cast<size_t>(tile) * ksteps + s_begin;
+        // The block scales of this CTA's steps, 32 per register (lane l holds step
+        // 32c + l of chunk c), read at once instead of one load per step: under a
+        // programmatic launch the caller guarantees they are not being written.
+        float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
+        float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
         for (uint32_t i = 0; i < nsteps; ++i) {
+            if (i != 0 && (i & 31u) == 0) {
+                sc_cur = sc_next;
+                sc_next = i + 32u + lane < nsteps ? __ldg(srow + i + 32u + lane) : 0.f;
+            }
             const uint32_t p = i % Cfg::NP;
             if (!warp_wait8(mdone0 + 8u * (i % Cfg::ND), (i / Cfg::ND) & 1, deadline, abort_flag,
                             kWaitMdone))
                 break;
             tc_fence_after();
-            const float sc = __ldg(srow + i);
+            const float sc = __shfl_sync(0xFFFFFFFFu, sc_cur, i & 31u);
             const uint32_t pcol = tP + lane_bits + p * 2 * TN + fh * Cfg::kTokPerFold;
             const float* inv = sInv + p * TN + fh * Cfg::kTokPerFold;
 #pragma unroll

@@ -80,11 +80,12 @@ enum {
 /* Call flags (w8a16_gemm_ex). */
 enum {
     /* Programmatic dependent launch: the kernel may start while the work queued
-     * before it on the stream is still running, and streams its first weight
-     * tiles before waiting for that work to finish; A, block_scale and C are only
-     * touched after the wait. Consecutive calls then overlap one call's start-up
-     * with the previous call's tail. Contract: no work queued earlier on the
-     * stream may write W (weights are read-only in inference). */
+     * before it on the stream is still running, and reads its first weight tiles
+     * and its block scales before waiting for that work to finish; A and C are
+     * only touched after the wait. Consecutive calls then overlap one call's
+     * start-up with the previous call's tail. Contract: no work queued earlier on
+     * the stream may write W or block_scale (the quantised weights are read-only
+     * in inference). */
     W8A16_FLAG_PDL = 1u
 };
 
