@@ -70,7 +70,6 @@ struct TcCfg {
     static constexpr uint32_t NF = tc_fold_warps(TN);
     static constexpr uint32_t NA = tc_a_bufs(TN);
     static constexpr uint32_t NP = tc_p_bufs(TN);
-    static constexpr uint32_t kThreads = tc_threads(TN);
     static constexpr uint32_t kConv0 = 3;                       // first converter warp
     static constexpr uint32_t kFold0 = kConv0 + NC;             // first fold warp
     static constexpr uint32_t kTokPerFold = TN * 4 / NF;        // tokens per fold thread
@@ -425,6 +424,22 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)   // tokens past M are not sent
                 if (fh * Cfg::kTokPerFold + t < toks_valid)
                     st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+            // This CTA's own rows: the thread holding row `row` of the tile (and
+            // tokens fh*kTokPerFold..) adds the ranks' partials in rank order.
+            if (warp_wait(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed) && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
+                const uint32_t lr = row - my_row0;
+                const uint32_t red_rows = tc_red_rows(split_k);
+                const uint32_t slot = TN * red_rows;   // floats between ranks
+                for (uint32_t t = fh * Cfg::kTokPerFold;
+                     t < toks_valid && t < (fh + 1) * Cfg::kTokPerFold; ++t) {
+                    const float* src_p = sRed + t * red_rows + lr;
+                    float v = 0.f;
+#pragma unroll 4
+                    for (uint32_t src = 0; src < split_k; ++src) v += src_p[src * slot];
+                    C[static_cast<size_t>(token0 + t) * ldc + tile * kTcRows + row] =
+                        __float2bfloat16_rn(v);
+                }
+            }
         }
     }
 
@@ -435,29 +450,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
-    if (split_k == 1) return;
 
-    // Each rank sums the rows it owns over the slots in rank (= K) order.
-    const bool got = warp_wait(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
-    if (got) {
-        const uint32_t total = my_rows * toks_valid;
-        const uint32_t red_rows = tc_red_rows(split_k);
-        for (uint32_t idx = threadIdx.x; idx < total; idx += Cfg::kThreads) {
-            const uint32_t tok = idx / my_rows, lr = idx % my_rows;
-            const uint32_t r = my_row0 + lr;
-            if (r >= rows_valid) continue;
-            // all ranks' partials are loaded at once, then added in rank order
-            float part[16];
-#pragma unroll
-            for (uint32_t src = 0; src < 16; ++src)
-                part[src] = src < split_k ? sRed[(src * TN + tok) * red_rows + lr] : 0.f;
-            float v = 0.f;
-#pragma unroll
-            for (uint32_t src = 0; src < 16; ++src)
-                if (src < split_k) v += part[src];
-            C[static_cast<size_t>(token0 + tok) * ldc + tile * kTcRows + r] = __float2bfloat16_rn(v);
-        }
-    }
 }
 
 // One CTA, one thread: waits on an mbarrier nothing arrives on, so the bounded

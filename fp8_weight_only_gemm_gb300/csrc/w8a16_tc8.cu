@@ -49,7 +49,6 @@ struct T8Cfg {
     static constexpr uint32_t NP = tc8_p_bufs(TN);         // TMEM product buffers (2 TN cols)
     static constexpr uint32_t NS = tc8_split_warps(TN);
     static constexpr uint32_t NF = tc8_fold_warps(TN);
-    static constexpr uint32_t kThreads = tc8_threads(TN);
     static constexpr uint32_t kTmemCols = tc8_tmem_cols(TN);
     static constexpr uint32_t kXBytes = TN * kKStep * 2;
     static constexpr uint32_t kBBytes = 2 * TN * kKStep;
@@ -574,6 +573,22 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)   // tokens past M are not sent
                 if (fh * Cfg::kTokPerFold + t < toks_valid)
                     st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+            // This CTA's own rows: the thread holding row `row` of the tile (and
+            // tokens fh*kTokPerFold..) adds the ranks' partials in rank order.
+            if (warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed) && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
+                const uint32_t lr = row - my_row0;
+                const uint32_t red_rows = tc_red_rows(split_k);
+                const uint32_t slot = TN * red_rows;   // floats between ranks
+                for (uint32_t t = fh * Cfg::kTokPerFold;
+                     t < toks_valid && t < (fh + 1) * Cfg::kTokPerFold; ++t) {
+                    const float* src_p = sRed + t * red_rows + lr;
+                    float v = 0.f;
+#pragma unroll 4
+                    for (uint32_t src = 0; src < split_k; ++src) v += src_p[src * slot];
+                    C[static_cast<size_t>(token0 + t) * ldc + tile * kTcRows + row] =
+                        __float2bfloat16_rn(v);
+                }
+            }
         }
     }
 
@@ -584,28 +599,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         tc_fence_after();
         tmem_dealloc(tP, Cfg::kTmemCols);
     }
-    if (split_k == 1) return;
 
-    const bool got = warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
-    if (got) {
-        const uint32_t total = my_rows * toks_valid;
-        const uint32_t red_rows = tc_red_rows(split_k);
-        for (uint32_t idx = threadIdx.x; idx < total; idx += Cfg::kThreads) {
-            const uint32_t tok = idx / my_rows, lr = idx % my_rows;
-            const uint32_t r = my_row0 + lr;
-            if (r >= rows_valid) continue;
-            // all ranks' partials are loaded at once, then added in rank order
-            float part[16];
-#pragma unroll
-            for (uint32_t src = 0; src < 16; ++src)
-                part[src] = src < split_k ? sRed[(src * TN + tok) * red_rows + lr] : 0.f;
-            float v = 0.f;
-#pragma unroll
-            for (uint32_t src = 0; src < 16; ++src)
-                if (src < split_k) v += part[src];
-            C[static_cast<size_t>(token0 + tok) * ldc + tile * kTcRows + r] = __float2bfloat16_rn(v);
-        }
-    }
 }
 
 using Tc8KernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*, uint32_t,
