@@ -36,22 +36,21 @@ constexpr uint32_t kMaxDynSmem = 232448;   // per-CTA dynamic shared memory limi
 // fold warps (step products -> FP32 accumulators).
 constexpr uint32_t tc_conv_warps(uint32_t tn) { return tn <= 32 ? 16u : 8u; }
 constexpr uint32_t tc_fold_warps(uint32_t tn) { return tn <= 32 ? 4u : 8u; }
+// + one warp whose lane 0 is the second MMA issuer (odd steps)
 constexpr uint32_t tc_threads(uint32_t tn) {
-    return 96u + 32u * (tc_conv_warps(tn) + tc_fold_warps(tn));
+    return 128u + 32u * (tc_conv_warps(tn) + tc_fold_warps(tn));
 }
 // Activation ring depth per token tile (its slots are held until the MMA that
 // reads them completes; the weight ring's are released as soon as converted).
 constexpr uint32_t tc_act_stages(uint32_t tn) {
-    return tn == 16 ? 8u : tn == 32 ? 4u : tn == 64 ? 3u : 2u;
+    return tn == 16 ? 8u : tn == 32 ? 4u : 2u;   // even: two MMA issuers alternate steps
 }
 // TMEM: NA operand buffers of 64 columns (one BF16 128x128 weight tile) and NP
 // product buffers of TN FP32 columns.
 constexpr uint32_t tc_tmem_cols(uint32_t tn) { return tn <= 64 ? 256u : 512u; }
 constexpr uint32_t tc_p_bufs(uint32_t tn) { return tn == 16 ? 4u : 2u; }
-constexpr uint32_t tc_a_bufs(uint32_t tn) {
-    return (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u > 4u
-               ? 4u
-               : (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u;
+constexpr uint32_t tc_a_bufs(uint32_t tn) {   // even: two MMA issuers alternate steps
+    return (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u >= 4u ? 4u : 2u;
 }
 // Split-K receive buffer of one CTA: a slot per cluster rank holding the rows
 // this CTA owns (at most ceil(128/split)) x TN FP32 partials.

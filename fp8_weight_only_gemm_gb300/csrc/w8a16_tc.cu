@@ -80,6 +80,10 @@ struct TcCfg {
     static_assert(kKPerConv == 32 || kKPerConv == 64, "converter K slice");
     static_assert(kTokPerFold % 8 == 0, "fold loads are whole x8 column groups");
     static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
+    // Two MMA issuers take alternate steps; each waits only on steps of its own
+    // parity, so a slot index it waits on must recur on its own steps.
+    static_assert(SA % 2 == 0 && NA % 2 == 0 && NP % 2 == 0, "rings of even depth");
+    static constexpr uint32_t kIssuer2 = kFold0 + NF;        // warp of the second MMA issuer
 };
 
 // Relaxed arrive: the only state peers touch before the matching wait is the
@@ -191,6 +195,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             if (addr >= wempty0 && addr < xfull0) count = Cfg::NC;        // converters
             else if (addr >= tfull0 && addr < mdone0) count = Cfg::NC;    // converters
             else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF; // fold warps
+            else if (addr == done_bar) count = 2;                           // MMA issuers
             mbar_init(addr, count);
         }
         if (lane == 0) *abort_flag = 0;
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     const uint32_t row = quarter * 32 + lane;              // weight row within the tile
     const uint32_t lane_bits = (quarter * 32) << 16;
     const bool is_conv = warp >= Cfg::kConv0 && warp < Cfg::kFold0;
-    const bool is_fold = warp >= Cfg::kFold0;
+    const bool is_fold = warp >= Cfg::kFold0 && warp < Cfg::kFold0 + Cfg::NF;
     const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
 
     if (warp == 0) {
@@ -281,11 +286,15 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             }
             drain_ring(xfull0, Cfg::SA, issued, timeout_ns);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == Cfg::kIssuer2) {
+        // --------------------------------------------------------- MMA issuers
+        // Two threads, even and odd steps: one thread's waits and fence overlap
+        // the other's MMAs, so the tensor pipe rather than one issuing thread
+        // sets the pace. Each commits its own steps (a commit covers the
+        // issuing thread's MMAs only).
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kTcRows, TN);
-            for (uint32_t i = 0; i < nsteps; ++i) {
+            for (uint32_t i = (warp == 1 ? 0u : 1u); i < nsteps; i += 2) {
                 const uint32_t a = i % Cfg::NA, p = i % Cfg::NP, j = i % Cfg::SA;
                 if (!mbar_wait(tfull0 + 8u * a, (i / Cfg::NA) & 1, deadline, abort_flag,
                                &g_tc_status, kWaitAFull))

@@ -111,7 +111,7 @@ def test_plans_for_the_workloads(lib, M, N, K, tn):
     if p["variant"] == binding.VARIANT_TC8:
         assert p["block"][0] == 352
     else:
-        assert p["block"][0] == (736 if tn <= 32 else 608)
+        assert p["block"][0] == (768 if tn <= 32 else 640)
     assert p["tmem_cols"] * p["ctas_per_sm"] <= 512
     assert p["smem_bytes"] * p["ctas_per_sm"] <= 232448
 
