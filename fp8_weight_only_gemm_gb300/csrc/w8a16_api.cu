@@ -296,7 +296,12 @@ int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
     uint32_t usable[17];
     for (uint32_t c = 0; c <= 16; ++c)   // splits whose shared memory does not fit are out
         usable[c] = (c >= 1 && v_smem(v, tn, stages, c) <= w8a16::kMaxDynSmem) ? cap[c] : 0u;
-    const uint32_t split = choose_split(row_tiles, token_tiles, ksteps, usable);
+    // The BF16 kernel runs one CTA per SM and is bound by its MMA pipe: once the
+    // tiles cover half the SMs, splitting K only adds waves and reductions.
+    const uint32_t sms = sm_count ? sm_count : 152u;
+    const uint32_t split = (v == W8A16_VARIANT_TC && 2u * row_tiles * token_tiles >= sms)
+                               ? 1u
+                               : choose_split(row_tiles, token_tiles, ksteps, usable);
     fill_tc(v, M, N, tn, stages, split, out);
     return W8A16_OK;
 }
