@@ -124,7 +124,7 @@ bool v_supported(int32_t v, uint32_t tn, uint32_t st) {
 }
 uint32_t default_stages(int32_t v, uint32_t tn) {
     if (v == W8A16_VARIANT_TC8) return tn == 16 ? 4 : tn == 32 ? 6 : 4;   // 16: two CTAs per SM
-    return tn == 16 ? 8 : tn == 32 ? 6 : tn == 64 ? 6 : 4;
+    return tn == 16 ? 8 : tn == 32 ? 4 : tn == 64 ? 6 : 4;
 }
 // The variant the planner uses for a token count: the two-term FP8 kernel while
 // its activation split is cheap (a 16-token tile), the BF16 kernel beyond.

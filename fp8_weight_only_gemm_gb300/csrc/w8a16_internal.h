@@ -47,10 +47,10 @@ constexpr uint32_t tc_act_stages(uint32_t tn) {
 }
 // TMEM: NA operand buffers of 64 columns (one BF16 128x128 weight tile) and NP
 // product buffers of TN FP32 columns.
-constexpr uint32_t tc_tmem_cols(uint32_t tn) { return tn <= 64 ? 256u : 512u; }
+constexpr uint32_t tc_tmem_cols(uint32_t) { return 512u; }   // one CTA per SM
 constexpr uint32_t tc_p_bufs(uint32_t tn) { return tn == 16 ? 4u : 2u; }
 constexpr uint32_t tc_a_bufs(uint32_t tn) {   // even: two MMA issuers alternate steps
-    return (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u >= 4u ? 4u : 2u;
+    return (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u >= 4u ? 4u : 2u;   // 4 for every TN
 }
 // Split-K receive buffer of one CTA: a slot per cluster rank holding the rows
 // this CTA owns (at most ceil(128/split)) x TN FP32 partials.
@@ -58,11 +58,19 @@ constexpr uint32_t tc_red_rows(uint32_t split) { return (kTcRows + split - 1) / 
 constexpr uint32_t tc_red_bytes(uint32_t tn, uint32_t split) {
     return split <= 1 ? 0u : split * tc_red_rows(split) * tn * 4u;
 }
+// A CTA that allocates all 512 TMEM columns must be alone on its SM (a second
+// one would block in tcgen05.alloc): its dynamic shared memory is padded so that
+// two can never fit in the SM's 228 KiB.
+constexpr uint32_t kAloneSmem = 116u * 1024u;
+constexpr uint32_t alone_if_full_tmem(uint32_t bytes, uint32_t tmem_cols) {
+    return tmem_cols >= 512u && bytes < kAloneSmem ? kAloneSmem : bytes;
+}
 // Dynamic shared memory: 1 KiB alignment slack, the weight ring (`stages`
 // 16 KiB slots), the activation ring, the receive buffer, barriers and flags.
 constexpr uint32_t tc_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
-    return 1024u + stages * kTcRows * kKStep + tc_act_stages(tn) * tn * kKStep * 2u +
-           tc_red_bytes(tn, split) + 1024u;
+    return alone_if_full_tmem(1024u + stages * kTcRows * kKStep + tc_act_stages(tn) * tn * kKStep * 2u +
+                                  tc_red_bytes(tn, split) + 1024u,
+                              tc_tmem_cols(tn));
 }
 
 // FP8-datapath variant (TC8): E4M3 weights straight from the TMA ring into
@@ -79,9 +87,10 @@ constexpr uint32_t tc8_tmem_cols(uint32_t tn) {
     return tc8_p_bufs(tn) * 2u * tn <= 128u ? 128u : tc8_p_bufs(tn) * 2u * tn <= 256u ? 256u : 512u;
 }
 constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
-    return 1024u + stages * kTcRows * kKStep + tc8_b_stages(tn) * 2u * tn * kKStep +
-           tc8_act_stages(tn) * tn * kKStep * 2u + tc8_p_bufs(tn) * tn * 4u +
-           tc_red_bytes(tn, split) + 1024u;
+    return alone_if_full_tmem(1024u + stages * kTcRows * kKStep + tc8_b_stages(tn) * 2u * tn * kKStep +
+                                  tc8_act_stages(tn) * tn * kKStep * 2u + tc8_p_bufs(tn) * tn * 4u +
+                                  tc_red_bytes(tn, split) + 1024u,
+                              tc8_tmem_cols(tn));
 }
 
 // Kernel launchers (implemented in the kernel translation units). They assume

@@ -66,9 +66,9 @@ struct TcCfg {
     static constexpr uint32_t kTmemCols = tc_tmem_cols(TN);
     static constexpr uint32_t NC = tc_conv_warps(TN);
     static constexpr uint32_t kKPerConv = kKStep * 4 / NC;     // K of a step per converter warp
-    static constexpr uint32_t ND = SA > 4 ? SA : 4;            // MMA-completion barriers
-    static constexpr uint32_t NF = tc_fold_warps(TN);
     static constexpr uint32_t NA = tc_a_bufs(TN);
+    static constexpr uint32_t ND = SA > NA ? SA : NA;          // MMA-completion barriers (>= 4)
+    static constexpr uint32_t NF = tc_fold_warps(TN);
     static constexpr uint32_t NP = tc_p_bufs(TN);
     static constexpr uint32_t kConv0 = 3;                       // first converter warp
     static constexpr uint32_t kFold0 = kConv0 + NC;             // first fold warp

@@ -216,63 +216,86 @@ __device__ __forceinline__ void split_token_w32(uint2 av, uint8_t* bs, float* in
     if (lane == 0) inv[t] = fold_factor(E, mx);
 }
 
-// Split four tokens' blocks (t0..t0+3), 8 lanes per token, 16 values per lane:
-// lane c of a token holds K 8c..8c+7 and 64+8c..64+8c+7 (16-byte chunk c of each
-// BF16 box, so the 8 lanes of a token read one 128-byte row without conflicts).
-template <uint32_t TN>
+// Split P passes of four tokens' blocks (tokens t0 + p*dt .. +3 for p < P), 8 lanes
+// per token, 16 values per lane: lane c of a token holds K 8c..8c+7 and
+// 64+8c..64+8c+7 (16-byte chunk c of each BF16 box, so the 8 lanes of a token read
+// one 128-byte row without conflicts). All loads come first and all stores last,
+// so the P passes' dependency chains interleave.
+template <uint32_t TN, uint32_t P>
 __device__ __forceinline__ void split_tokens_w8(const uint8_t* xs, uint8_t* bs, float* inv,
-                                                uint32_t t0, uint32_t lane) {
+                                                uint32_t t0, uint32_t dt, uint32_t lane) {
     const uint32_t tt = lane >> 3, c = lane & 7;
-    const uint32_t t = t0 + tt, sw7 = t & 7;
-    const uint8_t* xr = xs + t * 128 + ((c ^ sw7) << 4);
-    const uint4 a0 = *reinterpret_cast<const uint4*>(xr);
-    const uint4 a1 = *reinterpret_cast<const uint4*>(xr + TN * 128);
-    const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    float x[16];
+    uint32_t w[P][8];
 #pragma unroll
-    for (uint32_t e = 0; e < 8; ++e) {
-        x[2 * e] = __uint_as_float(w[e] << 16);
-        x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    for (uint32_t p = 0; p < P; ++p) {
+        const uint32_t t = t0 + p * dt + tt;
+        const uint8_t* xr = xs + t * 128 + ((c ^ (t & 7)) << 4);
+        const uint4 a0 = *reinterpret_cast<const uint4*>(xr);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(xr + TN * 128);
+        w[p][0] = a0.x; w[p][1] = a0.y; w[p][2] = a0.z; w[p][3] = a0.w;
+        w[p][4] = a1.x; w[p][5] = a1.y; w[p][6] = a1.z; w[p][7] = a1.w;
     }
-    float mx = 0.f;
-    bool bad = false;
+    float mx[P], x[P][16];
+    bool bad[P];
 #pragma unroll
-    for (uint32_t e = 0; e < 16; ++e) {
-        const float a = fabsf(x[e]);
-        if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
-        else bad = true;   // NaN or infinity
+    for (uint32_t p = 0; p < P; ++p) {
+        mx[p] = 0.f;
+        bad[p] = false;
+#pragma unroll
+        for (uint32_t e = 0; e < 8; ++e) {
+            x[p][2 * e] = __uint_as_float(w[p][e] << 16);
+            x[p][2 * e + 1] = __uint_as_float(w[p][e] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (uint32_t e = 0; e < 16; ++e) {
+            const float a = fabsf(x[p][e]);
+            if (a <= 3.4028235e38f) mx[p] = fmaxf(mx[p], a);
+            else bad[p] = true;   // NaN or infinity
+        }
     }
 #pragma unroll
-    for (uint32_t o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    const int E = block_exponent(mx);
-    float p1, p2;
-    split_scales(E, p1, p2);
+    for (uint32_t o = 4; o > 0; o >>= 1)
 #pragma unroll
-    for (uint32_t e = 0; e < 16; ++e) x[e] = (x[e] * p1) * p2;
-    uint32_t hw[4], lw[4];
+        for (uint32_t p = 0; p < P; ++p) mx[p] = fmaxf(mx[p], __shfl_xor_sync(0xFFFFFFFFu, mx[p], o));
+    int E[P];
 #pragma unroll
-    for (uint32_t q = 0; q < 4; ++q) {
-        two_terms4(x + 4 * q, hw[q], lw[q]);
-        if (bad) hw[q] = 0x7F7F7F7Fu;   // a non-finite value: NaN codes
+    for (uint32_t p = 0; p < P; ++p) {
+        E[p] = block_exponent(mx[p]);
+        float p1, p2;
+        split_scales(E[p], p1, p2);
+#pragma unroll
+        for (uint32_t e = 0; e < 16; ++e) x[p][e] = (x[p][e] * p1) * p2;
     }
+    uint32_t hw[P][4], lw[P][4];
+#pragma unroll
+    for (uint32_t p = 0; p < P; ++p)
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q) {
+            two_terms4(x[p] + 4 * q, hw[p][q], lw[p][q]);
+            if (bad[p]) hw[p][q] = 0x7F7F7F7Fu;   // a non-finite value: NaN codes
+        }
     // E4M3 rows t (hi) and TN + t (lo), 128 bytes each, 128-byte swizzle: K 8c.. is
     // 8 bytes in chunk c/2, K 64+8c.. in chunk 4 + c/2. Odd tokens store their
     // second half first so that the two tokens of a half-warp write disjoint banks.
-    const uint32_t posA = (((c >> 1) ^ sw7) << 4) + ((c & 1) << 3);
-    const uint32_t posB = ((((c >> 1) + 4) ^ sw7) << 4) + ((c & 1) << 3);
     const bool odd = tt & 1;
-    const uint32_t p_1 = odd ? posB : posA, p_2 = odd ? posA : posB;
-    const uint2 h_1 = odd ? make_uint2(hw[2], hw[3]) : make_uint2(hw[0], hw[1]);
-    const uint2 h_2 = odd ? make_uint2(hw[0], hw[1]) : make_uint2(hw[2], hw[3]);
-    const uint2 l_1 = odd ? make_uint2(lw[2], lw[3]) : make_uint2(lw[0], lw[1]);
-    const uint2 l_2 = odd ? make_uint2(lw[0], lw[1]) : make_uint2(lw[2], lw[3]);
-    uint8_t* rh = bs + t * 128;
-    uint8_t* rl = bs + (TN + t) * 128;
-    *reinterpret_cast<uint2*>(rh + p_1) = h_1;
-    *reinterpret_cast<uint2*>(rh + p_2) = h_2;
-    *reinterpret_cast<uint2*>(rl + p_1) = l_1;
-    *reinterpret_cast<uint2*>(rl + p_2) = l_2;
-    if (c == 0) inv[t] = fold_factor(E, mx);
+#pragma unroll
+    for (uint32_t p = 0; p < P; ++p) {
+        const uint32_t t = t0 + p * dt + tt, sw7 = t & 7;
+        const uint32_t posA = (((c >> 1) ^ sw7) << 4) + ((c & 1) << 3);
+        const uint32_t posB = ((((c >> 1) + 4) ^ sw7) << 4) + ((c & 1) << 3);
+        const uint32_t p_1 = odd ? posB : posA, p_2 = odd ? posA : posB;
+        const uint2 h_1 = odd ? make_uint2(hw[p][2], hw[p][3]) : make_uint2(hw[p][0], hw[p][1]);
+        const uint2 h_2 = odd ? make_uint2(hw[p][0], hw[p][1]) : make_uint2(hw[p][2], hw[p][3]);
+        const uint2 l_1 = odd ? make_uint2(lw[p][2], lw[p][3]) : make_uint2(lw[p][0], lw[p][1]);
+        const uint2 l_2 = odd ? make_uint2(lw[p][0], lw[p][1]) : make_uint2(lw[p][2], lw[p][3]);
+        uint8_t* rh = bs + t * 128;
+        uint8_t* rl = bs + (TN + t) * 128;
+        *reinterpret_cast<uint2*>(rh + p_1) = h_1;
+        *reinterpret_cast<uint2*>(rh + p_2) = h_2;
+        *reinterpret_cast<uint2*>(rl + p_1) = l_1;
+        *reinterpret_cast<uint2*>(rl + p_2) = l_2;
+        if (c == 0) inv[t] = fold_factor(E[p], mx[p]);
+    }
 }
 
 template <uint32_t TN, uint32_t STAGES>
@@ -482,8 +505,12 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 for (uint32_t t = 0; t < toks_valid; ++t) split_token_w32<TN>(xcur[t], bs, inv, t, lane);
             } else {
                 // rows past the last token are TMA zero fill: splitting them is harmless
-                for (uint32_t t0 = t_first; t0 < toks_valid; t0 += dt)
-                    split_tokens_w8<TN>(xs, bs, inv, t0, lane);
+                uint32_t t0 = t_first;
+                if constexpr (TN >= 32) {   // two passes at once where registers allow
+                    for (; t0 + dt < toks_valid; t0 += 2 * dt)
+                        split_tokens_w8<TN, 2>(xs, bs, inv, t0, dt, lane);
+                }
+                for (; t0 < toks_valid; t0 += dt) split_tokens_w8<TN, 1>(xs, bs, inv, t0, dt, lane);
             }
             fence_proxy_async_smem();   // the tensor core reads these terms
             __syncwarp();
