@@ -55,8 +55,11 @@ constexpr uint32_t tc_a_bufs(uint32_t tn) {   // even: two MMA issuers alternate
 // Split-K receive buffer of one CTA: a slot per cluster rank holding the rows
 // this CTA owns (at most ceil(128/split)) x TN FP32 partials.
 constexpr uint32_t tc_red_rows(uint32_t split) { return (kTcRows + split - 1) / split; }
+// Receive layout [rank][row][token]: a row's TN partials are contiguous (16-byte
+// pushes), rows padded by 4 floats so that consecutive rows start in different banks.
+constexpr uint32_t tc_red_stride(uint32_t tn) { return tn + 4u; }
 constexpr uint32_t tc_red_bytes(uint32_t tn, uint32_t split) {
-    return split <= 1 ? 0u : split * tc_red_rows(split) * tn * 4u;
+    return split <= 1 ? 0u : split * tc_red_rows(split) * tc_red_stride(tn) * 4u;
 }
 // A CTA that allocates all 512 TMEM columns must be alone on its SM (a second
 // one would block in tcgen05.alloc): its dynamic shared memory is padded so that

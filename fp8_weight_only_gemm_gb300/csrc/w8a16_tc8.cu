@@ -84,11 +84,31 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, uint32_t remote_bar, float a) {
+__device__ __forceinline__ void st_async_v4f32(uint32_t remote_addr, uint32_t remote_bar, float a,
+                                               float b, float c, float d) {
     asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr),
-        "f"(a), "r"(remote_bar)
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            remote_addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
         : "memory");
+}
+
+// Bytes pushed per row by all of its fold threads (token groups of kTokPerFold).
+template <uint32_t TN, uint32_t TPF>
+__device__ __forceinline__ uint32_t red_row_bytes(uint32_t toks_valid);
+
+// Bytes one fold thread pushes per row: its token group's valid tokens, rounded up
+// to whole 16-byte groups of 4.
+__device__ __forceinline__ uint32_t push_bytes(uint32_t toks_valid, uint32_t first, uint32_t count) {
+    const uint32_t v = toks_valid > first ? min(toks_valid - first, count) : 0u;
+    return 16u * ((v + 3u) / 4u);
+}
+template <uint32_t TN, uint32_t TPF>
+__device__ __forceinline__ uint32_t red_row_bytes(uint32_t toks_valid) {
+    uint32_t b = 0;
+#pragma unroll
+    for (uint32_t first = 0; first < TN; first += TPF) b += push_bytes(toks_valid, first, TPF);
+    return b;
 }
 // Generic-proxy shared-memory writes become visible to the tensor core's reads.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -364,7 +384,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         __syncwarp();
     }
     if (threadIdx.x == 0) {
-        if (split_k > 1) mbar_arrive_expect_tx(red_bar, split_k * my_rows * toks_valid * 4u);
+        if (split_k > 1)
+            mbar_arrive_expect_tx(red_bar, split_k * my_rows * red_row_bytes<TN, Cfg::kTokPerFold>(toks_valid));
         // First weight tiles before anything else; weights are requested before
         // waiting on the previous grid (under a programmatic launch the caller
         // guarantees that grid does not write W).
@@ -592,28 +613,42 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             // the last rank r with r * 128 / split_k <= row (no division by split_k)
             const uint32_t owner = ((row + 1) * split_k - 1) / kTcRows;
             const uint32_t lrow = row - owned_row0(owner, split_k);
+            // receive layout [rank][row][token]: this thread's tokens are contiguous
+            // and go as 16-byte groups; the owner reads them back the same way
             const uint32_t off =
-                ((rank * TN + fh * Cfg::kTokPerFold) * tc_red_rows(split_k) + lrow) * 4u;
+                ((rank * tc_red_rows(split_k) + lrow) * tc_red_stride(TN) + fh * Cfg::kTokPerFold) * 4u;
             const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
             const uint32_t dbar = dsmem_map(red_bar, owner);
+            const uint32_t ngroups = push_bytes(toks_valid, fh * Cfg::kTokPerFold, Cfg::kTokPerFold) / 16u;
 #pragma unroll
-            for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t)   // tokens past M are not sent
-                if (fh * Cfg::kTokPerFold + t < toks_valid)
-                    st_async_f32(dst + 4u * t * tc_red_rows(split_k), dbar, acc[t]);
+            for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)   // groups past M are not sent
+                if (g < ngroups)
+                    st_async_v4f32(dst + 16u * g, dbar, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2],
+                                   acc[4 * g + 3]);
             // This CTA's own rows: the thread holding row `row` of the tile (and
             // tokens fh*kTokPerFold..) adds the ranks' partials in rank order.
-            if (warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed) && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
+            const bool got = warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+            if (got && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
                 const uint32_t lr = row - my_row0;
-                const uint32_t red_rows = tc_red_rows(split_k);
-                const uint32_t slot = TN * red_rows;   // floats between ranks
+                const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats
+                const float* src_row = sRed + lr * tc_red_stride(TN);
                 for (uint32_t t = fh * Cfg::kTokPerFold;
-                     t < toks_valid && t < (fh + 1) * Cfg::kTokPerFold; ++t) {
-                    const float* src_p = sRed + t * red_rows + lr;
-                    float v = 0.f;
+                     t < toks_valid && t < (fh + 1) * Cfg::kTokPerFold; t += 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-                    for (uint32_t src = 0; src < split_k; ++src) v += src_p[src * slot];
-                    C[static_cast<size_t>(token0 + t) * ldc + tile * kTcRows + row] =
-                        __float2bfloat16_rn(v);
+                    for (uint32_t src = 0; src < split_k; ++src) {   // rank order
+                        const float4 q = *reinterpret_cast<const float4*>(src_row + src * rank_stride + t);
+                        v.x += q.x;
+                        v.y += q.y;
+                        v.z += q.z;
+                        v.w += q.w;
+                    }
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (uint32_t u = 0; u < 4; ++u)
+                        if (t + u < toks_valid)
+                            C[static_cast<size_t>(token0 + t + u) * ldc + tile * kTcRows + row] =
+                                __float2bfloat16_rn(vv[u]);
                 }
             }
         }

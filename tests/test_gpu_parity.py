@@ -85,7 +85,7 @@ def test_forced_splits(split_k, M, variant):
 @pytest.mark.parametrize("variant,M,stages,split", [
     (2, 4, 4, 2), (2, 4, 6, 2), (2, 4, 8, 2), (2, 4, 10, 3), (2, 24, 3, 2), (2, 24, 4, 2),
     (2, 24, 6, 2), (2, 24, 8, 3), (2, 48, 4, 2), (2, 48, 6, 2), (2, 48, 8, 3), (2, 100, 4, 2),
-    (2, 100, 6, 1), (2, 100, 6, 2),
+    (2, 100, 6, 1), (2, 100, 4, 3),
     (3, 4, 4, 2), (3, 4, 6, 2), (3, 4, 8, 3), (3, 24, 4, 2), (3, 24, 6, 2), (3, 24, 8, 3),
     (3, 48, 4, 2), (3, 48, 6, 3)])
 def test_stage_instances(variant, M, stages, split):

@@ -152,7 +152,8 @@ def test_plan_variant_validation(lib):
         binding.plan_variant(8, 1024, 1024, binding.VARIANT_TC, stages=5)    # no instance
     # the widest token tile's 6-slot ring leaves room for small split-K receive
     # buffers only
-    assert binding.plan_variant(100, 1024, 2048, binding.VARIANT_TC, split_k=2, stages=6).stages == 6
+    assert binding.plan_variant(100, 1024, 2048, binding.VARIANT_TC, split_k=2, stages=4).stages == 4
+    assert binding.plan_variant(100, 1024, 2048, binding.VARIANT_TC, split_k=1, stages=6).stages == 6
     with pytest.raises(binding.W8A16Error) as e:
         binding.plan_variant(100, 1024, 2048, binding.VARIANT_TC, split_k=14, stages=6)
     assert "shared memory" in str(e.value)
