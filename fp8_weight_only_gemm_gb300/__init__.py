@@ -3,16 +3,19 @@
 C[M, N] (BF16) = A[M, K] (BF16, any row pitch) x dequant(W[N, K] FP8 E4M3, one FP32
 scale per 128x128 block)^T, computed by hand-written tcgen05/TMA kernels in
 ``libw8a16.so`` behind a C ABI (include/w8a16.h). This package is the thin
-Python binding: torch provides device memory and streams only.
+Python binding: torch provides device memory and streams only. The library also
+holds the weight block quantiser that produces W and the block scales.
 """
 from .binding import (FLAG_PDL, Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8,
-                      W8A16Error,
+                      WEIGHTS_BF16, WEIGHTS_F32, W8A16Error,
                       check_args, cluster_capacity, device_status, gemm, gemm_host, gemm_ptr,
                       header_functions, last_error, load, plan_current, plan_for, plan_variant,
-                      selftest_wait_timeout, strerror, version)
+                      quantize_weights, quantize_weights_ptr, selftest_wait_timeout, strerror,
+                      version)
 
 __all__ = ["FLAG_PDL", "Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "VARIANT_TC8",
-           "W8A16Error",
+           "WEIGHTS_BF16", "WEIGHTS_F32", "W8A16Error",
            "check_args", "cluster_capacity", "device_status", "gemm", "gemm_host", "gemm_ptr",
            "header_functions", "last_error", "load", "plan_current", "plan_for", "plan_variant",
-           "selftest_wait_timeout", "strerror", "version"]
+           "quantize_weights", "quantize_weights_ptr", "selftest_wait_timeout", "strerror",
+           "version"]

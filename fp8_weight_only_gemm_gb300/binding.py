@@ -20,6 +20,7 @@ W8A16_OK = 0
 FLAG_PDL = 1
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8 = 0, 1, 2, 3
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
+WEIGHTS_F32, WEIGHTS_BF16 = 0, 1
 
 
 class Plan(ctypes.Structure):
@@ -56,6 +57,7 @@ _SIGS = {
     "w8a16_plan_variant": (_INT, [_U32, _U32, _U32, _I32, _U32, _U32, _U32, ctypes.POINTER(Plan)]),
     "w8a16_gemm_with_plan": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32,
                                     ctypes.POINTER(Plan), _U32, _VP]),
+    "w8a16_quantize_weights": (_INT, [_VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP]),
     "w8a16_last_error": (ctypes.c_char_p, []),
     "w8a16_strerror": (ctypes.c_char_p, [_INT]),
     "w8a16_device_status": (_INT, [_VP, _INT, ctypes.POINTER(_U32), ctypes.POINTER(_U32),
@@ -219,6 +221,37 @@ def gemm_host(A_host, W_host, scale_host, C_host, dA, dW, dScale, dC, *, copy_we
             dScale.data_ptr(), dC.data_ptr(), 1 if copy_weights else 0, _stream_handle(stream))
     _check(rc)
     return C_host
+
+
+def quantize_weights(W, *, stream=None):
+    """(codes uint8 [N, K], block_scale float32 [ceil(N/128), K/128]) of a CUDA
+    float32 or bfloat16 [N, K] weight tensor (rows contiguous, any row pitch)."""
+    import torch
+    if W.dim() != 2 or W.stride(1) != 1:
+        raise ValueError("W must be 2-D with contiguous rows")
+    if W.dtype == torch.float32:
+        wt = WEIGHTS_F32
+    elif W.dtype == torch.bfloat16:
+        wt = WEIGHTS_BF16
+    else:
+        raise TypeError(f"W must be float32 or bfloat16, got {W.dtype}")
+    if not W.is_cuda:
+        raise ValueError("W must be on a CUDA device")
+    N, K = W.shape
+    codes = torch.empty((N, K), dtype=torch.uint8, device=W.device)
+    scale = torch.empty(((N + 127) // 128, K // 128 if K % 128 == 0 else 1), dtype=torch.float32,
+                        device=W.device)
+    with torch.cuda.device(W.device):
+        rc = load().w8a16_quantize_weights(W.data_ptr(), wt, W.stride(0), N, K, codes.data_ptr(),
+                                           scale.data_ptr(), _stream_handle(stream))
+    _check(rc)
+    return codes, scale
+
+
+def quantize_weights_ptr(W_ptr, w_dtype, w_row_stride, N, K, codes_ptr, scale_ptr, stream=0) -> int:
+    """Raw-pointer call (returns the library's code; does not raise)."""
+    return load().w8a16_quantize_weights(W_ptr or None, w_dtype, w_row_stride, N, K, codes_ptr or None,
+                                         scale_ptr or None, stream or None)
 
 
 def device_status(stream=None, clear=False) -> tuple[int, int, int]:

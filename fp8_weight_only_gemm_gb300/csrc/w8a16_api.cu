@@ -407,6 +407,39 @@ int w8a16_check_args(const void* A, uint32_t a_row_stride, const void* W, const 
     return ok();
 }
 
+int w8a16_quantize_weights(const void* W, uint32_t w_dtype, uint32_t w_row_stride, uint32_t N,
+                           uint32_t K, void* codes, float* block_scale, w8a16_stream_t stream) {
+    if (N < 1) return fail(W8A16_ERR_N_ZERO, "w8a16_quantize_weights: n=0 has no rows to quantise");
+    if (K < w8a16::kKStep || K % w8a16::kKStep != 0)
+        return fail(W8A16_ERR_K_BLOCK, "w8a16_quantize_weights: K=" + u(K) +
+                                           " must be a positive multiple of 128 (one scale per 128x128 block)");
+    if (w_row_stride < K)
+        return fail(W8A16_ERR_PITCH, "w8a16_quantize_weights: w_row_stride=" + u(w_row_stride) +
+                                         " must cover K=" + u(K));
+    if (w_row_stride % 4 != 0)
+        return fail(W8A16_ERR_A_PITCH_ALIGN, "w8a16_quantize_weights: w_row_stride=" + u(w_row_stride) +
+                                                 " must be a multiple of 4 (vector loads of 4 values)");
+    if (w_dtype != W8A16_WEIGHTS_F32 && w_dtype != W8A16_WEIGHTS_BF16)
+        return fail(W8A16_ERR_ARG, "w8a16_quantize_weights: unknown weight type " + u(w_dtype));
+    if (N > 0x7FFFFFFFu || K > 0x7FFFFFFFu || (N + 127u) / 128u > 65535u)
+        return fail(W8A16_ERR_RANGE, "w8a16_quantize_weights: N=" + u(N) + " K=" + u(K) + " out of range");
+    if (!W || !codes || !block_scale)
+        return fail(W8A16_ERR_NULL, std::string("w8a16_quantize_weights: NULL ") +
+                                        (!W ? "W" : !codes ? "codes" : "block_scale") + " pointer");
+    const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+    if (addr(W) % 16 || addr(codes) % 4 || addr(block_scale) % 4)
+        return fail(W8A16_ERR_ALIGN,
+                    "w8a16_quantize_weights: alignment (W needs 16 bytes, codes and block_scale 4)");
+    DeviceInfo info;
+    std::string err;
+    int rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    rc = w8a16::launch_quantize(W, w_dtype == W8A16_WEIGHTS_BF16, w_row_stride, N, K, codes, block_scale,
+                                static_cast<cudaStream_t>(stream), &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
 int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
                    const uint32_t* cluster_ctas, w8a16_plan_t* out) {
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_for: NULL plan pointer");

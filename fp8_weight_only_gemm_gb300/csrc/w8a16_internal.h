@@ -107,6 +107,8 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
 // device when launched in clusters of `cluster` CTAs.
 int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
                         std::string* err);
+int launch_quantize(const void* W, bool bf16, uint32_t ldw, uint32_t N, uint32_t K, void* codes,
+                    float* scales, cudaStream_t s, std::string* err);
 int launch_tc8(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
                uint32_t flags, std::string* err);
 int tc8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,

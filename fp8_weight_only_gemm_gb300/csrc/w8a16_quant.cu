@@ -1,0 +1,107 @@
+// Weight block quantiser for sm_103a: FP32 or BF16 W -> E4M3 codes + one FP32
+// scale per 128x128 block, the format the W8A16 GEMM consumes (page
+// "metrale_model_layers/layers/ops/w8a16_gemm_pipelined_m32.rs", doc comment of
+// `w8a16_gemm_pipelined_m32_strided`: W as FP8 E4M3 [N, K], block_scale FP32
+// [N/128, K/128]). Per block: amax = max |w|, scale = amax / 448 (FP32, round to
+// nearest), code = E4M3 round-to-nearest-even of w / scale (FP32 quotient,
+// saturating at +-448); amax = 0 gives scale 0 and codes 0. NaN inputs do not
+// enter amax (fmax ignores them) and encode as the NaN code.
+//
+// One CTA per block, 8 warps x 16 rows, a lane per 4 consecutive columns: each
+// warp instruction reads one 512-byte (FP32) or 256-byte (BF16) row segment and
+// writes 128 code bytes. The block's values stay in registers between the
+// maximum and the encoding, so W is read once: the kernel is bound by HBM.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <string>
+
+#include "w8a16_internal.h"
+
+namespace w8a16 {
+namespace {
+
+constexpr uint32_t kQRows = 128, kQCols = 128, kQWarps = 8, kQRowsPerWarp = kQRows / kQWarps;
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {   // lo -> byte 0
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kQWarps * 32)
+    quantize_blocks_kernel(const void* __restrict__ W, uint32_t ldw, uint32_t N, uint32_t K,
+                           uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    __shared__ float warp_max[kQWarps];
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t kb = blockIdx.x, nb = blockIdx.y;
+    const uint32_t col = kb * kQCols + 4 * lane;
+    const uint32_t row0 = nb * kQRows + warp * kQRowsPerWarp;
+    float v[kQRowsPerWarp][4];
+    float mx = 0.f;
+#pragma unroll
+    for (uint32_t r = 0; r < kQRowsPerWarp; ++r) {
+        const uint32_t row = row0 + r;
+        if (row < N) {
+            const size_t off = static_cast<size_t>(row) * ldw + col;
+            if constexpr (BF16) {
+                const uint2 q = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(W) + off);
+                v[r][0] = __uint_as_float(q.x << 16);
+                v[r][1] = __uint_as_float(q.x & 0xFFFF0000u);
+                v[r][2] = __uint_as_float(q.y << 16);
+                v[r][3] = __uint_as_float(q.y & 0xFFFF0000u);
+            } else {
+                const float4 q = *reinterpret_cast<const float4*>(static_cast<const float*>(W) + off);
+                v[r][0] = q.x;
+                v[r][1] = q.y;
+                v[r][2] = q.z;
+                v[r][3] = q.w;
+            }
+        } else {
+            v[r][0] = v[r][1] = v[r][2] = v[r][3] = 0.f;
+        }
+#pragma unroll
+        for (uint32_t e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(v[r][e]));
+    }
+#pragma unroll
+    for (uint32_t o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (lane == 0) warp_max[warp] = mx;
+    __syncthreads();
+    float amax = warp_max[0];
+#pragma unroll
+    for (uint32_t w = 1; w < kQWarps; ++w) amax = fmaxf(amax, warp_max[w]);
+    const float scale = __fdiv_rn(amax, 448.f);
+    if (threadIdx.x == 0) scales[static_cast<size_t>(nb) * (K / kQCols) + kb] = scale;
+#pragma unroll
+    for (uint32_t r = 0; r < kQRowsPerWarp; ++r) {
+        const uint32_t row = row0 + r;
+        if (row >= N) break;
+        uint32_t word = 0;
+        if (scale != 0.f)
+            word = e4m3x2(__fdiv_rn(v[r][0], scale), __fdiv_rn(v[r][1], scale)) |
+                   (e4m3x2(__fdiv_rn(v[r][2], scale), __fdiv_rn(v[r][3], scale)) << 16);
+        *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(row) * K + col) = word;
+    }
+}
+
+}  // namespace
+
+int launch_quantize(const void* W, bool bf16, uint32_t ldw, uint32_t N, uint32_t K, void* codes,
+                    float* scales, cudaStream_t s, std::string* err) {
+    const dim3 grid(K / kQCols, (N + kQRows - 1) / kQRows, 1);
+    if (bf16)
+        quantize_blocks_kernel<true><<<grid, kQWarps * 32, 0, s>>>(W, ldw, N, K,
+                                                                   static_cast<uint8_t*>(codes), scales);
+    else
+        quantize_blocks_kernel<false><<<grid, kQWarps * 32, 0, s>>>(W, ldw, N, K,
+                                                                    static_cast<uint8_t*>(codes), scales);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = std::string("quantiser launch failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    return W8A16_OK;
+}
+
+}  // namespace w8a16

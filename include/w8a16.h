@@ -203,6 +203,32 @@ W8A16_API int w8a16_gemm_with_plan(const void *A, uint32_t a_row_stride, const v
 /* Message of the last failed call on this host thread ("" if none). */
 W8A16_API const char *w8a16_last_error(void);
 
+/* Weight element types accepted by w8a16_quantize_weights. */
+enum {
+    W8A16_WEIGHTS_F32 = 0,
+    W8A16_WEIGHTS_BF16 = 1
+};
+
+/* Block quantiser: produces the W and block_scale operands of w8a16_gemm from
+ * higher-precision weights. Output format: page "metrale_model_layers/layers/ops/
+ * w8a16_gemm_pipelined_m32.rs", doc comment of `w8a16_gemm_pipelined_m32_strided`
+ * (W as FP8 E4M3 [N][K], block_scale FP32 [N/128][K/128], one scale per 128x128
+ * block). The page does not print the quantiser; our reading, consistent with the
+ * 448 range of E4M3: per block, amax = max |w|; scale = amax / 448 (FP32, round to
+ * nearest); code = E4M3 round-to-nearest-even of w / scale (FP32 quotient),
+ * saturating at +-448; a block with amax = 0 gets scale 0 and all codes 0.
+ *   W           FP32 or BF16 (w_dtype = W8A16_WEIGHTS_*), [N][w_row_stride], first K
+ *               of each row read; device pointer, 16-byte aligned.
+ *   codes       [N][K] E4M3 bytes (row pitch K), 4-byte aligned, written.
+ *   block_scale [ceil(N/128)][K/128] FP32, 4-byte aligned, written.
+ * Checks, before any device work: N >= 1, K a positive multiple of 128,
+ * w_row_stride >= K and a multiple of 4, known w_dtype, non-NULL and aligned
+ * pointers. NaN weights do not enter a block's amax and encode as the NaN code.
+ * Asynchronous on `stream`. */
+W8A16_API int w8a16_quantize_weights(const void *W, uint32_t w_dtype, uint32_t w_row_stride,
+                                     uint32_t N, uint32_t K, void *codes, float *block_scale,
+                                     w8a16_stream_t stream);
+
 /* Fixed description of a W8A16_ERR_* code. */
 W8A16_API const char *w8a16_strerror(int code);
 

@@ -87,6 +87,11 @@ class Oracle:
             _u16p, ctypes.c_uint32, _u8p, _f32p, ctypes.c_uint32, ctypes.c_uint32,
             ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64, _u16p, _f64p, _f64p, ctypes.c_int]
         lib.oracle_w8a16_gemm_samples.restype = ctypes.c_int
+        lib.oracle_e4m3_encode_rne.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode_rne.restype = ctypes.c_uint8
+        lib.oracle_quantize_weights.argtypes = [_f32p, ctypes.c_uint32, ctypes.c_uint32,
+                                                ctypes.c_uint32, _u8p, _f32p]
+        lib.oracle_quantize_weights.restype = ctypes.c_int
         self.lib = lib
 
     # -- scalar codecs -----------------------------------------------------
@@ -98,6 +103,28 @@ class Oracle:
 
     def bf16_rne(self, x: float) -> int:
         return int(self.lib.oracle_double_to_bf16_rne(float(x)))
+
+    def e4m3_encode(self, x: float) -> int:
+        """E4M3 code of the FP32 value x: nearest, ties to even, saturating."""
+        return int(self.lib.oracle_e4m3_encode_rne(float(x)))
+
+    # -- the weight block quantiser -----------------------------------------
+    def quantize_weights(self, W, N, K, w_row_stride=None):
+        """(codes uint8 [N, K], scales float32 [ceil(N/128), K/128]) of the FP32
+        weights W (``N * w_row_stride`` elements)."""
+        import numpy as np
+        ld = K if w_row_stride is None else int(w_row_stride)
+        W = np.ascontiguousarray(np.asarray(W, dtype=np.float32).reshape(-1))
+        if W.size < N * ld:
+            raise ValueError("W too small")
+        codes = np.zeros(N * K, dtype=np.uint8)
+        scales = np.zeros(((N + 127) // 128) * (K // 128), dtype=np.float32)
+        rc = self.lib.oracle_quantize_weights(
+            W.ctypes.data_as(_f32p), ld, N, K, codes.ctypes.data_as(_u8p),
+            scales.ctypes.data_as(_f32p))
+        if rc != 0:
+            raise ValueError(f"oracle_quantize_weights rejected N={N} K={K} ld={ld}")
+        return codes.reshape(N, K), scales.reshape((N + 127) // 128, K // 128)
 
     # -- the GEMM ----------------------------------------------------------
     def gemm(self, A, W, scale, M, N, K, a_row_stride=None, C=None, c_row_stride=None,

@@ -25,6 +25,15 @@
  * max +-448, subnormals m * 2^-9); the scale grid has ceil(N/128) rows, row n
  * using scale row floor(n/128); NaN inputs propagate as in IEEE arithmetic.
  *
+ * It also holds the oracle of the weight block quantiser, the step that makes
+ * W and block_scale (same page: the block layout of `block_scale`, one FP32 scale
+ * per 128x128 block, with E4M3 codes for W). Our reading of the encoding, the
+ * plainest one consistent with it and with the 448 range of E4M3: per block,
+ * amax = max |w|, scale = amax / 448 in FP32, code = e4m3_rne(w / scale) with the
+ * quotient in FP32 and saturation to +-448; a block with amax = 0 gets scale 0
+ * and codes 0. The FP32 divisions are the ones the GPU takes too (a quantised
+ * code is decided in the precision that produces it).
+ *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -pthread (no fast-math).
  */
 #include <math.h>
@@ -294,4 +303,77 @@ int oracle_w8a16_gemm_samples(const uint16_t *A, uint32_t a_row_stride, const ui
     j.exact = exact;
     j.absum = absum;
     return run_threads(&j, count, nthreads, run_samples);
+}
+
+/* ---- E4M3 (FN) encode, round to nearest, ties to even, saturating ----------
+ * The 127 non-negative finite codes 0x00..0x7E decode to increasing values, so
+ * the nearest code of |x| is found by bisection over that ordered list; on an
+ * exact midpoint the code with an even mantissa (code bit 0 clear) wins. Values
+ * beyond 448 saturate to 448; the sign bit is the sign of x (so -0 and negative
+ * values that round to zero give 0x80); NaN gives 0x7F. */
+uint8_t oracle_e4m3_encode_rne(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (oracle_e4m3_to_double((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const double dlo = a - oracle_e4m3_to_double((uint8_t)lo);
+    const double dhi = oracle_e4m3_to_double((uint8_t)hi) - a;
+    int code;
+    if (dlo < dhi)
+        code = lo;
+    else if (dhi < dlo)
+        code = hi;
+    else
+        code = (lo & 1) ? hi : lo; /* tie: even mantissa */
+    return sign | (uint8_t)code;
+}
+
+/* Block quantiser. W: FP32 [N][w_row_stride] (first K of each row used),
+ * codes: [N][K] E4M3, scales: [ceil(N/128)][K/128] FP32. A block's rows stop at N.
+ * Returns 0, or -1 on bad sizes. */
+int oracle_quantize_weights(const float *W, uint32_t w_row_stride, uint32_t N, uint32_t K,
+                            uint8_t *codes, float *scales)
+{
+    if (N == 0 || K == 0 || K % 128 != 0 || w_row_stride < K)
+        return -1;
+    const uint32_t nb_rows = (N + 127) / 128, kb_cols = K / 128;
+    for (uint32_t nb = 0; nb < nb_rows; ++nb) {
+        const uint32_t r1 = (nb + 1) * 128 < N ? (nb + 1) * 128 : N;
+        for (uint32_t kb = 0; kb < kb_cols; ++kb) {
+            float amax = 0.0f;
+            for (uint32_t r = nb * 128; r < r1; ++r)
+                for (uint32_t k = kb * 128; k < kb * 128 + 128; ++k) {
+                    const float v = fabsf(W[(size_t)r * w_row_stride + k]);
+                    if (v > amax)
+                        amax = v;
+                }
+#if ORACLE_MUTANT == 7
+            const float scale = amax / 447.0f; /* mutant: wrong range */
+#else
+            const float scale = amax / 448.0f;
+#endif
+            scales[(size_t)nb * kb_cols + kb] = scale;
+            for (uint32_t r = nb * 128; r < r1; ++r)
+                for (uint32_t k = kb * 128; k < kb * 128 + 128; ++k) {
+                    uint8_t c = 0;
+                    if (scale != 0.0f) {
+                        const float q = W[(size_t)r * w_row_stride + k] / scale;
+                        c = oracle_e4m3_encode_rne(q);
+                    }
+                    codes[(size_t)r * K + k] = c;
+                }
+        }
+    }
+    return 0;
 }

@@ -171,3 +171,32 @@ def test_forced_plan_must_match_shape(lib):
 
 def test_version(lib):
     assert "sm_103a" in binding.version()
+
+
+@pytest.mark.parametrize("args,code,needle", [
+    # (dtype, ldw, N, K)
+    ((0, 256, 0, 256), ERR["N_ZERO"], "n=0"),
+    ((0, 256, 4, 200), ERR["K_BLOCK"], "K=200"),
+    ((0, 200, 4, 256), ERR["PITCH"], "w_row_stride=200"),
+    ((0, 258, 4, 256), ERR["A_PITCH_ALIGN"], "multiple of 4"),
+    ((7, 256, 4, 256), -13, "unknown weight type"),
+])
+def test_quantizer_checks(lib, args, code, needle):
+    dt, ldw, N, K = args
+    rc = binding.quantize_weights_ptr(0x1000, dt, ldw, N, K, 0x2000, 0x3000)
+    assert rc == code and needle in binding.last_error(), binding.last_error()
+
+
+def test_quantizer_pointer_checks(lib):
+    assert binding.quantize_weights_ptr(0, 0, 256, 4, 256, 0x2000, 0x3000) == ERR["NULL"]
+    assert binding.quantize_weights_ptr(0x1008, 0, 256, 4, 256, 0x2000, 0x3000) == ERR["ALIGN"]
+    assert binding.quantize_weights_ptr(0x1000, 0, 256, 4, 256, 0x2002, 0x3000) == ERR["ALIGN"]
+    import torch
+    if not torch.cuda.is_available():
+        assert binding.quantize_weights_ptr(0x1000, 1, 256, 4, 256, 0x2000, 0x3000) == ERR["DEVICE"]
+
+
+def test_quantizer_constants_match_header():
+    text = binding.HEADER.read_text()
+    assert int(re.search(r"W8A16_WEIGHTS_F32\s*=\s*(\d+)", text).group(1)) == binding.WEIGHTS_F32
+    assert int(re.search(r"W8A16_WEIGHTS_BF16\s*=\s*(\d+)", text).group(1)) == binding.WEIGHTS_BF16

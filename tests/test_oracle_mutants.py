@@ -3,7 +3,8 @@ exponent bias, truncation instead of round-to-nearest-even, one scale for every 
 block, a transposed scale grid, W read as [K][N], a dropped last term) and at
 least one pin of tests/test_oracle_pins.py must fail on it. The mistakes live
 behind ORACLE_MUTANT in oracle/w8a16_oracle.c and are compiled only here, into
-a temporary directory."""
+a temporary directory. The seventh plants a wrong range in the weight block
+quantiser (scale = amax / 447)."""
 import pytest
 
 import oracle
@@ -16,6 +17,7 @@ MUTANTS = {
     4: "scale grid read transposed",
     5: "W read as [K][N]",
     6: "last term of the sum dropped",
+    7: "block scale uses 447 instead of 448",
 }
 
 

@@ -25,6 +25,8 @@ import numpy as np
 import pytest
 import torch
 
+import workloads
+
 GOLDEN = Path(__file__).resolve().parent / "golden"
 
 
@@ -263,10 +265,77 @@ def pin_nan_propagation(o):
     assert isnan[:, 7].all() and isnan.sum() == M
 
 
+# ---- weight block quantiser pins ------------------------------------------
+
+def pin_e4m3_encode_round_trip(o):
+    """Every finite code encodes back to itself (the encoder inverts the decoder)."""
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            continue
+        assert o.e4m3_encode(o.e4m3_to_double(c)) == c, hex(c)
+    assert o.e4m3_encode(float("nan")) & 0x7F == 0x7F
+    assert o.e4m3_encode(1e6) == 0x7E and o.e4m3_encode(-1e6) == 0xFE   # saturation
+
+
+def pin_e4m3_encode_ties_vs_torch(o):
+    """Exact midpoints between neighbouring codes round to the even code, and
+    random values round as torch's float8_e4m3fn cast (an independent encoder)."""
+    vals = []
+    for c in range(0x7E):
+        a, b = o.e4m3_to_double(c), o.e4m3_to_double(c + 1)
+        vals += [(a + b) / 2, -(a + b) / 2, a + (b - a) / 3, b - (b - a) / 5]
+    g = torch.Generator().manual_seed(31)
+    vals += (torch.randn(20000, generator=g) * 64).tolist()
+    x = torch.tensor(vals, dtype=torch.float32)
+    ref = x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([o.e4m3_encode(float(v)) for v in x.numpy()], dtype=np.uint8)
+    assert np.array_equal(ref, got), int((ref != got).sum())
+    for c in range(0x7E):   # the tie itself: even mantissa wins
+        mid = (o.e4m3_to_double(c) + o.e4m3_to_double(c + 1)) / 2
+        if float(np.float32(mid)) == mid:
+            assert o.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1), hex(c)
+
+
+def pin_quantizer_vs_recipe(o):
+    """Blocks, ragged N, a zero block and a row pitch: the oracle quantiser equals
+    the input recipe's torch implementation code for code and scale for scale."""
+    g = torch.Generator().manual_seed(32)
+    N, K, ld = 300, 384, 400
+    w = torch.randn(N, ld, generator=g) * 0.02
+    w[128:256, 128:256] = 0.0                                   # one zero block
+    w[5, 7] = 3.0                                               # an outlier
+    codes, scales = o.quantize_weights(w.numpy(), N, K, w_row_stride=ld)
+    rc, rs = workloads.block_quantize_e4m3(w[:, :K].contiguous())
+    assert np.array_equal(codes, rc.numpy())
+    assert np.array_equal(scales, rs.numpy())
+    assert scales[1, 1] == 0.0 and not codes[128:256, 128:256].any()
+
+
+def pin_quantizer_block_maximum(o):
+    """The largest |w| of a block encodes as +-448 and dequantises within one E4M3
+    step of the original: a closed form of scale = amax / 448."""
+    g = torch.Generator().manual_seed(33)
+    w = torch.randn(256, 256, generator=g)
+    codes, scales = o.quantize_weights(w.numpy(), 256, 256)
+    for nb in range(2):
+        for kb in range(2):
+            blk = w[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+            amax = float(blk.abs().max())
+            assert scales[nb, kb] == np.float32(np.float32(amax) / np.float32(448.0))
+            r, c = divmod(int(blk.abs().argmax()), 128)
+            assert codes[nb * 128 + r, kb * 128 + c] & 0x7F == 0x7E
+            deq = np.array([o.e4m3_to_double(int(x)) for x in
+                            codes[nb * 128:(nb + 1) * 128, kb * 128].tolist()]) * scales[nb, kb]
+            step = 2.0 ** np.floor(np.log2(np.maximum(np.abs(blk[:, 0].numpy()), 1e-30))) / 8
+            assert np.all(np.abs(deq - blk[:, 0].numpy()) <= np.maximum(step, 2.0 ** -9 * scales[nb, kb]))
+
+
 PINS = [pin_e4m3_fixed_points, pin_e4m3_all_codes_vs_torch, pin_bf16_fixed_points,
         pin_bf16_vs_torch_on_binary32, pin_hand_worked_example, pin_identity_weights,
         pin_all_ones_closed_form, pin_brute_force_tiny, pin_zero_block,
-        pin_pads_untouched_and_ignored, pin_linearity, pin_nan_propagation]
+        pin_pads_untouched_and_ignored, pin_linearity, pin_nan_propagation,
+        pin_e4m3_encode_round_trip, pin_e4m3_encode_ties_vs_torch, pin_quantizer_vs_recipe,
+        pin_quantizer_block_maximum]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
