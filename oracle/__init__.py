@@ -92,6 +92,13 @@ class Oracle:
         lib.oracle_quantize_weights.argtypes = [_f32p, ctypes.c_uint32, ctypes.c_uint32,
                                                 ctypes.c_uint32, _u8p, _f32p]
         lib.oracle_quantize_weights.restype = ctypes.c_int
+        lib.oracle_quantize_activations.argtypes = [_u16p, ctypes.c_uint32, ctypes.c_uint32,
+                                                    ctypes.c_uint32, _u8p, _f32p]
+        lib.oracle_quantize_activations.restype = ctypes.c_int
+        lib.oracle_w8a8_gemm.argtypes = [
+            _u8p, ctypes.c_uint32, _f32p, _u8p, _f32p, _u16p, ctypes.c_uint32,
+            ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _f64p, _f64p, ctypes.c_int]
+        lib.oracle_w8a8_gemm.restype = ctypes.c_int
         self.lib = lib
 
     # -- scalar codecs -----------------------------------------------------
@@ -160,6 +167,52 @@ class Oracle:
             int(threads or os.cpu_count() or 1))
         if rc != 0:
             raise ValueError(f"oracle rejected M={M} N={N} K={K} strides=({a_row_stride},{c_row_stride})")
+        Cv = C.reshape(M, c_row_stride) if C.size == M * c_row_stride else C
+        return (Cv,
+                exact.reshape(M, N) if exact is not None else None,
+                absum.reshape(M, N) if absum is not None else None)
+
+    # -- W8A8: the activation quantiser and the FP8 x FP8 product ------------
+    def quantize_activations(self, A, M, K, a_row_stride=None):
+        """(codes uint8 [M, K], scales float32 [K/128, M]) of BF16 activations A
+        (uint16 codes, ``M * a_row_stride`` elements)."""
+        ld = K if a_row_stride is None else int(a_row_stride)
+        A = np.ascontiguousarray(A, dtype=np.uint16).reshape(-1)
+        assert A.size >= (M - 1) * ld + K
+        codes = np.zeros(M * K, dtype=np.uint8)
+        scales = np.zeros((K // 128) * M, dtype=np.float32)
+        rc = self.lib.oracle_quantize_activations(A.ctypes.data_as(_u16p), ld, M, K,
+                                                  codes.ctypes.data_as(_u8p),
+                                                  scales.ctypes.data_as(_f32p))
+        if rc != 0:
+            raise ValueError(f"oracle_quantize_activations rejected M={M} K={K} ld={ld}")
+        return codes.reshape(M, K), scales.reshape(K // 128, M)
+
+    def w8a8_gemm(self, Aq, a_scale, W, scale, M, N, K, a_row_stride=None, C=None,
+                  c_row_stride=None, threads=None, want_exact=False):
+        """C[m, n] of the W8A8 product (see oracle_w8a8_gemm); same returns as gemm()."""
+        a_row_stride = K if a_row_stride is None else int(a_row_stride)
+        c_row_stride = N if c_row_stride is None else int(c_row_stride)
+        Aq = np.ascontiguousarray(Aq, dtype=np.uint8).reshape(-1)
+        a_scale = np.ascontiguousarray(a_scale, dtype=np.float32).reshape(-1)
+        W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+        scale = np.ascontiguousarray(scale, dtype=np.float32).reshape(-1)
+        assert Aq.size >= (M - 1) * a_row_stride + K and a_scale.size == (K // 128) * M
+        assert W.size == N * K and scale.size == ((N + 127) // 128) * (K // 128)
+        if C is None:
+            C = np.zeros(M * c_row_stride, dtype=np.uint16)
+        C = np.ascontiguousarray(C, dtype=np.uint16).reshape(-1).copy()
+        exact = np.zeros(M * N, dtype=np.float64) if want_exact else None
+        absum = np.zeros(M * N, dtype=np.float64) if want_exact else None
+        rc = self.lib.oracle_w8a8_gemm(
+            Aq.ctypes.data_as(_u8p), a_row_stride, a_scale.ctypes.data_as(_f32p),
+            W.ctypes.data_as(_u8p), scale.ctypes.data_as(_f32p), C.ctypes.data_as(_u16p),
+            c_row_stride, M, N, K,
+            exact.ctypes.data_as(_f64p) if exact is not None else None,
+            absum.ctypes.data_as(_f64p) if absum is not None else None,
+            int(threads or os.cpu_count() or 1))
+        if rc != 0:
+            raise ValueError(f"oracle_w8a8_gemm rejected M={M} N={N} K={K}")
         Cv = C.reshape(M, c_row_stride) if C.size == M * c_row_stride else C
         return (Cv,
                 exact.reshape(M, N) if exact is not None else None,

@@ -135,6 +135,8 @@ typedef struct {
     uint16_t *sout;          /* sampled mode: [count] BF16 results */
     uint64_t begin, end;     /* this thread's share */
     const double *dec;       /* 256-entry E4M3 table */
+    const uint8_t *Aq;       /* W8A8: E4M3 activation codes [M][a_row_stride] (A unused) */
+    const float *a_scale;    /* W8A8: activation group scales [K/128][M] */
 } oracle_job;
 
 /* One output element, exactly as the definition reads. */
@@ -142,7 +144,7 @@ static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_
                        double *abs_out)
 {
     const uint32_t kb_count = j->K / 128;
-    const uint16_t *arow = j->A + (uint64_t)m * j->a_row_stride;
+    const uint16_t *arow = j->A ? j->A + (uint64_t)m * j->a_row_stride : NULL;
     const uint8_t *wrow = j->W + (uint64_t)n * j->K;
     const float *srow = j->scale + (uint64_t)(n / 128) * kb_count;
     double sum = 0.0, asum = 0.0;
@@ -160,7 +162,13 @@ static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_
 #else
         const double w = j->dec[wrow[k]];
 #endif
-        const double a = oracle_bf16_to_double(arow[k]);
+#if ORACLE_MUTANT == 8
+        const uint64_t ai = (uint64_t)m * (j->K / 128) + k / 128; /* mutant: token-major scales */
+#else
+        const uint64_t ai = (uint64_t)(k / 128) * j->M + m;
+#endif
+        const double a = j->Aq ? j->dec[j->Aq[(uint64_t)m * j->a_row_stride + k]] * (double)j->a_scale[ai]
+                               : oracle_bf16_to_double(arow[k]);
 #if ORACLE_MUTANT == 6
         if (k == j->K - 1)
             continue; /* mutant: last term dropped */
@@ -376,4 +384,69 @@ int oracle_quantize_weights(const float *W, uint32_t w_row_stride, uint32_t N, u
         }
     }
     return 0;
+}
+
+/* ---- W8A8: FP8 activations with per-token 128-K group scales -----------------
+ * The adjacent precision variant (page "metrale_model_layers/layers/ops/
+ * fp8_act_quant.rs", module doc: per-token quantisation in 128-element K groups;
+ * the page gives the launch shape, not the arithmetic). Our reading, the same rule
+ * as the weight quantiser on 1x128 groups: per (token m, group g), amax = max |a|,
+ * scale = amax / 448 in FP32, code = E4M3 RNE of a / scale (FP32 quotient),
+ * saturating; amax = 0 gives scale 0 and codes 0; NaN values do not enter amax.
+ * Scales are stored group-major, a_scale[g][m], so one K step's scales of
+ * consecutive tokens are contiguous.
+ *
+ * Quantiser. A: BF16 [M][a_row_stride] (first K of a row), codes: [M][K],
+ * scales: [K/128][M]. Returns 0, or -1 on bad sizes. */
+int oracle_quantize_activations(const uint16_t *A, uint32_t a_row_stride, uint32_t M, uint32_t K,
+                                uint8_t *codes, float *scales)
+{
+    if (M == 0 || K == 0 || K % 128 != 0 || a_row_stride < K)
+        return -1;
+    for (uint32_t m = 0; m < M; ++m)
+        for (uint32_t g = 0; g < K / 128; ++g) {
+            float amax = 0.0f;
+            for (uint32_t k = g * 128; k < g * 128 + 128; ++k) {
+                const float v = fabsf((float)oracle_bf16_to_double(A[(size_t)m * a_row_stride + k]));
+                if (v > amax)
+                    amax = v;
+            }
+            const float scale = amax / 448.0f;
+            scales[(size_t)g * M + m] = scale;
+            for (uint32_t k = g * 128; k < g * 128 + 128; ++k) {
+                uint8_t c = 0;
+                if (scale != 0.0f)
+                    c = oracle_e4m3_encode_rne((float)oracle_bf16_to_double(A[(size_t)m * a_row_stride + k]) /
+                                               scale);
+                codes[(size_t)m * K + k] = c;
+            }
+        }
+    return 0;
+}
+
+/* W8A8 product: C[m][n] = bf16_rne( sum_k (e4m3(Aq[m][k]) * a_scale[k/128][m]) *
+ *                                          (e4m3(W[n][k]) * scale[n/128][k/128]) ),
+ * the sum in FP64 in k order (each term rounds once: 28 x 28 significant bits).
+ * Same layouts as oracle_w8a16_gemm otherwise. */
+int oracle_w8a8_gemm(const uint8_t *Aq, uint32_t a_row_stride, const float *a_scale, const uint8_t *W,
+                     const float *scale, uint16_t *C, uint32_t c_row_stride, uint32_t M, uint32_t N,
+                     uint32_t K, double *exact, double *absum, int nthreads)
+{
+    if (M == 0 || N == 0 || K == 0 || K % 128 != 0 || a_row_stride < K || c_row_stride < N)
+        return -1;
+    oracle_job j;
+    memset(&j, 0, sizeof j);
+    j.Aq = Aq;
+    j.a_scale = a_scale;
+    j.a_row_stride = a_row_stride;
+    j.W = W;
+    j.scale = scale;
+    j.C = C;
+    j.c_row_stride = c_row_stride;
+    j.M = M;
+    j.N = N;
+    j.K = K;
+    j.exact = exact;
+    j.absum = absum;
+    return run_threads(&j, (uint64_t)M * N, nthreads, run_full);
 }

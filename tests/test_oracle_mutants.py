@@ -4,7 +4,8 @@ block, a transposed scale grid, W read as [K][N], a dropped last term) and at
 least one pin of tests/test_oracle_pins.py must fail on it. The mistakes live
 behind ORACLE_MUTANT in oracle/w8a16_oracle.c and are compiled only here, into
 a temporary directory. The seventh plants a wrong range in the weight block
-quantiser (scale = amax / 447)."""
+quantiser (scale = amax / 447); the eighth reads the W8A8 activation scales in the
+wrong layout."""
 import pytest
 
 import oracle
@@ -18,6 +19,7 @@ MUTANTS = {
     5: "W read as [K][N]",
     6: "last term of the sum dropped",
     7: "block scale uses 447 instead of 448",
+    8: "W8A8 activation scales read token-major",
 }
 
 

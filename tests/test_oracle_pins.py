@@ -330,12 +330,77 @@ def pin_quantizer_block_maximum(o):
             assert np.all(np.abs(deq - blk[:, 0].numpy()) <= np.maximum(step, 2.0 ** -9 * scales[nb, kb]))
 
 
+# ---- W8A8 pins (activation quantiser and FP8 x FP8 product) ----------------
+
+def _torch_act_quant(a_bf16: torch.Tensor):
+    """Independent torch statement of the per-token 128-group quantiser."""
+    M, K = a_bf16.shape
+    x = a_bf16.float().reshape(M, K // 128, 128)
+    amax = x.abs().amax(dim=2)
+    s = amax / 448.0
+    safe = torch.where(s > 0, s, torch.ones_like(s))
+    c = (x / safe[:, :, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    c[s == 0] = 0
+    return c.reshape(M, K).numpy(), s.t().contiguous().numpy()
+
+
+def pin_act_quantizer_vs_torch(o):
+    g = torch.Generator().manual_seed(41)
+    M, K, ld = 5, 512, 520
+    a = (torch.randn(M, ld, generator=g) * 3).to(torch.bfloat16)
+    a[2, 128:256] = 0                                           # a zero group
+    codes, scales = o.quantize_activations(_codes(a), M, K, a_row_stride=ld)
+    rc, rs = _torch_act_quant(a[:, :K])
+    assert np.array_equal(codes, rc) and np.array_equal(scales, rs)
+    assert scales[1, 2] == 0 and not codes[2, 128:256].any()
+
+
+def pin_w8a8_reduces_to_w8a16(o):
+    """With unit activation scales the W8A8 product is the W8A16 product of the
+    activations' E4M3 values (exact in BF16), bit for bit."""
+    g = torch.Generator().manual_seed(42)
+    M, N, K = 3, 200, 256
+    aq = torch.randint(0, 256, (M, K), generator=g, dtype=torch.uint8)
+    aq[(aq & 0x7F) == 0x7F] = 0x38                              # no NaN codes
+    w = torch.randn(N, K, generator=g) * 0.05
+    wc, ws = workloads.block_quantize_e4m3(w)
+    ones = np.ones((K // 128, M), dtype=np.float32)
+    c8, _, _ = o.w8a8_gemm(aq.numpy(), ones, wc.numpy(), ws.numpy(), M, N, K)
+    vals = _e4m3_torch(aq.numpy().reshape(-1)).reshape(M, K)
+    a16 = _codes(torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16))
+    c16, _, _ = o.gemm(a16, wc.numpy(), ws.numpy(), M, N, K)
+    assert np.array_equal(c8, c16)
+
+
+def pin_w8a8_brute_force_tiny(o):
+    """Exact rational sums on tiny shapes with random group and block scales."""
+    g = torch.Generator().manual_seed(43)
+    M, N, K = 2, 130, 256
+    aq = torch.randint(0, 0x7E, (M, K), generator=g, dtype=torch.uint8)
+    wq = torch.randint(0, 0x7E, (N, K), generator=g, dtype=torch.uint8)
+    sa = (torch.rand(K // 128, M, generator=g) + 0.5).numpy().astype(np.float32)
+    sw = (torch.rand((N + 127) // 128, K // 128, generator=g) + 0.5).numpy().astype(np.float32)
+    sign = torch.randint(0, 2, (M, K), generator=g, dtype=torch.uint8) << 7
+    aq = aq | sign
+    got, _, _ = o.w8a8_gemm(aq.numpy(), sa, wq.numpy(), sw, M, N, K)
+    av = _e4m3_torch(aq.numpy().reshape(-1)).reshape(M, K)
+    wv = _e4m3_torch(wq.numpy().reshape(-1)).reshape(N, K)
+    for m in range(M):
+        for n in (0, 1, 127, 128, 129):
+            tot = Fraction(0)
+            for k in range(K):
+                tot += (Fraction(float(av[m, k])) * Fraction(float(sa[k // 128, m]))) * \
+                       (Fraction(float(wv[n, k])) * Fraction(float(sw[n // 128, k // 128])))
+            assert got[m, n] == _rne_bf16_exact(tot), (m, n)
+
+
 PINS = [pin_e4m3_fixed_points, pin_e4m3_all_codes_vs_torch, pin_bf16_fixed_points,
         pin_bf16_vs_torch_on_binary32, pin_hand_worked_example, pin_identity_weights,
         pin_all_ones_closed_form, pin_brute_force_tiny, pin_zero_block,
         pin_pads_untouched_and_ignored, pin_linearity, pin_nan_propagation,
         pin_e4m3_encode_round_trip, pin_e4m3_encode_ties_vs_torch, pin_quantizer_vs_recipe,
-        pin_quantizer_block_maximum]
+        pin_quantizer_block_maximum,
+        pin_act_quantizer_vs_torch, pin_w8a8_reduces_to_w8a16, pin_w8a8_brute_force_tiny]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
