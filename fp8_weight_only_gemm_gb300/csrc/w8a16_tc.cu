@@ -41,6 +41,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "w8a16_cluster.cuh"
 #include "w8a16_device.cuh"
 #include "w8a16_internal.h"
 
@@ -86,51 +87,10 @@ struct TcCfg {
     static constexpr uint32_t kIssuer2 = kFold0 + NF;        // warp of the second MMA issuer
 };
 
-// Relaxed arrive: the only state peers touch before the matching wait is the
-// receive mbarrier, whose initialisation fence.mbarrier_init already releases to
-// the cluster. A release arrive would also wait for this CTA's in-flight weight
-// loads, holding the activation producer back by about a microsecond.
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
-__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
 
-// One FP32 register into another CTA's shared memory, counted on that CTA's
-// mbarrier as completed transaction bytes.
-__device__ __forceinline__ void st_async_v4f32(uint32_t remote_addr, uint32_t remote_bar, float a,
-                                               float b, float c, float d) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-            remote_addr),
-        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-        : "memory");
-}
 
-// Bytes pushed per row by all of its fold threads (token groups of kTokPerFold).
-template <uint32_t TN, uint32_t TPF>
-__device__ __forceinline__ uint32_t red_row_bytes(uint32_t toks_valid);
 
-// Bytes one fold thread pushes per row: its token group's valid tokens, rounded up
-// to whole 16-byte groups of 4.
-__device__ __forceinline__ uint32_t push_bytes(uint32_t toks_valid, uint32_t first, uint32_t count) {
-    const uint32_t v = toks_valid > first ? min(toks_valid - first, count) : 0u;
-    return 16u * ((v + 3u) / 4u);
-}
-template <uint32_t TN, uint32_t TPF>
-__device__ __forceinline__ uint32_t red_row_bytes(uint32_t toks_valid) {
-    uint32_t b = 0;
-#pragma unroll
-    for (uint32_t first = 0; first < TN; first += TPF) b += push_bytes(toks_valid, first, TPF);
-    return b;
-}
 
 template <uint32_t NREG>
 __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[NREG]) {
@@ -149,10 +109,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// First row of the weight tile owned by cluster rank r when split_k CTAs share it.
-__device__ __forceinline__ uint32_t owned_row0(uint32_t r, uint32_t split_k) {
-    return r * kTcRows / split_k;
-}
 
 // Wait until the last `depth` copies a producer issued into a ring have landed.
 __device__ __forceinline__ void drain_ring(uint32_t bar_base, uint32_t depth, uint32_t issued,
