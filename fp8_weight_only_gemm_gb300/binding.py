@@ -18,7 +18,7 @@ HEADER = PKG.parent / "include" / "w8a16.h"
 # Values mirrored from include/w8a16.h (checked against the header by the tests).
 W8A16_OK = 0
 FLAG_PDL = 1
-VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8 = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8 = 0, 1, 2, 3, 4
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
 WEIGHTS_F32, WEIGHTS_BF16 = 0, 1
 
@@ -58,6 +58,11 @@ _SIGS = {
     "w8a16_gemm_with_plan": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32,
                                     ctypes.POINTER(Plan), _U32, _VP]),
     "w8a16_quantize_weights": (_INT, [_VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP]),
+    "w8a16_quantize_activations": (_INT, [_VP, _U32, _U32, _U32, _VP, _VP, _U32, _VP]),
+    "w8a16_gemm_w8a8": (_INT, [_VP, _U32, _VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32,
+                               _VP]),
+    "w8a16_gemm_w8a8_with_plan": (_INT, [_VP, _U32, _VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32,
+                                         _U32, ctypes.POINTER(Plan), _U32, _VP]),
     "w8a16_last_error": (ctypes.c_char_p, []),
     "w8a16_strerror": (ctypes.c_char_p, [_INT]),
     "w8a16_device_status": (_INT, [_VP, _INT, ctypes.POINTER(_U32), ctypes.POINTER(_U32),
@@ -246,6 +251,55 @@ def quantize_weights(W, *, stream=None):
                                            scale.data_ptr(), _stream_handle(stream))
     _check(rc)
     return codes, scale
+
+
+def quantize_activations(A, *, stream=None):
+    """(codes uint8 [M, K], scales float32 [K/128, S]) of CUDA bfloat16 activations
+    [M, K] (rows contiguous, any pitch); S = M rounded up to a multiple of 4, the
+    columns past M unused."""
+    import torch
+    if A.dim() != 2 or A.stride(1) != 1 or A.dtype != torch.bfloat16 or not A.is_cuda:
+        raise ValueError("A must be a CUDA bfloat16 [M, K] tensor with contiguous rows")
+    M, K = A.shape
+    S = (M + 3) // 4 * 4
+    codes = torch.empty((M, K), dtype=torch.uint8, device=A.device)
+    scales = torch.zeros((max(K // 128, 1), S), dtype=torch.float32, device=A.device)
+    with torch.cuda.device(A.device):
+        rc = load().w8a16_quantize_activations(A.data_ptr(), A.stride(0), M, K, codes.data_ptr(),
+                                               scales.data_ptr(), S, _stream_handle(stream))
+    _check(rc)
+    return codes, scales
+
+
+def gemm_w8a8(A_codes, a_scale, W, scale, C=None, *, stream=None, plan: Plan | None = None,
+              flags: int = 0):
+    """C[:, :N] (bf16) = (A_codes x a_scale) @ (W x block scales)^T on the GPU.
+    A_codes: uint8 [M, K] (row pitch a multiple of 16 bytes); a_scale: float32
+    [K/128, >=M] (row pitch a multiple of 4); W: uint8 [N, K]; scale: float32
+    [ceil(N/128), K/128]; C: optional bf16 [M, >=N]."""
+    import torch
+    M, K = A_codes.shape
+    N = W.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A_codes.device)
+    args = (A_codes.data_ptr(), A_codes.stride(0), a_scale.data_ptr(), a_scale.stride(0), W.data_ptr(),
+            scale.data_ptr(), C.data_ptr(), C.stride(0), M, N, K)
+    with torch.cuda.device(A_codes.device):
+        s = _stream_handle(stream)
+        if plan is None:
+            rc = load().w8a16_gemm_w8a8(*args, flags, s)
+        else:
+            rc = load().w8a16_gemm_w8a8_with_plan(*args, ctypes.byref(plan), flags, s)
+    _check(rc)
+    return C
+
+
+def gemm_w8a8_ptr(A_ptr, a_row_stride, a_scale_ptr, a_scale_stride, W_ptr, scale_ptr, C_ptr,
+                  c_row_stride, M, N, K, stream=0, flags: int = 0) -> int:
+    """Raw-pointer W8A8 call (returns the library's code; does not raise)."""
+    return load().w8a16_gemm_w8a8(A_ptr or None, a_row_stride, a_scale_ptr or None, a_scale_stride,
+                                  W_ptr or None, scale_ptr or None, C_ptr or None, c_row_stride, M, N,
+                                  K, flags, stream or None)
 
 
 def quantize_weights_ptr(W_ptr, w_dtype, w_row_stride, N, K, codes_ptr, scale_ptr, stream=0) -> int:

@@ -106,23 +106,32 @@ uint32_t token_tile_for(uint32_t M) {
 
 // Tensor-core variants: TC (BF16 datapath) and TC8 (FP8 datapath, token tiles
 // up to 64). Per-variant sizes come from the shared constants.
-bool is_tc_variant(int32_t v) { return v == W8A16_VARIANT_TC || v == W8A16_VARIANT_TC8; }
+bool is_tc_variant(int32_t v) {
+    return v == W8A16_VARIANT_TC || v == W8A16_VARIANT_TC8 || v == W8A16_VARIANT_W8A8;
+}
 uint32_t max_token_tile(int32_t v) { return v == W8A16_VARIANT_TC8 ? 64u : 128u; }
 uint32_t v_threads(int32_t v, uint32_t tn) {
-    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_threads(tn) : w8a16::tc_threads(tn);
+    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_threads(tn)
+           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_threads(tn)
+                                     : w8a16::tc_threads(tn);
 }
 uint32_t v_smem(int32_t v, uint32_t tn, uint32_t st, uint32_t split) {
-    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_smem_bytes(tn, st, split)
-                                  : w8a16::tc_smem_bytes(tn, st, split);
+    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_smem_bytes(tn, st, split)
+           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_smem_bytes(tn, st, split)
+                                     : w8a16::tc_smem_bytes(tn, st, split);
 }
 uint32_t v_tmem(int32_t v, uint32_t tn) {
-    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_tmem_cols(tn) : w8a16::tc_tmem_cols(tn);
+    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_tmem_cols(tn)
+           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_tmem_cols(tn)
+                                     : w8a16::tc_tmem_cols(tn);
 }
 bool v_supported(int32_t v, uint32_t tn, uint32_t st) {
-    return v == W8A16_VARIANT_TC8 ? w8a16::tc8_supported_stages(tn, st)
-                                  : w8a16::tc_supported_stages(tn, st);
+    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_supported_stages(tn, st)
+           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_supported_stages(tn, st)
+                                     : w8a16::tc_supported_stages(tn, st);
 }
 uint32_t default_stages(int32_t v, uint32_t tn) {
+    if (v == W8A16_VARIANT_W8A8) return 4;
     if (v == W8A16_VARIANT_TC8) return tn == 16 ? 4 : tn == 32 ? 6 : 4;   // 16: two CTAs per SM
     return tn == 16 ? 8 : tn == 32 ? 4 : tn == 64 ? 6 : 4;
 }
@@ -325,8 +334,9 @@ int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::s
     }
     Entry e{dev, v, tn, stages, {0}};
     for (uint32_t c = 1; c <= 16; ++c) {
-        int rc = v == W8A16_VARIANT_TC8 ? w8a16::tc8_cluster_capacity(tn, stages, c, &e.cap[c], err)
-                                        : w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
+        int rc = v == W8A16_VARIANT_TC8    ? w8a16::tc8_cluster_capacity(tn, stages, c, &e.cap[c], err)
+                 : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_cluster_capacity(tn, stages, c, &e.cap[c], err)
+                                           : w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
         if (rc) return rc;
     }
     std::lock_guard<std::mutex> lock(mu);
@@ -339,9 +349,9 @@ int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::s
 // the model's (SMs x CTAs per SM), because the cluster occupancy query reports one
 // CTA per SM even where two co-reside (launches of two-per-SM plans do run all
 // their CTAs at once).
-int plan_live(uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& info, w8a16_plan_t* out,
+int plan_live(int32_t v, uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& info, w8a16_plan_t* out,
               std::string* err) {
-    const int32_t v = auto_variant(M);
+    if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
     const uint32_t tn = token_tile_for(v, M);
     const uint32_t stages = default_stages(v, tn);
     uint32_t cap[17];
@@ -366,6 +376,9 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
         return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
                                        "' is not an integer number of milliseconds in 1..600000");
     if (forced) {
+        if (forced->variant == W8A16_VARIANT_W8A8)
+            return fail(W8A16_ERR_PLAN, "w8a16_gemm: a W8A8 plan needs FP8 activations "
+                                        "(w8a16_gemm_w8a8_with_plan)");
         rc = validate_plan(g.M, g.N, g.K, *forced);
         if (rc) return rc;
     }
@@ -377,7 +390,7 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
     if (forced) {
         plan = *forced;
     } else {
-        rc = plan_live(g.M, g.N, g.K, info, &plan, &err);
+        rc = plan_live(W8A16_VARIANT_AUTO, g.M, g.N, g.K, info, &plan, &err);
         if (rc) return fail(rc, err);
     }
     if (plan.variant == W8A16_VARIANT_SIMT)
@@ -386,6 +399,58 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
         rc = w8a16::launch_tc8(g, plan, stream, ts.ns, flags, &err);
     else
         rc = w8a16::launch_tc(g, plan, stream, ts.ns, flags, &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
+// W8A8: the same size rules as w8a16_gemm, plus the activation code pitch (a
+// multiple of 16 bytes: TMA row stride) and the scale pitch (>= M, a multiple of 4).
+int run_w8a8(const w8a16::W8A8Args& g, const w8a16_plan_t* forced, uint32_t flags,
+             cudaStream_t stream) {
+    if (flags & ~static_cast<uint32_t>(W8A16_FLAG_PDL))
+        return fail(W8A16_ERR_ARG, "w8a16_gemm_w8a8: unknown flag bits " + u(flags));
+    if (g.M < 1) return fail(W8A16_ERR_M_ZERO, "w8a16_gemm_w8a8: m=0 has no rows to compute");
+    if (g.K < w8a16::kKStep || g.K % w8a16::kKStep != 0)
+        return fail(W8A16_ERR_K_BLOCK, "w8a16_gemm_w8a8: K=" + u(g.K) + " must be a positive multiple of 128");
+    if (g.lda < g.K || g.ldc < g.N || g.a_scale_stride < g.M)
+        return fail(W8A16_ERR_PITCH, "w8a16_gemm_w8a8: pitches (a=" + u(g.lda) + ", c=" + u(g.ldc) +
+                                         ", a_scale=" + u(g.a_scale_stride) + ") must cover k=" + u(g.K) +
+                                         ", n=" + u(g.N) + ", m=" + u(g.M));
+    if (g.lda % 16 != 0 || g.a_scale_stride % 4 != 0)
+        return fail(W8A16_ERR_A_PITCH_ALIGN, "w8a16_gemm_w8a8: a_row_stride=" + u(g.lda) +
+                                                 " must be a multiple of 16 bytes and a_scale_stride=" +
+                                                 u(g.a_scale_stride) + " a multiple of 4");
+    if (g.N < 1) return fail(W8A16_ERR_N_ZERO, "w8a16_gemm_w8a8: n=0 has no columns to compute");
+    if (g.M > 0x7FFFFFFFu || g.N > 0x7FFFFFFFu || g.K > 0x7FFFFFFFu || ceil_div(g.M, 16) > 65535u * 8u)
+        return fail(W8A16_ERR_RANGE, "w8a16_gemm_w8a8: M, N or K out of range");
+    if (!g.A || !g.a_scale || !g.W || !g.scale || !g.C)
+        return fail(W8A16_ERR_NULL, "w8a16_gemm_w8a8: NULL operand pointer");
+    const auto addr = [](const void* q) { return reinterpret_cast<uintptr_t>(q); };
+    if (addr(g.A) % 16 || addr(g.a_scale) % 16 || addr(g.W) % 16 || addr(g.scale) % 4 || addr(g.C) % 2)
+        return fail(W8A16_ERR_ALIGN, "w8a16_gemm_w8a8: alignment (A, a_scale and W need 16 bytes, "
+                                     "block_scale 4, C 2)");
+    const TimeoutSetting& ts = timeout_setting();
+    if (!ts.valid)
+        return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
+                                       "' is not an integer number of milliseconds in 1..600000");
+    if (forced) {
+        if (forced->variant != W8A16_VARIANT_W8A8)
+            return fail(W8A16_ERR_PLAN, "w8a16_gemm_w8a8: the plan is not a W8A8 plan");
+        const int rc = validate_plan(g.M, g.N, g.K, *forced);
+        if (rc) return rc;
+    }
+    DeviceInfo info;
+    std::string err;
+    int rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    w8a16_plan_t plan;
+    if (forced) {
+        plan = *forced;
+    } else {
+        rc = plan_live(W8A16_VARIANT_W8A8, g.M, g.N, g.K, info, &plan, &err);
+        if (rc) return fail(rc, err);
+    }
+    rc = w8a16::launch_w8a8(g, plan, stream, ts.ns, flags, &err);
     if (rc) return fail(rc, err);
     return ok();
 }
@@ -440,6 +505,54 @@ int w8a16_quantize_weights(const void* W, uint32_t w_dtype, uint32_t w_row_strid
     return ok();
 }
 
+int w8a16_gemm_w8a8(const void* A, uint32_t a_row_stride, const float* a_scale, uint32_t a_scale_stride,
+                    const void* W, const float* block_scale, void* C, uint32_t c_row_stride, uint32_t M,
+                    uint32_t N, uint32_t K, uint32_t flags, w8a16_stream_t stream) {
+    const w8a16::W8A8Args g{A, a_row_stride, a_scale, a_scale_stride, W, block_scale, C, c_row_stride, M, N, K};
+    return run_w8a8(g, nullptr, flags, static_cast<cudaStream_t>(stream));
+}
+
+int w8a16_gemm_w8a8_with_plan(const void* A, uint32_t a_row_stride, const float* a_scale,
+                              uint32_t a_scale_stride, const void* W, const float* block_scale, void* C,
+                              uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
+                              const w8a16_plan_t* plan, uint32_t flags, w8a16_stream_t stream) {
+    if (!plan) return fail(W8A16_ERR_NULL, "w8a16_gemm_w8a8_with_plan: NULL plan");
+    const w8a16::W8A8Args g{A, a_row_stride, a_scale, a_scale_stride, W, block_scale, C, c_row_stride, M, N, K};
+    return run_w8a8(g, plan, flags, static_cast<cudaStream_t>(stream));
+}
+
+int w8a16_quantize_activations(const void* A, uint32_t a_row_stride, uint32_t M, uint32_t K, void* codes,
+                               float* scales, uint32_t scale_stride, w8a16_stream_t stream) {
+    if (M < 1) return fail(W8A16_ERR_M_ZERO, "w8a16_quantize_activations: m=0 has no rows");
+    if (K < w8a16::kKStep || K % w8a16::kKStep != 0)
+        return fail(W8A16_ERR_K_BLOCK, "w8a16_quantize_activations: K=" + u(K) +
+                                           " must be a positive multiple of 128 (one scale per 128-K group)");
+    if (a_row_stride < K || scale_stride < M)
+        return fail(W8A16_ERR_PITCH, "w8a16_quantize_activations: a_row_stride=" + u(a_row_stride) +
+                                         " must cover K=" + u(K) + " and scale_stride=" + u(scale_stride) +
+                                         " must cover M=" + u(M));
+    if (a_row_stride % 8 != 0 || scale_stride % 4 != 0)
+        return fail(W8A16_ERR_A_PITCH_ALIGN, "w8a16_quantize_activations: a_row_stride=" + u(a_row_stride) +
+                                                 " must be a multiple of 8 and scale_stride=" +
+                                                 u(scale_stride) + " a multiple of 4");
+    if (M > 0x7FFFFFFFu || K > 0x7FFFFFFFu)
+        return fail(W8A16_ERR_RANGE, "w8a16_quantize_activations: M or K out of range");
+    if (!A || !codes || !scales)
+        return fail(W8A16_ERR_NULL, std::string("w8a16_quantize_activations: NULL ") +
+                                        (!A ? "A" : !codes ? "codes" : "scales") + " pointer");
+    const auto addr = [](const void* q) { return reinterpret_cast<uintptr_t>(q); };
+    if (addr(A) % 16 || addr(codes) % 16 || addr(scales) % 16)
+        return fail(W8A16_ERR_ALIGN, "w8a16_quantize_activations: A, codes and scales need 16-byte alignment");
+    DeviceInfo info;
+    std::string err;
+    int rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    rc = w8a16::launch_quantize_act(A, a_row_stride, M, K, codes, scales, scale_stride,
+                                    static_cast<cudaStream_t>(stream), &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
 int w8a16_plan_for(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
                    const uint32_t* cluster_ctas, w8a16_plan_t* out) {
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_for: NULL plan pointer");
@@ -457,7 +570,7 @@ int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t* out) {
     std::string err;
     rc = current_device_info(&info, &err);
     if (rc) return fail(rc, err);
-    rc = plan_live(M, N, K, info, out, &err);
+    rc = plan_live(W8A16_VARIANT_AUTO, M, N, K, info, out, &err);
     if (rc) return fail(rc, err);
     return ok();
 }
@@ -590,11 +703,14 @@ const char* w8a16_strerror(int code) {
 
 int w8a16_device_status(w8a16_stream_t stream, int clear, uint32_t* status, uint32_t* where,
                         uint32_t* detail) {
-    w8a16::StatusWord w{0, 0, 0}, w8{0, 0, 0};
+    w8a16::StatusWord w{0, 0, 0}, w8{0, 0, 0}, wa{0, 0, 0};
     cudaError_t e = w8a16::tc_status_read(&w, clear != 0, reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaSuccess)
         e = w8a16::tc8_status_read(&w8, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess)
+        e = w8a16::w8a8_status_read(&wa, clear != 0, reinterpret_cast<cudaStream_t>(stream));
     if (w.code == 0) w = w8;
+    if (w.code == 0) w = wa;
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(W8A16_ERR_DEVICE, std::string("w8a16_device_status: ") + cudaGetErrorString(e));

@@ -21,6 +21,20 @@ struct GemmArgs {
     uint32_t M, N, K;
 };
 
+// W8A8 operands: E4M3 activation codes [M][lda bytes] with FP32 group scales
+// [K/128][a_scale_stride], the weights and C as in GemmArgs.
+struct W8A8Args {
+    const void* A;
+    uint32_t lda;
+    const float* a_scale;
+    uint32_t a_scale_stride;
+    const void* W;
+    const float* scale;
+    void* C;
+    uint32_t ldc;
+    uint32_t M, N, K;
+};
+
 struct StatusWord {
     uint32_t code, where, detail;
 };
@@ -96,6 +110,23 @@ constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) 
                               tc8_tmem_cols(tn));
 }
 
+// W8A8 variant: activation ring of 4 slots (TN x 128 codes + TN FP32 scales),
+// 4 product buffers of TN columns, 4 fold warps (8 from a 64-token tile), two MMA
+// issuers and the two producers in the first four warps.
+constexpr uint32_t w8a8_act_stages(uint32_t) { return 4u; }
+constexpr uint32_t w8a8_fold_warps(uint32_t tn) { return tn <= 32 ? 4u : 8u; }
+constexpr uint32_t w8a8_threads(uint32_t tn) { return 128u + 32u * w8a8_fold_warps(tn); }
+constexpr uint32_t w8a8_tmem_cols(uint32_t tn) { return 4u * tn < 32u ? 32u : 4u * tn; }
+// A tensor TMA writes shared memory at 128-byte aligned addresses only: each
+// slot of TN FP32 group scales is padded to a multiple of 128 bytes.
+constexpr uint32_t w8a8_scale_slot_bytes(uint32_t tn) { return (tn * 4u + 127u) / 128u * 128u; }
+constexpr uint32_t w8a8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
+    return alone_if_full_tmem(1024u + stages * kTcRows * kKStep + w8a8_act_stages(tn) * tn * kKStep +
+                                  w8a8_act_stages(tn) * w8a8_scale_slot_bytes(tn) + tc_red_bytes(tn, split) +
+                                  1024u,
+                              w8a8_tmem_cols(tn));
+}
+
 // Kernel launchers (implemented in the kernel translation units). They assume
 // the arguments and plan were validated; they return a W8A16_* code and, on
 // failure, a message in *err.
@@ -107,8 +138,22 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
 // device when launched in clusters of `cluster` CTAs.
 int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
                         std::string* err);
+// W8A8 operands: E4M3 activation codes [M][row_stride bytes] and FP32 activation
+// scales [K/128][scale_stride] (K-group major).
+bool tensor_map_act_codes(const void* codes, uint32_t M, uint32_t K, uint32_t row_stride,
+                          uint32_t token_tile, int device, CUtensorMap* out, std::string* err);
+bool tensor_map_act_scales(const float* scales, uint32_t M, uint32_t K, uint32_t scale_stride,
+                           uint32_t token_tile, int device, CUtensorMap* out, std::string* err);
 int launch_quantize(const void* W, bool bf16, uint32_t ldw, uint32_t N, uint32_t K, void* codes,
                     float* scales, cudaStream_t s, std::string* err);
+int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+                uint32_t flags, std::string* err);
+bool w8a8_supported_stages(uint32_t tn, uint32_t stages);
+int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+                          std::string* err);
+cudaError_t w8a8_status_read(StatusWord* out, bool clear, cudaStream_t s);
+int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* scales,
+                        uint32_t scale_stride, cudaStream_t s, std::string* err);
 int launch_tc8(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
                uint32_t flags, std::string* err);
 int tc8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,

@@ -1,4 +1,4 @@
-// Weight block quantiser for sm_103a: FP32 or BF16 W -> E4M3 codes + one FP32
+// Block quantisers for sm_103a. Weights: FP32 or BF16 W -> E4M3 codes + one FP32
 // scale per 128x128 block, the format the W8A16 GEMM consumes (page
 // "metrale_model_layers/layers/ops/w8a16_gemm_pipelined_m32.rs", doc comment of
 // `w8a16_gemm_pipelined_m32_strided`: W as FP8 E4M3 [N, K], block_scale FP32
@@ -11,6 +11,10 @@
 // warp instruction reads one 512-byte (FP32) or 256-byte (BF16) row segment and
 // writes 128 code bytes. The block's values stay in registers between the
 // maximum and the encoding, so W is read once: the kernel is bound by HBM.
+//
+// Activations (the W8A8 variant's first half; page "metrale_model_layers/layers/
+// ops/fp8_act_quant.rs", module doc: per-token 128-element K groups): the same
+// rule on 1 x 128 groups, a warp per group.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -85,7 +89,51 @@ __global__ void __launch_bounds__(kQWarps * 32)
     }
 }
 
+// Per-token 128-K groups of BF16 activations: a warp per (token, group), a lane
+// per 4 values. scales are K-group major: scales[g * scale_stride + m].
+__global__ void __launch_bounds__(256)
+    quantize_act_kernel(const uint16_t* __restrict__ A, uint32_t lda, uint32_t M, uint32_t K,
+                        uint8_t* __restrict__ codes, float* __restrict__ scales, uint32_t scale_stride) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t item = static_cast<uint64_t>(blockIdx.x) * 8u + (threadIdx.x >> 5);
+    const uint32_t groups = K / kQCols;
+    if (item >= static_cast<uint64_t>(M) * groups) return;
+    const uint32_t m = static_cast<uint32_t>(item / groups), g = static_cast<uint32_t>(item % groups);
+    const uint32_t col = g * kQCols + 4 * lane;
+    const uint2 q = *reinterpret_cast<const uint2*>(A + static_cast<size_t>(m) * lda + col);
+    const float v[4] = {__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                        __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)};
+    float mx = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (uint32_t o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    const float scale = __fdiv_rn(mx, 448.f);
+    uint32_t word = 0;
+    if (scale != 0.f)
+        word = e4m3x2(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale)) |
+               (e4m3x2(__fdiv_rn(v[2], scale), __fdiv_rn(v[3], scale)) << 16);
+    *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(m) * K + col) = word;
+    if (lane == 0) scales[static_cast<size_t>(g) * scale_stride + m] = scale;
+}
+
 }  // namespace
+
+int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* scales,
+                        uint32_t scale_stride, cudaStream_t s, std::string* err) {
+    const uint64_t items = static_cast<uint64_t>(M) * (K / kQCols);
+    const uint64_t blocks = (items + 7) / 8;
+    if (blocks > 0x7FFFFFFFull) {
+        *err = "activation quantiser: too many groups";
+        return W8A16_ERR_RANGE;
+    }
+    quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const uint16_t*>(A), lda, M, K, static_cast<uint8_t*>(codes), scales, scale_stride);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = std::string("activation quantiser launch failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    return W8A16_OK;
+}
 
 int launch_quantize(const void* W, bool bf16, uint32_t ldw, uint32_t N, uint32_t K, void* codes,
                     float* scales, cudaStream_t s, std::string* err) {

@@ -1,0 +1,490 @@
+// W8A8 tensor-core kernel for sm_103a: E4M3 activations (per-token 128-K group
+// scales) times E4M3 weights (128x128 block scales), tcgen05.mma kind::f8f6f4.
+//
+// The adjacent precision variant of the W8A16 GEMM: the activations come already
+// quantised (page "metrale_model_layers/layers/ops/fp8_act_quant.rs", module
+// doc: per-token quantisation in 128-element K groups), so each 128-K step is one
+// FP8 x FP8 product P = A_q W_q^T folded as acc += s_w * s_a[token] * P, with
+// the same tiles, rings, split-K and reduction order as the two-term kernel
+// (w8a16_tc8.cu) but no activation split: the activation codes are the MMA's
+// B operand as TMA lands them (N = TN, one MMA per 32 K).
+//
+// Warp roles: 0 weight producer (TMA), 1 TMEM owner + MMA issuer for even steps,
+// 2 activation producer (TMA: the step's codes and its TN group scales), 3 MMA
+// issuer for odd steps, then NF fold warps. Two issuers each wait only on their
+// own steps' slots (every ring has an even number of slots), so one thread's
+// waits overlap the other's MMAs.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "w8a16_cluster.cuh"
+#include "w8a16_device.cuh"
+#include "w8a16_internal.h"
+
+namespace w8a16 {
+
+__device__ DeviceStatus g_w8a8_status;
+
+namespace {
+
+constexpr uint32_t kWTileBytes = kTcRows * kKStep;   // 16 KiB of E4M3 weights per stage
+
+enum : uint32_t {
+    kWaitW = 21, kWaitX = 22, kWaitXEmpty = 23, kWaitMdone = 24, kWaitPEmpty = 25, kWaitDone = 26,
+    kWaitDrain = 27, kWaitRed = 28
+};
+
+template <uint32_t TN, uint32_t STAGES>
+struct A8Cfg {
+    static constexpr uint32_t SA = w8a8_act_stages(TN);    // activation ring (codes + scales)
+    static constexpr uint32_t NP = 4;                      // TMEM product buffers (TN columns)
+    static constexpr uint32_t NF = w8a8_fold_warps(TN);
+    static constexpr uint32_t kTmemCols = w8a8_tmem_cols(TN);
+    static constexpr uint32_t kCodeBytes = TN * kKStep;    // one step's E4M3 activation tile
+    static constexpr uint32_t kScaleSlot = w8a8_scale_slot_bytes(TN) / 4u;   // floats per scale slot
+    static constexpr uint32_t kFold0 = 4;                  // first fold warp
+    static constexpr uint32_t kTokPerFold = TN * 4 / NF;
+    static constexpr uint32_t ND = STAGES > SA ? (STAGES > NP ? STAGES : NP) : (SA > NP ? SA : NP);
+    // barriers: wfull[S], xfull[SA], xempty[SA], mdone[ND], pempty[NP], done, red
+    static constexpr uint32_t kNumBars = STAGES + 2 * SA + ND + NP + 2;
+    static_assert(STAGES % 2 == 0 && SA % 2 == 0 && NP % 2 == 0, "rings of even depth");
+    static_assert(NP * TN <= kTmemCols, "TMEM budget");
+    static_assert(kTokPerFold % 16 == 0, "fold loads are whole x16 column groups");
+    static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
+};
+
+__device__ __forceinline__ bool warp_wait_a8(uint32_t bar, uint32_t parity, uint64_t deadline,
+                                             volatile int* abort_flag, uint32_t detail) {
+    const bool ok = mbar_wait(bar, parity, deadline, abort_flag, &g_w8a8_status, detail);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__device__ __forceinline__ void drain_ring_a8(uint32_t bar_base, uint32_t depth, uint32_t issued,
+                                              uint64_t timeout_ns) {
+    const uint64_t dl = globaltimer_ns() + timeout_ns;
+    for (uint32_t j = issued > depth ? issued - depth : 0; j < issued; ++j) {
+        volatile int never = 0;
+        mbar_wait(bar_base + 8u * (j % depth), (j / depth) & 1, dl, &never, &g_w8a8_status, kWaitDrain);
+    }
+}
+
+template <uint32_t TN, uint32_t STAGES>
+__global__ void __launch_bounds__(w8a8_threads(TN), 1)
+    w8a16_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      const __grid_constant__ CUtensorMap tmS, const float* __restrict__ scale,
+                      __nv_bfloat16* __restrict__ C, uint32_t ldc, uint32_t M, uint32_t N, uint32_t K,
+                      uint32_t split_k, uint64_t timeout_ns) {
+    using Cfg = A8Cfg<TN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sW = smem;                                        // STAGES x 16 KiB weights
+    uint8_t* sX = sW + STAGES * kWTileBytes;                   // SA x TN x 128 activation codes
+    float* sS = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kCodeBytes);   // SA slots of TN scales
+    float* sRed = sS + Cfg::SA * Cfg::kScaleSlot;              // split-K receive slots
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sRed) +
+                                                 tc_red_bytes(TN, split_k));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    // mdone[i % ND] completes when step i's MMAs have: it frees weight slot
+    // i % STAGES and fills product buffer i % NP. The fold of step i frees
+    // activation slot i % SA (it reads the scales; the MMAs read the codes first).
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t wfull0 = bar0;
+    const uint32_t xfull0 = wfull0 + 8u * STAGES, xempty0 = xfull0 + 8u * Cfg::SA;
+    const uint32_t mdone0 = xempty0 + 8u * Cfg::SA;
+    const uint32_t pempty0 = mdone0 + 8u * Cfg::ND;
+    const uint32_t done_bar = pempty0 + 8u * Cfg::NP;
+    const uint32_t red_bar = done_bar + 8u;
+
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t tile = blockIdx.x / split_k;
+    const uint32_t rank = blockIdx.x - tile * split_k;
+    const uint32_t token0 = blockIdx.y * TN;
+    const uint32_t ksteps = K / kKStep;                        // < 2^24: products fit 32 bits
+    const uint32_t s_begin = rank * ksteps / split_k;
+    const uint32_t s_end = (rank + 1) * ksteps / split_k;
+    const uint32_t nsteps = s_end - s_begin;
+    const uint64_t deadline = globaltimer_ns() + timeout_ns;
+    const uint32_t my_row0 = owned_row0(rank, split_k);
+    const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
+    const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
+    const uint32_t rows_valid = min(kTcRows, N - tile * kTcRows);
+    const uint32_t toks_valid = min(TN, M - token0);
+
+    if (warp == 0) {
+        for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
+            const uint32_t addr = bar0 + 8u * b;
+            uint32_t count = 1;
+            if (addr >= xempty0 && addr < mdone0) count = Cfg::NF;          // fold warps
+            else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;   // fold warps
+            else if (addr == done_bar) count = 2;                           // MMA issuers
+            mbar_init(addr, count);
+        }
+        if (lane == 0) *abort_flag = 0;
+        fence_barrier_init();
+        __syncwarp();
+    }
+    if (threadIdx.x == 0) {
+        if (split_k > 1)
+            mbar_arrive_expect_tx(red_bar, split_k * my_rows * red_row_bytes<TN, Cfg::kTokPerFold>(toks_valid));
+        // weights before the dependency wait (a programmatic launch's caller
+        // guarantees the previous grid writes neither W nor its scales)
+        const uint64_t pol_w = l2_policy_evict_first();
+        for (uint32_t i = 0; i < npre; ++i) {
+            mbar_arrive_expect_tx(wfull0 + 8u * i, kWTileBytes);
+            tma_load_2d(smem_u32(sW + i * kWTileBytes), &tmW, wfull0 + 8u * i,
+                        static_cast<int32_t>((s_begin + i) * kKStep),
+                        static_cast<int32_t>(tile * kTcRows), pol_w);
+        }
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmS);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (split_k > 1) cluster_arrive();
+    if (threadIdx.x == 0) grid_launch_dependents();
+    const uint32_t tP = *tmem_slot;                            // NP x TN columns: FP32 products
+    const uint32_t quarter = warp & 3;
+    const uint32_t row = quarter * 32 + lane;
+    const uint32_t lane_bits = (quarter * 32) << 16;
+    const bool is_fold = warp >= Cfg::kFold0 && warp < Cfg::kFold0 + Cfg::NF;
+
+    if (warp == 0) {
+        // ------------------------------------------------ weight producer (TMA)
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            uint32_t issued = npre;
+            for (uint32_t i = npre; i < nsteps; ++i) {
+                const uint32_t s = i % STAGES, q = i - STAGES;   // slot s last held step q
+                if (!mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline, abort_flag,
+                               &g_w8a8_status, kWaitMdone))
+                    break;
+                mbar_arrive_expect_tx(wfull0 + 8u * s, kWTileBytes);
+                tma_load_2d(smem_u32(sW + s * kWTileBytes), &tmW, wfull0 + 8u * s,
+                            static_cast<int32_t>((s_begin + i) * kKStep),
+                            static_cast<int32_t>(tile * kTcRows), pol_w);
+                issued = i + 1;
+            }
+            drain_ring_a8(wfull0, STAGES, issued, timeout_ns);
+        }
+    } else if (warp == 2) {
+        // ------------------------- activation producer (TMA): codes and scales
+        if (lane == 0) {
+            const uint64_t pol_a = l2_policy_evict_last();
+            grid_dependency_wait();   // the activations may be the previous grid's output
+            uint32_t issued = 0;
+            for (uint32_t i = 0; i < nsteps; ++i) {
+                const uint32_t j = i % Cfg::SA;
+                if (i >= Cfg::SA && !mbar_wait(xempty0 + 8u * j, ((i / Cfg::SA) - 1) & 1, deadline,
+                                               abort_flag, &g_w8a8_status, kWaitXEmpty))
+                    break;
+                mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kCodeBytes + TN * 4u);
+                tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes), &tmX, xfull0 + 8u * j,
+                            static_cast<int32_t>((s_begin + i) * kKStep), static_cast<int32_t>(token0),
+                            pol_a);
+                tma_load_2d(smem_u32(sS + j * Cfg::kScaleSlot), &tmS, xfull0 + 8u * j, static_cast<int32_t>(token0),
+                            static_cast<int32_t>(s_begin + i), pol_a);
+                issued = i + 1;
+            }
+            drain_ring_a8(xfull0, Cfg::SA, issued, timeout_ns);
+        }
+    } else if (warp == 1 || warp == 3) {
+        // ----------------------------------- MMA issuers: even steps, odd steps
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, TN);
+            const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
+            const uint64_t dx0 = smem_desc_kmajor_sw128(smem_u32(sX));
+            for (uint32_t i = (warp == 1 ? 0u : 1u); i < nsteps; i += 2) {
+                const uint32_t s = i % STAGES, j = i % Cfg::SA, p = i % Cfg::NP;
+                if (!mbar_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, &g_w8a8_status,
+                               kWaitW))
+                    break;
+                if (!mbar_wait(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, &g_w8a8_status,
+                               kWaitX))
+                    break;
+                if (i >= Cfg::NP && !mbar_wait(pempty0 + 8u * p, ((i / Cfg::NP) - 1) & 1, deadline,
+                                               abort_flag, &g_w8a8_status, kWaitPEmpty))
+                    break;
+                tc_fence_after();
+                const uint64_t dw = dw0 + ((s * kWTileBytes) >> 4);
+                const uint64_t dx = dx0 + ((j * Cfg::kCodeBytes) >> 4);
+#pragma unroll
+                for (uint32_t kk = 0; kk < kKStep / 32; ++kk)   // 32 bytes of K per MMA
+                    tc_mma_ss_f8(tP + p * TN, dw + 2 * kk, dx + 2 * kk, idesc, kk > 0);
+                tc_commit(mdone0 + 8u * (i % Cfg::ND));
+            }
+            tc_commit(done_bar);   // this thread's MMAs, before TMEM is released
+            volatile int never = 0;
+            mbar_wait(done_bar, 0, globaltimer_ns() + timeout_ns, &never, &g_w8a8_status, kWaitDone);
+        }
+    } else if (is_fold) {
+        // ------------------------- fold: acc += s_w * s_a[token] * P per token
+        const uint32_t fh = (warp - Cfg::kFold0) >> 2;
+        float acc[Cfg::kTokPerFold];
+#pragma unroll
+        for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) acc[t] = 0.f;
+        const float* srow = scale + static_cast<size_t>(tile) * ksteps + s_begin;
+        // this CTA's weight block scales, 32 per register (lane l: step 32c + l)
+        float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
+        float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
+        for (uint32_t i = 0; i < nsteps; ++i) {
+            if (i != 0 && (i & 31u) == 0) {
+                sc_cur = sc_next;
+                sc_next = i + 32u + lane < nsteps ? __ldg(srow + i + 32u + lane) : 0.f;
+            }
+            const uint32_t p = i % Cfg::NP, j = i % Cfg::SA;
+            if (!warp_wait_a8(mdone0 + 8u * (i % Cfg::ND), (i / Cfg::ND) & 1, deadline, abort_flag,
+                              kWaitMdone))
+                break;
+            // the slot's scales were written by TMA: observe its completion here too
+            // (already complete; the slot is not refilled before this warp frees it)
+            if (!warp_wait_a8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
+            tc_fence_after();
+            const float sw = __shfl_sync(0xFFFFFFFFu, sc_cur, i & 31u);
+            const uint32_t pcol = tP + lane_bits + p * TN + fh * Cfg::kTokPerFold;
+            const float* sa = sS + j * Cfg::kScaleSlot + fh * Cfg::kTokPerFold;
+#pragma unroll
+            for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
+                float v[16];
+                tmem_ld_32x32b_x16(pcol + c, v);
+                tc_wait_ld();
+#pragma unroll
+                for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sw * sa[c + t], v[t], acc[c + t]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(pempty0 + 8u * p);
+                mbar_arrive(xempty0 + 8u * j);
+            }
+        }
+        if (split_k == 1) {
+            if (row < rows_valid) {
+                const uint32_t n = tile * kTcRows + row;
+#pragma unroll
+                for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) {
+                    const uint32_t m = fh * Cfg::kTokPerFold + t;
+                    if (m < toks_valid)
+                        C[static_cast<size_t>(token0 + m) * ldc + n] = __float2bfloat16_rn(acc[t]);
+                }
+            }
+        } else {
+            cluster_wait();
+            // the last rank r with r * 128 / split_k <= row (no division by split_k)
+            const uint32_t owner = ((row + 1) * split_k - 1) / kTcRows;
+            const uint32_t lrow = row - owned_row0(owner, split_k);
+            // receive layout [rank][row][token]: this thread's tokens are contiguous
+            // and go as 16-byte groups; the owner reads them back the same way
+            const uint32_t off =
+                ((rank * tc_red_rows(split_k) + lrow) * tc_red_stride(TN) + fh * Cfg::kTokPerFold) * 4u;
+            const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
+            const uint32_t dbar = dsmem_map(red_bar, owner);
+            const uint32_t ngroups = push_bytes(toks_valid, fh * Cfg::kTokPerFold, Cfg::kTokPerFold) / 16u;
+#pragma unroll
+            for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)   // groups past M are not sent
+                if (g < ngroups)
+                    st_async_v4f32(dst + 16u * g, dbar, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2],
+                                   acc[4 * g + 3]);
+            // This CTA's own rows: the thread holding row `row` (and tokens
+            // fh*kTokPerFold..) adds the ranks' partials in rank order.
+            const bool got = warp_wait_a8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+            if (got && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
+                const uint32_t lr = row - my_row0;
+                const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats
+                const float* src_row = sRed + lr * tc_red_stride(TN);
+                for (uint32_t t = fh * Cfg::kTokPerFold;
+                     t < toks_valid && t < (fh + 1) * Cfg::kTokPerFold; t += 4) {
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (uint32_t src = 0; src < split_k; ++src) {   // rank order
+                        const float4 q = *reinterpret_cast<const float4*>(src_row + src * rank_stride + t);
+                        v.x += q.x;
+                        v.y += q.y;
+                        v.z += q.z;
+                        v.w += q.w;
+                    }
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (uint32_t u = 0; u < 4; ++u)
+                        if (t + u < toks_valid)
+                            C[static_cast<size_t>(token0 + t + u) * ldc + tile * kTcRows + row] =
+                                __float2bfloat16_rn(vv[u]);
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tP, Cfg::kTmemCols);
+    }
+}
+
+using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*,
+                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+struct A8Instance {
+    uint32_t tn, stages;
+    A8KernelFn fn;
+};
+#define W8A16_A8_INST(TN_, ST_) {TN_, ST_, &w8a16_w8a8_kernel<TN_, ST_>}
+const A8Instance kA8Instances[] = {
+    W8A16_A8_INST(16, 4),  W8A16_A8_INST(16, 6),  W8A16_A8_INST(32, 4), W8A16_A8_INST(32, 6),
+    W8A16_A8_INST(64, 4),  W8A16_A8_INST(64, 6),  W8A16_A8_INST(128, 4),
+};
+#undef W8A16_A8_INST
+constexpr int kNumA8 = sizeof(kA8Instances) / sizeof(kA8Instances[0]);
+
+int find_a8(uint32_t tn, uint32_t stages) {
+    for (int i = 0; i < kNumA8; ++i)
+        if (kA8Instances[i].tn == tn && kA8Instances[i].stages == stages) return i;
+    return -1;
+}
+
+cudaError_t ensure_attributes_a8(int inst, int device) {
+    static std::mutex mu;
+    static bool done[64][kNumA8] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (done[device][inst]) return cudaSuccess;
+    const A8Instance& k = kA8Instances[inst];
+    uint32_t most = 0;
+    for (uint32_t sp = 1; sp <= 16; ++sp) {
+        const uint32_t b = w8a8_smem_bytes(k.tn, k.stages, sp);
+        if (b <= kMaxDynSmem && b > most) most = b;
+    }
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(most));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) done[device][inst] = true;
+    return e;
+}
+
+}  // namespace
+
+bool w8a8_supported_stages(uint32_t tn, uint32_t stages) { return find_a8(tn, stages) >= 0; }
+
+int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+                uint32_t flags, std::string* err) {
+    const int inst = find_a8(p.token_tile, p.stages);
+    if (inst < 0) {
+        *err = "no W8A8 kernel instance for token_tile=" + std::to_string(p.token_tile) +
+               " stages=" + std::to_string(p.stages);
+        return W8A16_ERR_PLAN;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = ensure_attributes_a8(inst, dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("W8A8 kernel attribute setup failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    GemmArgs wg{};
+    wg.W = g.W;
+    wg.N = g.N;
+    wg.K = g.K;
+    CUtensorMap mw, mx, ms;
+    if (!tc_tensor_map_w(wg, dev, &mw, err) ||
+        !tensor_map_act_codes(g.A, g.M, g.K, g.lda, p.token_tile, dev, &mx, err) ||
+        !tensor_map_act_scales(g.a_scale, g.M, g.K, g.a_scale_stride, p.token_tile, dev, &ms, err))
+        return W8A16_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
+    cfg.blockDim = dim3(w8a8_threads(p.token_tile), 1, 1);
+    cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, p.split_k);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.split_k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, ms, g.scale,
+                           static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, p.split_k,
+                           timeout_ns);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("W8A8 kernel launch failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    return W8A16_OK;
+}
+
+int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+                          std::string* err) {
+    const int inst = find_a8(tn, stages);
+    if (inst < 0 || cluster < 1 || cluster > 16) {
+        *err = "no W8A8 kernel instance, or cluster size outside 1..16";
+        return W8A16_ERR_PLAN;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = ensure_attributes_a8(inst, dev);
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(cluster * 64, 1, 1);
+    cfg.blockDim = dim3(w8a8_threads(tn), 1, 1);
+    cfg.dynamicSmemBytes = w8a8_smem_bytes(tn, stages, cluster);
+    if (cfg.dynamicSmemBytes > kMaxDynSmem) {
+        *ctas = 0;
+        return W8A16_OK;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kA8Instances[inst].fn), &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("cudaOccupancyMaxActiveClusters failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_DEVICE;
+    }
+    *ctas = static_cast<uint32_t>(n) * cluster;
+    return W8A16_OK;
+}
+
+cudaError_t w8a8_status_read(StatusWord* out, bool clear, cudaStream_t s) {
+    DeviceStatus st;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&st, g_w8a8_status, sizeof st, 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    out->code = st.code;
+    out->where = st.where;
+    out->detail = st.detail;
+    if (clear) {
+        const DeviceStatus zero{0, 0, 0};
+        e = cudaMemcpyToSymbolAsync(g_w8a8_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
+}  // namespace w8a16

@@ -99,7 +99,9 @@ enum {
                                 kind::f8f6f4 MMAs as loaded; each BF16 activation enters
                                 as two E4M3 terms (exact for |a| >= 2^-14 of its token's
                                 128-K block maximum, within 2^-22 of it otherwise); a
-                                non-finite activation makes its token's outputs NaN */
+                                non-finite activation makes its token's outputs NaN */,
+    W8A16_VARIANT_W8A8 = 4   /* the W8A8 kernel (w8a16_gemm_w8a8 only): FP8 activations with
+                                per-token 128-K group scales, one kind::f8f6f4 MMA per 32 K */
 };
 
 /*
@@ -228,6 +230,46 @@ enum {
 W8A16_API int w8a16_quantize_weights(const void *W, uint32_t w_dtype, uint32_t w_row_stride,
                                      uint32_t N, uint32_t K, void *codes, float *block_scale,
                                      w8a16_stream_t stream);
+
+/* Per-token group activation quantiser, the first half of the W8A8 variant: BF16
+ * activations -> E4M3 codes with one FP32 scale per token and 128-K group. The page
+ * ("metrale_model_layers/layers/ops/fp8_act_quant.rs", module doc) gives the
+ * grouping (one 128-element K group per scale) but not the arithmetic; our reading,
+ * the same rule as w8a16_quantize_weights on 1x128 groups: amax = max |a|, scale =
+ * amax / 448 (FP32, round to nearest), code = E4M3 RNE of a / scale, saturating;
+ * amax = 0 gives scale 0 and codes 0; NaN values do not enter amax.
+ *   A      BF16 [M][a_row_stride] (first K of a row read), a_row_stride a multiple of 8.
+ *   codes  E4M3 [M][K], written (row pitch K).
+ *   scales FP32 [K/128][scale_stride], written: K-group major, so one K step's scales
+ *          of consecutive tokens are contiguous; scale_stride >= M, a multiple of 4.
+ * A, codes and scales 16-byte aligned. Checks before any device work. */
+W8A16_API int w8a16_quantize_activations(const void *A, uint32_t a_row_stride, uint32_t M,
+                                         uint32_t K, void *codes, float *scales,
+                                         uint32_t scale_stride, w8a16_stream_t stream);
+
+/* W8A8 GEMM, the adjacent precision variant:
+ *   C[m][n] = bf16( sum_k (e4m3(A[m][k]) * a_scale[k/128][m]) *
+ *                         (e4m3(W[n][k]) * block_scale[n/128][k/128]) )
+ * with A and a_scale as w8a16_quantize_activations writes them (a_row_stride in bytes,
+ * >= K and a multiple of 16; a_scale_stride >= M, a multiple of 4), W, block_scale
+ * and C as in w8a16_gemm. Per 128-K step one FP8 x FP8 product on the tensor cores,
+ * folded in FP32 as acc += block_scale * a_scale * P, split-K partials added in rank
+ * order (deterministic). A, a_scale and W 16-byte aligned. flags: W8A16_FLAG_PDL
+ * (the previous grid must not write W or block_scale). Same error codes and checks
+ * as w8a16_gemm, plus the two pitches above. */
+W8A16_API int w8a16_gemm_w8a8(const void *A, uint32_t a_row_stride, const float *a_scale,
+                              uint32_t a_scale_stride, const void *W, const float *block_scale,
+                              void *C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
+                              uint32_t flags, w8a16_stream_t stream);
+
+/* w8a16_gemm_w8a8 with an explicit plan (variant W8A16_VARIANT_W8A8, from
+ * w8a16_plan_variant); a plan of another variant is refused with W8A16_ERR_PLAN. */
+W8A16_API int w8a16_gemm_w8a8_with_plan(const void *A, uint32_t a_row_stride,
+                                        const float *a_scale, uint32_t a_scale_stride,
+                                        const void *W, const float *block_scale, void *C,
+                                        uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
+                                        const w8a16_plan_t *plan, uint32_t flags,
+                                        w8a16_stream_t stream);
 
 /* Fixed description of a W8A16_ERR_* code. */
 W8A16_API const char *w8a16_strerror(int code);
