@@ -16,6 +16,12 @@ The K steps are replayed from CUDA graphs (one kernel per step).
   roofline = the dominant (only) kernel against the measured HBM copy bandwidth
   cpu_baseline = the CPU oracle on the host cores, on a bounded sample
 
+--path w8a8 times the W8A8 variant instead: a step is the per-token 128-group
+activation quantiser followed by the FP8 x FP8 block-scaled GEMM (two launches);
+`value` still counts the BF16-activation problem's bytes, and the roofline entry
+is the GEMM kernel alone (its own algorithmic bytes: FP8 activation codes and
+group scales instead of BF16 activations), timed from a graph of GEMM launches.
+
 --impl reference times the CPU oracle (the reference arm: there is no runnable
 reference implementation) on the same workload and metric.
 """
@@ -38,6 +44,15 @@ sys.path.insert(0, str(ROOT))
 import workloads  # noqa: E402
 
 METRIC = "W8A16 GEMM achieved HBM GB/s and TFLOP/s at M=1..32; % of GB300 HBM roofline"
+METRIC_W8A8 = ("W8A8 variant (activation quantiser + FP8xFP8 GEMM) achieved HBM GB/s of the W8A16 "
+               "problem; % of GB300 HBM roofline")
+
+
+def w8a8_gemm_bytes(wl) -> int:
+    """Algorithmic bytes of one W8A8 GEMM launch: E4M3 weights, block scales,
+    E4M3 activation codes, FP32 group scales, BF16 output, each once."""
+    kb = wl.K // 128
+    return wl.N * wl.K + 4 * ((wl.N + 127) // 128) * kb + wl.M * wl.K + 4 * wl.M * kb + 2 * wl.M * wl.N
 DEFAULT_WORKLOAD = "decode_gemv_m1_n4096_k4096"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -59,9 +74,14 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=None) -> str:
+    """Hash of the listed kernel sources (names under the package's csrc/; all
+    of them when None)."""
+    csrc = ROOT / "fp8_weight_only_gemm_gb300" / "csrc"
+    paths = sorted(csrc.glob("*")) if files is None else [csrc / f for f in sorted(files)]
     h = hashlib.sha256()
-    for f in sorted((ROOT / "fp8_weight_only_gemm_gb300" / "csrc").glob("*")):
+    for f in paths:
+        h.update(f.name.encode())
         h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
@@ -75,7 +95,7 @@ def recorded_traffic(workload: str):
     try:
         d = json.loads(p.read_text())
         e = d.get(workload)
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        if e and e.get("kernel_source_hash") == kernel_source_hash(e.get("kernel_sources")):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         return None
@@ -152,16 +172,36 @@ def bench_gpu(args, ws, rank, local):
     A0, W0, S0, C0 = (case.A.to(dev), case.W.to(dev), case.scale.to(dev), case.C0.to(dev))
     sets = [(A0.clone(), W0.clone(), S0.clone(), C0.clone()) for _ in range(nsets)]
     del A0, W0, S0, C0
-    plan = w8.plan_current(wl.M, wl.N, wl.K)
+    w8a8 = args.path == "w8a8"
+    qsets = [w8.quantize_activations(A[:, :wl.K]) for (A, _, _, _) in sets] if w8a8 else None
+    plan = (w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_W8A8, 0, 0, props.multi_processor_count).as_dict()
+            if w8a8 else w8.plan_current(wl.M, wl.N, wl.K))
     stream = torch.cuda.Stream(dev)
     lib = w8.load()
     sh = int(stream.cuda_stream)
     flags = w8.FLAG_PDL if args.pdl == "on" else 0
 
+    def gemm8(i, fl):
+        A, W, S, C = sets[i % nsets]
+        q, qs = qsets[i % nsets]
+        rc = lib.w8a16_gemm_w8a8(q.data_ptr(), q.stride(0), qs.data_ptr(), qs.stride(0), W.data_ptr(),
+                                 S.data_ptr(), C.data_ptr(), C.stride(0), wl.M, wl.N, wl.K, fl, sh)
+        if rc != 0:
+            raise RuntimeError(w8.last_error())
+
     def call(i, fl=None):
         A, W, S, C = sets[i % nsets]
+        fl = flags if fl is None else fl
+        if w8a8:
+            q, qs = qsets[i % nsets]
+            rc = lib.w8a16_quantize_activations(A.data_ptr(), A.stride(0), wl.M, wl.K, q.data_ptr(),
+                                                qs.data_ptr(), qs.stride(0), sh)
+            if rc != 0:
+                raise RuntimeError(w8.last_error())
+            gemm8(i, fl)
+            return
         rc = lib.w8a16_gemm_ex(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
-                               C.stride(0), wl.M, wl.N, wl.K, flags if fl is None else fl, sh)
+                               C.stride(0), wl.M, wl.N, wl.K, fl, sh)
         if rc != 0:
             raise RuntimeError(w8.last_error())
 
@@ -182,6 +222,12 @@ def bench_gpu(args, ws, rank, local):
                 for i in range(cnt):
                     call(i)
             graphs[n] = g
+        if w8a8:   # the GEMM kernel alone, for its roofline entry
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(G):
+                    gemm8(i, flags)
+            graphs["gemm"] = g
     torch.cuda.synchronize(dev)
 
     def run_steps(k):
@@ -218,16 +264,61 @@ def bench_gpu(args, ws, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
         dist.barrier()
+    kernel_bytes, kernel_us = wl.roofline_bytes(), ms * 1e3 / args.steps
+    if w8a8:
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graphs["gemm"].replay()
+            s1, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(1, args.steps // G)
+            s1.record(stream)
+            for _ in range(reps):
+                graphs["gemm"].replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        kernel_bytes, kernel_us = w8a8_gemm_bytes(wl), s1.elapsed_time(e1) * 1e3 / (reps * G)
     sec = ms / 1e3
     bytes_step = wl.roofline_bytes()
     gbs = bytes_step * args.steps / sec / 1e9
     tflops = wl.flops() * args.steps / sec / 1e12
     hbm, bf16, bf16_sus, src = peaks()
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload + ("/w8a8" if w8a8 else ""))
+    kernel_gbs = kernel_bytes / kernel_us / 1e3
 
     # end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w8a8:
+        A_h = case.A.pin_memory()
+        W_h = case.W.pin_memory()
+        S_h = case.scale.pin_memory()
+        C_h = case.C0.clone().pin_memory()
+        dA, dW, dS, dC = sets[0]
+        e_steps = max(3, min(args.steps, 200))
+
+        def host_step():
+            dA.copy_(A_h, non_blocking=True)
+            dW.copy_(W_h, non_blocking=True)
+            dS.copy_(S_h, non_blocking=True)
+            call(0, 0)
+            C_h.copy_(dC, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                host_step()
+            torch.cuda.synchronize(dev)
+            s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s2.record(stream)
+            for _ in range(e_steps):
+                host_step()
+            e2.record(stream)
+        torch.cuda.synchronize(dev)
+        e_sec = s2.elapsed_time(e2) / 1e3
+        e2e = {"value": bytes_step * e_steps / e_sec / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": case.A.numel() * 2 + wl.N * wl.K + case.scale.numel() * 4,
+               "d2h_bytes_per_step": case.C0.numel() * 2, "steps": e_steps,
+               "ms_per_step": e_sec * 1e3 / e_steps,
+               "path": "pinned host copies + quantiser + W8A8 GEMM + copy of C, one stream"}
+    elif not args.no_e2e:
         A_h = case.A.pin_memory()
         W_h = case.W.pin_memory()
         S_h = case.scale.pin_memory()
@@ -256,10 +347,11 @@ def bench_gpu(args, ws, rank, local):
         raise RuntimeError(f"device status {st}: a bounded wait ran out during the benchmark")
 
     line = {
-        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "metric": METRIC_W8A8 if w8a8 else METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "M": wl.M, "N": wl.N, "K": wl.K,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8" if w8a8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K,
                    "a_row_stride": wl.lda, "c_row_stride": wl.ldc, "seed": wl.seed,
                    "l2": f"inputs rotate over {nsets} buffer sets ({nsets * set_bytes / 1e6:.0f} MB, "
                          f">= 3x the {l2 / 1e6:.0f} MB L2): weights stream from HBM every step",
@@ -269,12 +361,14 @@ def bench_gpu(args, ws, rank, local):
                               "plain stream order"),
                    "plan": plan, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "tflops": tflops,
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": traffic,
+        "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": kernel_gbs / hbm, "traffic": traffic,
                      "peak_source": f"{src}: hbm copy bandwidth",
-                     "bytes_per_launch": bytes_step,
+                     "kernel": "w8a16_w8a8_kernel" if w8a8 else "the planned W8A16 kernel",
+                     "kernel_us": kernel_us,
+                     "bytes_per_launch": kernel_bytes,
                      "tensor_frac_of_bf16_peak": tflops / bf16},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if w8a8 else 1),
         "clocks": clk.summary(),
         "e2e": e2e,
     }
@@ -282,38 +376,44 @@ def bench_gpu(args, ws, rank, local):
 
 
 # ----------------------------------------------------------- CPU oracle --
-def oracle_rate(wl, seconds: float, threads: int | None = None):
-    """Time the CPU oracle on a bounded sample of the workload: full calls of the
-    workload when one takes under `seconds`, else a row subset."""
+def oracle_step(wl, path: str, threads: int):
+    """One full call of the workload on the CPU oracle (for w8a8: its activation
+    quantiser, then its W8A8 product)."""
     import oracle
     case = workloads.make_case(wl)
     o = oracle.get()
-    threads = threads or os.cpu_count() or 1
     A, W, S, C0 = case.A_np(), case.W_np(), case.scale_np(), case.C0_np()
+    if path == "w8a8":
+        def step():
+            q, qs = o.quantize_activations(A, wl.M, wl.K, a_row_stride=wl.lda)
+            o.w8a8_gemm(q, qs, W, S, wl.M, wl.N, wl.K, C=C0, c_row_stride=wl.ldc, threads=threads)
+    else:
+        def step():
+            o.gemm(A, W, S, wl.M, wl.N, wl.K, a_row_stride=wl.lda, C=C0, c_row_stride=wl.ldc,
+                   threads=threads)
+    return step
+
+
+def oracle_rate(wl, seconds: float, threads: int | None = None, path: str = "w8a16"):
+    """Time the CPU oracle on a bounded sample of the workload: as many full calls
+    as fit in about `seconds` (at least one)."""
+    threads = threads or os.cpu_count() or 1
+    step = oracle_step(wl, path, threads)
     t0 = time.perf_counter()
-    o.gemm(A, W, S, wl.M, wl.N, wl.K, a_row_stride=wl.lda, C=C0, c_row_stride=wl.ldc,
-           threads=threads)
+    step()
     t1 = time.perf_counter() - t0
     reps = max(1, int(seconds / max(t1, 1e-6)))
     t0 = time.perf_counter()
     for _ in range(reps):
-        o.gemm(A, W, S, wl.M, wl.N, wl.K, a_row_stride=wl.lda, C=C0, c_row_stride=wl.ldc,
-               threads=threads)
+        step()
     dt = (time.perf_counter() - t0) / reps
     return wl.roofline_bytes() / dt / 1e9, dt, reps, threads
 
 
 def bench_reference(args):
     wl = workloads.CONFIGS[args.workload]
-    import oracle
-    case = workloads.make_case(wl)
-    o = oracle.get()
     threads = os.cpu_count() or 1
-    A, W, S, C0 = case.A_np(), case.W_np(), case.scale_np(), case.C0_np()
-
-    def step():
-        o.gemm(A, W, S, wl.M, wl.N, wl.K, a_row_stride=wl.lda, C=C0, c_row_stride=wl.ldc,
-               threads=threads)
+    step = oracle_step(wl, args.path, threads)
 
     for _ in range(args.warmup):
         step()
@@ -322,14 +422,15 @@ def bench_reference(args):
         step()
     sec = time.perf_counter() - t0
     v = wl.roofline_bytes() * args.steps / sec / 1e9
-    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
+    return {"impl": "reference", "metric": METRIC_W8A8 if args.path == "w8a8" else METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": args.workload, "M": wl.M, "N": wl.N, "K": wl.K},
+            "config": {"workload": args.workload, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"{args.steps} full calls of {args.workload} on the CPU oracle "
-                                       "(FP64, plain k-order loops)"},
+                                       f"({'quantiser + W8A8 product, ' if args.path == 'w8a8' else ''}"
+                                       "FP64, plain k-order loops)"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "note": "no runnable reference implementation exists (the pages ship host code only); "
                     "the reference arm is the CPU oracle"}
@@ -343,6 +444,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", choices=["w8a16", "w8a8"], default="w8a16",
+                    help="w8a8: activation quantiser + W8A8 GEMM per step")
     ap.add_argument("--pdl", choices=["on", "off"], default="on",
                     help="queue the timed calls with W8A16_FLAG_PDL (weights are read-only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -370,9 +473,11 @@ def main():
     line = bench_gpu(args, ws, rank, local)
     if rank == 0:
         if args.cpu_seconds > 0:
-            v, dt, reps, thr = oracle_rate(workloads.CONFIGS[args.workload], args.cpu_seconds)
+            v, dt, reps, thr = oracle_rate(workloads.CONFIGS[args.workload], args.cpu_seconds,
+                                           path=args.path)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle",
                                     "sample": f"{reps} full calls of {args.workload} "
+                                              f"{'(quantiser + W8A8 product) ' if args.path == 'w8a8' else ''}"
                                               f"({dt * 1e3:.1f} ms each) on the CPU oracle"}
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -276,9 +276,12 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
     return W8A16_OK;
 }
 
-void model_capacity(uint32_t sm_count, uint32_t per_sm, uint32_t* cap) {
+// Co-resident CTAs per cluster size on `sm_count` SMs: whole clusters of CTAs
+// that fit per SM at that split (the split-K receive buffer grows shared memory).
+void model_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t sm_count, uint32_t* cap) {
     cap[0] = 0;
-    for (uint32_t c = 1; c <= 16; ++c) cap[c] = ((sm_count ? sm_count : 152u) * per_sm / c) * c;
+    for (uint32_t c = 1; c <= 16; ++c)
+        cap[c] = ((sm_count ? sm_count : 152u) * tc_ctas_per_sm(v, tn, stages, c) / c) * c;
 }
 
 uint32_t token_tile_for(int32_t v, uint32_t M) {
@@ -299,7 +302,7 @@ int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
     const uint32_t ksteps = K / w8a16::kKStep;
     uint32_t model[17];
     if (!cap) {
-        model_capacity(sm_count, tc_ctas_per_sm(v, tn, stages, 1), model);
+        model_capacity(v, tn, stages, sm_count, model);
         cap = model;
     }
     uint32_t usable[17];
@@ -358,7 +361,7 @@ int plan_live(int32_t v, uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& i
     int rc = live_capacity(v, tn, stages, cap, err);
     if (rc) return rc;
     uint32_t model[17];
-    model_capacity(static_cast<uint32_t>(info.sm_count), tc_ctas_per_sm(v, tn, stages, 1), model);
+    model_capacity(v, tn, stages, static_cast<uint32_t>(info.sm_count), model);
     for (uint32_t c = 1; c <= 16; ++c) cap[c] = cap[c] == 0 ? 0u : model[c];
     return plan_core(v, M, N, K, static_cast<uint32_t>(info.sm_count), cap, out);
 }

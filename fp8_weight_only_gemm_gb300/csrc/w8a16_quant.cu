@@ -14,12 +14,18 @@
 //
 // Activations (the W8A8 variant's first half; page "metrale_model_layers/layers/
 // ops/fp8_act_quant.rs", module doc: per-token 128-element K groups): the same
-// rule on 1 x 128 groups, a warp per group.
+// rule on 1 x 128 groups, a warp per group. It is queued as a programmatic
+// dependent launch: its CTAs may start while the previous kernel of the stream
+// runs and wait for that kernel's completion before touching memory; then they
+// let the next kernel (a W8A8 GEMM queued with W8A16_FLAG_PDL) start its weight
+// prefetch, and that kernel's own dependency wait covers these outputs.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <string>
 
+#include "w8a16_device.cuh"
 #include "w8a16_internal.h"
 
 namespace w8a16 {
@@ -94,6 +100,10 @@ __global__ void __launch_bounds__(kQWarps * 32)
 __global__ void __launch_bounds__(256)
     quantize_act_kernel(const uint16_t* __restrict__ A, uint32_t lda, uint32_t M, uint32_t K,
                         uint8_t* __restrict__ codes, float* __restrict__ scales, uint32_t scale_stride) {
+    grid_dependency_wait();   // A may be the previous kernel's output; codes may be its input
+    // only now may the next kernel start: it then overlaps this grid alone, which
+    // writes neither its weights nor their scales
+    grid_launch_dependents();
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t item = static_cast<uint64_t>(blockIdx.x) * 8u + (threadIdx.x >> 5);
     const uint32_t groups = K / kQCols;
@@ -125,9 +135,19 @@ int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, voi
         *err = "activation quantiser: too many groups";
         return W8A16_ERR_RANGE;
     }
-    quantize_act_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        static_cast<const uint16_t*>(A), lda, M, K, static_cast<uint8_t*>(codes), scales, scale_stride);
-    const cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel, static_cast<const uint16_t*>(A), lda, M, K,
+                                       static_cast<uint8_t*>(codes), scales, scale_stride);
+    if (e != cudaSuccess) cudaGetLastError();
     if (e != cudaSuccess) {
         *err = std::string("activation quantiser launch failed: ") + cudaGetErrorString(e);
         return W8A16_ERR_LAUNCH;

@@ -242,7 +242,10 @@ W8A16_API int w8a16_quantize_weights(const void *W, uint32_t w_dtype, uint32_t w
  *   codes  E4M3 [M][K], written (row pitch K).
  *   scales FP32 [K/128][scale_stride], written: K-group major, so one K step's scales
  *          of consecutive tokens are contiguous; scale_stride >= M, a multiple of 4.
- * A, codes and scales 16-byte aligned. Checks before any device work. */
+ * A, codes and scales 16-byte aligned. Checks before any device work. The kernel is
+ * queued as a programmatic dependent launch that waits for the previous kernel of the
+ * stream before it reads or writes memory (nothing for the caller to do); a following
+ * w8a16_gemm_w8a8 with W8A16_FLAG_PDL then prefetches its weights while it runs. */
 W8A16_API int w8a16_quantize_activations(const void *A, uint32_t a_row_stride, uint32_t M,
                                          uint32_t K, void *codes, float *scales,
                                          uint32_t scale_stride, w8a16_stream_t stream);
