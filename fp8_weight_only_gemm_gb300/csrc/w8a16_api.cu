@@ -11,6 +11,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -289,12 +290,60 @@ uint32_t token_tile_for(int32_t v, uint32_t M) {
     return tn > max_token_tile(v) ? max_token_tile(v) : tn;
 }
 
+// W8A8 plan: split and stage count from a stream model. A launch costs a fixed
+// start-up and drain per wave of co-resident CTAs (a partial wave costs as much as
+// a full one), plus the weight bytes at the bandwidth its in-flight loads can
+// sustain (bytes in flight / latency, capped at HBM bandwidth; a CTA has at most
+// `stages` weight tiles, and no more than its K steps, in flight), plus a little
+// reduction work per split rank. live[i] (NULL: model only) is the device's
+// cluster table for kA8Stages[i]; a zero entry rules that cluster size out.
+constexpr uint32_t kA8Stages[2] = {4, 6};
+
+void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
+                 uint32_t sm_count, const uint32_t* const live[2], uint32_t* split_out,
+                 uint32_t* stages_out) {
+    constexpr double kWaveSeconds = 4.0e-6, kLatency = 2.5e-6, kHbm = 6.8e12, kPerRank = 5.0e-8;
+    const double wbytes = static_cast<double>(row_tiles) * token_tiles * w8a16::kTcRows * w8a16::kKStep * ksteps;
+    double best = 1e300;
+    *split_out = 1;
+    *stages_out = kA8Stages[0];
+    for (uint32_t i = 0; i < 2; ++i) {
+        const uint32_t st = kA8Stages[i];
+        if (!w8a16::w8a8_supported_stages(tn, st)) continue;
+        uint32_t cap[17];
+        model_capacity(W8A16_VARIANT_W8A8, tn, st, sm_count, cap);
+        for (uint32_t sp = 1; sp <= (ksteps < 16u ? ksteps : 16u); ++sp) {
+            if (w8a16::w8a8_smem_bytes(tn, st, sp) > w8a16::kMaxDynSmem || cap[sp] == 0) continue;
+            if (live && live[i] && live[i][sp] == 0) continue;
+            const double ctas = static_cast<double>(row_tiles) * token_tiles * sp;
+            const double waves = std::ceil(ctas / cap[sp]);
+            const uint32_t per_cta = ceil_div(ksteps, sp) < st ? ceil_div(ksteps, sp) : st;
+            const double inflight = (ctas < cap[sp] ? ctas : cap[sp]) * per_cta * w8a16::kTcRows * w8a16::kKStep;
+            const double bw = inflight / kLatency < kHbm ? inflight / kLatency : kHbm;
+            const double t = waves * kWaveSeconds + wbytes / bw + kPerRank * sp;
+            if (t < best * (1.0 - 1e-9)) {
+                best = t;
+                *split_out = sp;
+                *stages_out = st;
+            }
+        }
+    }
+}
+
 // Pure planner: variant by M (or as given), token tile by M, stage count by
 // token tile, split from the wave model over `cap` (NULL: every cluster size
-// fills every SM slot).
+// fills every SM slot). The W8A8 variant has its own model (choose_w8a8).
 int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
               const uint32_t* cap, w8a16_plan_t* out) {
     if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
+    if (v == W8A16_VARIANT_W8A8) {
+        const uint32_t tn = token_tile_for(v, M);
+        uint32_t sp = 1, st = kA8Stages[0];
+        choose_w8a8(tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep, sm_count, nullptr,
+                    &sp, &st);
+        fill_tc(v, M, N, tn, st, sp, out);
+        return W8A16_OK;
+    }
     const uint32_t tn = token_tile_for(v, M);
     const uint32_t stages = default_stages(v, tn);
     const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows);
@@ -356,6 +405,21 @@ int plan_live(int32_t v, uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& i
               std::string* err) {
     if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
     const uint32_t tn = token_tile_for(v, M);
+    if (v == W8A16_VARIANT_W8A8) {
+        uint32_t tables[2][17] = {};
+        const uint32_t* live[2] = {nullptr, nullptr};
+        for (uint32_t i = 0; i < 2; ++i) {
+            if (!w8a16::w8a8_supported_stages(tn, kA8Stages[i])) continue;
+            const int rc = live_capacity(v, tn, kA8Stages[i], tables[i], err);
+            if (rc) return rc;
+            live[i] = tables[i];
+        }
+        uint32_t sp = 1, st = kA8Stages[0];
+        choose_w8a8(tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep,
+                    static_cast<uint32_t>(info.sm_count), live, &sp, &st);
+        fill_tc(v, M, N, tn, st, sp, out);
+        return W8A16_OK;
+    }
     const uint32_t stages = default_stages(v, tn);
     uint32_t cap[17];
     int rc = live_capacity(v, tn, stages, cap, err);
