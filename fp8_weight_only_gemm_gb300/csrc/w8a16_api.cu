@@ -292,18 +292,24 @@ uint32_t token_tile_for(int32_t v, uint32_t M) {
 
 // W8A8 plan: split and stage count from a stream model. A launch costs a fixed
 // start-up and drain per wave of co-resident CTAs (a partial wave costs as much as
-// a full one), plus the weight bytes at the bandwidth its in-flight loads can
-// sustain (bytes in flight / latency, capped at HBM bandwidth; a CTA has at most
-// `stages` weight tiles, and no more than its K steps, in flight), plus a little
-// reduction work per split rank. live[i] (NULL: model only) is the device's
-// cluster table for kA8Stages[i]; a zero entry rules that cluster size out.
+// a full one), plus the longer of two floors: the weight bytes at the bandwidth
+// its in-flight loads can sustain (bytes in flight / latency, capped at HBM
+// bandwidth; a CTA has at most `stages` weight tiles, and no more than its K
+// steps, in flight) and the CTAs' K steps at a per-step cost growing with the
+// token tile (MMAs and fold); plus a little reduction work per split rank. As for
+// the BF16 kernel, wide tiles (64 and 128 tokens) that already cover half the SMs
+// are not split. live[i] (NULL: model only) is the device's cluster table for
+// kA8Stages[i]; a zero entry rules that cluster size out.
 constexpr uint32_t kA8Stages[2] = {4, 6};
 
 void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
                  uint32_t sm_count, const uint32_t* const live[2], uint32_t* split_out,
                  uint32_t* stages_out) {
     constexpr double kWaveSeconds = 4.0e-6, kLatency = 2.5e-6, kHbm = 6.8e12, kPerRank = 5.0e-8;
+    const double step_seconds = 4.5e-7 * tn / 128.0;
     const double wbytes = static_cast<double>(row_tiles) * token_tiles * w8a16::kTcRows * w8a16::kKStep * ksteps;
+    const uint32_t sms = sm_count ? sm_count : 152u;
+    const uint32_t max_split = (tn >= 64 && 2u * row_tiles * token_tiles >= sms) ? 1u : (ksteps < 16u ? ksteps : 16u);
     double best = 1e300;
     *split_out = 1;
     *stages_out = kA8Stages[0];
@@ -312,7 +318,7 @@ void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t
         if (!w8a16::w8a8_supported_stages(tn, st)) continue;
         uint32_t cap[17];
         model_capacity(W8A16_VARIANT_W8A8, tn, st, sm_count, cap);
-        for (uint32_t sp = 1; sp <= (ksteps < 16u ? ksteps : 16u); ++sp) {
+        for (uint32_t sp = 1; sp <= max_split; ++sp) {
             if (w8a16::w8a8_smem_bytes(tn, st, sp) > w8a16::kMaxDynSmem || cap[sp] == 0) continue;
             if (live && live[i] && live[i][sp] == 0) continue;
             const double ctas = static_cast<double>(row_tiles) * token_tiles * sp;
@@ -320,7 +326,8 @@ void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t
             const uint32_t per_cta = ceil_div(ksteps, sp) < st ? ceil_div(ksteps, sp) : st;
             const double inflight = (ctas < cap[sp] ? ctas : cap[sp]) * per_cta * w8a16::kTcRows * w8a16::kKStep;
             const double bw = inflight / kLatency < kHbm ? inflight / kLatency : kHbm;
-            const double t = waves * kWaveSeconds + wbytes / bw + kPerRank * sp;
+            const double compute = waves * ceil_div(ksteps, sp) * step_seconds;
+            const double t = waves * kWaveSeconds + (wbytes / bw > compute ? wbytes / bw : compute) + kPerRank * sp;
             if (t < best * (1.0 - 1e-9)) {
                 best = t;
                 *split_out = sp;

@@ -344,7 +344,7 @@ struct A8Instance {
 #define W8A16_A8_INST(TN_, ST_) {TN_, ST_, &w8a16_w8a8_kernel<TN_, ST_>}
 const A8Instance kA8Instances[] = {
     W8A16_A8_INST(16, 4),  W8A16_A8_INST(16, 6),  W8A16_A8_INST(32, 4), W8A16_A8_INST(32, 6),
-    W8A16_A8_INST(64, 4),  W8A16_A8_INST(64, 6),  W8A16_A8_INST(128, 4), W8A16_A8_INST(128, 6),
+    W8A16_A8_INST(64, 4),  W8A16_A8_INST(64, 6),  W8A16_A8_INST(128, 4),
 };
 #undef W8A16_A8_INST
 constexpr int kNumA8 = sizeof(kA8Instances) / sizeof(kA8Instances[0]);
