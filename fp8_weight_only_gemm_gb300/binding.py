@@ -18,7 +18,7 @@ HEADER = PKG.parent / "include" / "w8a16.h"
 # Values mirrored from include/w8a16.h (checked against the header by the tests).
 W8A16_OK = 0
 FLAG_PDL = 1
-VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8 = 0, 1, 2, 3, 4
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8, VARIANT_PRESPLIT = 0, 1, 2, 3, 4, 5
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
 WEIGHTS_F32, WEIGHTS_BF16 = 0, 1
 
@@ -44,6 +44,7 @@ class W8A16Error(RuntimeError):
 
 
 _VP, _U32, _I32, _INT = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int
+_U64 = ctypes.c_uint64
 _SIGS = {
     "w8a16_gemm": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _VP]),
     "w8a16_gemm_contiguous": (_INT, [_VP, _VP, _VP, _VP, _U32, _U32, _U32, _VP]),
@@ -59,6 +60,9 @@ _SIGS = {
                                     ctypes.POINTER(Plan), _U32, _VP]),
     "w8a16_quantize_weights": (_INT, [_VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP]),
     "w8a16_quantize_activations": (_INT, [_VP, _U32, _U32, _U32, _VP, _VP, _U32, _VP]),
+    "w8a16_workspace_bytes": (_U64, [_U32, _U32]),
+    "w8a16_gemm_ws": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, ctypes.POINTER(Plan), _VP,
+                             _U64, _U32, _VP]),
     "w8a16_gemm_w8a8": (_INT, [_VP, _U32, _VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32,
                                _VP]),
     "w8a16_gemm_w8a8_with_plan": (_INT, [_VP, _U32, _VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32,
@@ -77,7 +81,7 @@ _lib = None
 def header_functions() -> list[str]:
     """Names of the functions include/w8a16.h declares."""
     text = HEADER.read_text()
-    return sorted(set(re.findall(r"W8A16_API\s+(?:int|const char \*)\s*(w8a16_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"W8A16_API\s+(?:int|uint64_t|const char \*)\s*(w8a16_\w+)\s*\(", text)))
 
 
 def load(path: Path | str | None = None):
@@ -200,6 +204,44 @@ def gemm(A, W, scale, C=None, *, stream=None, plan: Plan | None = None, flags: i
             rc = lib.w8a16_gemm_with_plan(*args, ctypes.byref(plan), flags, s)
     _check(rc)
     return C
+
+
+def workspace_bytes(M: int, K: int) -> int:
+    """Workspace bytes of the pre-split path of gemm_ws at (M, K)."""
+    return int(load().w8a16_workspace_bytes(M, K))
+
+
+def gemm_ws(A, W, scale, C=None, *, workspace=None, stream=None, plan: Plan | None = None,
+            flags: int = 0):
+    """gemm() through w8a16_gemm_ws. workspace: a CUDA uint8 tensor of at least
+    workspace_bytes(M, K) bytes, 16-byte aligned; None allocates one with torch for
+    this call (a caller that repeats calls should keep one); False passes none."""
+    import torch
+    M, N, K = _shapes(A, W, scale, C)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N:
+        raise ValueError("C must be bfloat16 [M, >=N]")
+    if not (A.is_cuda and W.is_cuda and scale.is_cuda and C.is_cuda):
+        raise ValueError("all tensors must be on a CUDA device")
+    lib = load()
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_bytes(M, K)), dtype=torch.uint8, device=A.device)
+    ws_ptr, ws_bytes = (None, 0) if workspace is False else (workspace.data_ptr(), workspace.numel())
+    with torch.cuda.device(A.device):
+        rc = lib.w8a16_gemm_ws(A.data_ptr(), A.stride(0), W.data_ptr(), scale.data_ptr(), C.data_ptr(),
+                               C.stride(0), M, N, K, ctypes.byref(plan) if plan is not None else None,
+                               ws_ptr, ws_bytes, flags, _stream_handle(stream))
+    _check(rc)
+    return C
+
+
+def gemm_ws_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, ws_ptr, ws_bytes,
+                stream=0, plan: Plan | None = None, flags: int = 0) -> int:
+    """Raw-pointer w8a16_gemm_ws (returns the library's code; does not raise)."""
+    return load().w8a16_gemm_ws(A_ptr or None, a_row_stride, W_ptr or None, scale_ptr or None, C_ptr or None,
+                                c_row_stride, M, N, K, ctypes.byref(plan) if plan is not None else None,
+                                ws_ptr or None, ws_bytes, flags, stream or None)
 
 
 def gemm_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, stream=0,

@@ -108,31 +108,34 @@ uint32_t token_tile_for(uint32_t M) {
 // Tensor-core variants: TC (BF16 datapath) and TC8 (FP8 datapath, token tiles
 // up to 64). Per-variant sizes come from the shared constants.
 bool is_tc_variant(int32_t v) {
-    return v == W8A16_VARIANT_TC || v == W8A16_VARIANT_TC8 || v == W8A16_VARIANT_W8A8;
+    return v == W8A16_VARIANT_TC || v == W8A16_VARIANT_TC8 || v == W8A16_VARIANT_W8A8 ||
+           v == W8A16_VARIANT_PRESPLIT;
 }
+bool is_fp8_act_variant(int32_t v) { return v == W8A16_VARIANT_W8A8 || v == W8A16_VARIANT_PRESPLIT; }
+uint32_t v_terms(int32_t v) { return v == W8A16_VARIANT_PRESPLIT ? 2u : 1u; }
 uint32_t max_token_tile(int32_t v) { return v == W8A16_VARIANT_TC8 ? 64u : 128u; }
 uint32_t v_threads(int32_t v, uint32_t tn) {
-    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_threads(tn)
-           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_threads(tn)
-                                     : w8a16::tc_threads(tn);
+    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_threads(tn)
+           : is_fp8_act_variant(v) ? w8a16::w8a8_threads(tn, v_terms(v))
+                                   : w8a16::tc_threads(tn);
 }
 uint32_t v_smem(int32_t v, uint32_t tn, uint32_t st, uint32_t split) {
-    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_smem_bytes(tn, st, split)
-           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_smem_bytes(tn, st, split)
-                                     : w8a16::tc_smem_bytes(tn, st, split);
+    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_smem_bytes(tn, st, split)
+           : is_fp8_act_variant(v) ? w8a16::w8a8_smem_bytes(tn, st, split, v_terms(v))
+                                   : w8a16::tc_smem_bytes(tn, st, split);
 }
 uint32_t v_tmem(int32_t v, uint32_t tn) {
-    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_tmem_cols(tn)
-           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_tmem_cols(tn)
-                                     : w8a16::tc_tmem_cols(tn);
+    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_tmem_cols(tn)
+           : is_fp8_act_variant(v) ? w8a16::w8a8_tmem_cols(tn, v_terms(v))
+                                   : w8a16::tc_tmem_cols(tn);
 }
 bool v_supported(int32_t v, uint32_t tn, uint32_t st) {
-    return v == W8A16_VARIANT_TC8    ? w8a16::tc8_supported_stages(tn, st)
-           : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_supported_stages(tn, st)
-                                     : w8a16::tc_supported_stages(tn, st);
+    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_supported_stages(tn, st)
+           : is_fp8_act_variant(v) ? w8a16::w8a8_supported_stages(tn, st, v_terms(v))
+                                   : w8a16::tc_supported_stages(tn, st);
 }
 uint32_t default_stages(int32_t v, uint32_t tn) {
-    if (v == W8A16_VARIANT_W8A8) return 4;
+    if (is_fp8_act_variant(v)) return 4;
     if (v == W8A16_VARIANT_TC8) return tn == 16 ? 4 : tn == 32 ? 6 : 4;   // 16: two CTAs per SM
     return tn == 16 ? 8 : tn == 32 ? 4 : tn == 64 ? 6 : 4;
 }
@@ -150,6 +153,7 @@ uint32_t tc_ctas_per_sm(int32_t v, uint32_t tn, uint32_t stages, uint32_t split)
     const uint32_t by_threads = 2048u / v_threads(v, tn);
     uint32_t c = by_smem < by_tmem ? by_smem : by_tmem;
     c = c < by_threads ? c : by_threads;
+    if (is_fp8_act_variant(v) && c > w8a16::w8a8_max_ctas_by_regs(tn)) c = w8a16::w8a8_max_ctas_by_regs(tn);
     return c < 1u ? 1u : c;
 }
 
@@ -302,11 +306,11 @@ uint32_t token_tile_for(int32_t v, uint32_t M) {
 // kA8Stages[i]; a zero entry rules that cluster size out.
 constexpr uint32_t kA8Stages[2] = {4, 6};
 
-void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
+void choose_w8a8(int32_t v, uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
                  uint32_t sm_count, const uint32_t* const live[2], uint32_t* split_out,
                  uint32_t* stages_out) {
-    constexpr double kWaveSeconds = 4.0e-6, kLatency = 2.5e-6, kHbm = 6.8e12, kPerRank = 5.0e-8;
-    const double step_seconds = 4.5e-7 * tn / 128.0;
+    constexpr double kWaveSeconds = 6.0e-6, kLatency = 2.5e-6, kHbm = 6.8e12, kPerRank = 5.0e-8;
+    const double step_seconds = 4.5e-7 * tn / 128.0 * (v == W8A16_VARIANT_PRESPLIT ? 1.3 : 1.0);
     const double wbytes = static_cast<double>(row_tiles) * token_tiles * w8a16::kTcRows * w8a16::kKStep * ksteps;
     const uint32_t sms = sm_count ? sm_count : 152u;
     const uint32_t max_split = (tn >= 64 && 2u * row_tiles * token_tiles >= sms) ? 1u : (ksteps < 16u ? ksteps : 16u);
@@ -315,11 +319,11 @@ void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t
     *stages_out = kA8Stages[0];
     for (uint32_t i = 0; i < 2; ++i) {
         const uint32_t st = kA8Stages[i];
-        if (!w8a16::w8a8_supported_stages(tn, st)) continue;
+        if (!v_supported(v, tn, st)) continue;
         uint32_t cap[17];
-        model_capacity(W8A16_VARIANT_W8A8, tn, st, sm_count, cap);
+        model_capacity(v, tn, st, sm_count, cap);
         for (uint32_t sp = 1; sp <= max_split; ++sp) {
-            if (w8a16::w8a8_smem_bytes(tn, st, sp) > w8a16::kMaxDynSmem || cap[sp] == 0) continue;
+            if (v_smem(v, tn, st, sp) > w8a16::kMaxDynSmem || cap[sp] == 0) continue;
             if (live && live[i] && live[i][sp] == 0) continue;
             const double ctas = static_cast<double>(row_tiles) * token_tiles * sp;
             const double waves = std::ceil(ctas / cap[sp]);
@@ -343,10 +347,10 @@ void choose_w8a8(uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t
 int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
               const uint32_t* cap, w8a16_plan_t* out) {
     if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
-    if (v == W8A16_VARIANT_W8A8) {
+    if (is_fp8_act_variant(v)) {
         const uint32_t tn = token_tile_for(v, M);
         uint32_t sp = 1, st = kA8Stages[0];
-        choose_w8a8(tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep, sm_count, nullptr,
+        choose_w8a8(v, tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep, sm_count, nullptr,
                     &sp, &st);
         fill_tc(v, M, N, tn, st, sp, out);
         return W8A16_OK;
@@ -394,7 +398,7 @@ int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::s
     Entry e{dev, v, tn, stages, {0}};
     for (uint32_t c = 1; c <= 16; ++c) {
         int rc = v == W8A16_VARIANT_TC8    ? w8a16::tc8_cluster_capacity(tn, stages, c, &e.cap[c], err)
-                 : v == W8A16_VARIANT_W8A8 ? w8a16::w8a8_cluster_capacity(tn, stages, c, &e.cap[c], err)
+                 : is_fp8_act_variant(v)   ? w8a16::w8a8_cluster_capacity(tn, stages, v_terms(v), c, &e.cap[c], err)
                                            : w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
         if (rc) return rc;
     }
@@ -412,17 +416,17 @@ int plan_live(int32_t v, uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& i
               std::string* err) {
     if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
     const uint32_t tn = token_tile_for(v, M);
-    if (v == W8A16_VARIANT_W8A8) {
+    if (is_fp8_act_variant(v)) {
         uint32_t tables[2][17] = {};
         const uint32_t* live[2] = {nullptr, nullptr};
         for (uint32_t i = 0; i < 2; ++i) {
-            if (!w8a16::w8a8_supported_stages(tn, kA8Stages[i])) continue;
+            if (!v_supported(v, tn, kA8Stages[i])) continue;
             const int rc = live_capacity(v, tn, kA8Stages[i], tables[i], err);
             if (rc) return rc;
             live[i] = tables[i];
         }
         uint32_t sp = 1, st = kA8Stages[0];
-        choose_w8a8(tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep,
+        choose_w8a8(v, tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep,
                     static_cast<uint32_t>(info.sm_count), live, &sp, &st);
         fill_tc(v, M, N, tn, st, sp, out);
         return W8A16_OK;
@@ -453,6 +457,8 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
         if (forced->variant == W8A16_VARIANT_W8A8)
             return fail(W8A16_ERR_PLAN, "w8a16_gemm: a W8A8 plan needs FP8 activations "
                                         "(w8a16_gemm_w8a8_with_plan)");
+        if (forced->variant == W8A16_VARIANT_PRESPLIT)
+            return fail(W8A16_ERR_PLAN, "w8a16_gemm: a pre-split plan needs a workspace (w8a16_gemm_ws)");
         rc = validate_plan(g.M, g.N, g.K, *forced);
         if (rc) return rc;
     }
@@ -479,6 +485,64 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
 
 // W8A8: the same size rules as w8a16_gemm, plus the activation code pitch (a
 // multiple of 16 bytes: TMA row stride) and the scale pitch (>= M, a multiple of 4).
+// The W8A16 product through the two-term split: the split pre-pass into the
+// workspace, then the FP8 x FP8 kernel on it. Both are queued as programmatic
+// dependent launches; the kernel's weight prefetch overlaps only the split,
+// which writes neither the weights nor their scales.
+int run_presplit(const w8a16::GemmArgs& g, const w8a16_plan_t& plan, void* ws, uint64_t ts_ns,
+                 cudaStream_t stream) {
+    std::string err;
+    const uint32_t fstride = static_cast<uint32_t>(w8a16::split_ws_scale_stride(g.M));
+    uint8_t* codes = static_cast<uint8_t*>(ws);
+    float* factors = reinterpret_cast<float*>(codes + 2ull * g.M * g.K);
+    int rc = w8a16::launch_split_act(g.A, g.lda, g.M, g.K, codes, factors, fstride, stream, &err);
+    if (rc) return fail(rc, err);
+    const w8a16::W8A8Args a{codes, g.K, factors, fstride, g.W, g.scale, g.C, g.ldc, g.M, g.N, g.K, 2u};
+    rc = w8a16::launch_w8a8(a, plan, stream, ts_ns, W8A16_FLAG_PDL, &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
+int run_ws(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, void* ws, uint64_t ws_bytes,
+           uint32_t flags, cudaStream_t stream) {
+    if (flags & ~static_cast<uint32_t>(W8A16_FLAG_PDL))
+        return fail(W8A16_ERR_ARG, "w8a16_gemm_ws: unknown flag bits " + u(flags));
+    int rc = check_sizes(g.lda, g.ldc, g.M, g.N, g.K);
+    if (rc) return rc;
+    rc = check_ptrs(g.A, g.W, g.scale, g.C);
+    if (rc) return rc;
+    if (ws && reinterpret_cast<uintptr_t>(ws) % 16 != 0)
+        return fail(W8A16_ERR_ALIGN, "w8a16_gemm_ws: the workspace must be 16-byte aligned");
+    const uint64_t need = w8a16::split_ws_bytes(g.M, g.K);
+    const bool have_ws = ws != nullptr && ws_bytes >= need;
+    if (forced && forced->variant == W8A16_VARIANT_PRESPLIT && !have_ws)
+        return fail(W8A16_ERR_ARG, "w8a16_gemm_ws: a pre-split plan needs a workspace of " +
+                                       std::to_string(need) + " bytes (have " + std::to_string(ws ? ws_bytes : 0) +
+                                       ")");
+    if (forced && forced->variant != W8A16_VARIANT_PRESPLIT) return run(g, forced, flags, stream);
+    if (!forced && (g.M <= 16 || !have_ws)) return run(g, nullptr, flags, stream);
+    const TimeoutSetting& ts = timeout_setting();
+    if (!ts.valid)
+        return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
+                                       "' is not an integer number of milliseconds in 1..600000");
+    if (forced) {
+        rc = validate_plan(g.M, g.N, g.K, *forced);
+        if (rc) return rc;
+    }
+    DeviceInfo info;
+    std::string err;
+    rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    w8a16_plan_t plan;
+    if (forced) {
+        plan = *forced;
+    } else {
+        rc = plan_live(W8A16_VARIANT_PRESPLIT, g.M, g.N, g.K, info, &plan, &err);
+        if (rc) return fail(rc, err);
+    }
+    return run_presplit(g, plan, ws, ts.ns, stream);
+}
+
 int run_w8a8(const w8a16::W8A8Args& g, const w8a16_plan_t* forced, uint32_t flags,
              cudaStream_t stream) {
     if (flags & ~static_cast<uint32_t>(W8A16_FLAG_PDL))
@@ -582,7 +646,7 @@ int w8a16_quantize_weights(const void* W, uint32_t w_dtype, uint32_t w_row_strid
 int w8a16_gemm_w8a8(const void* A, uint32_t a_row_stride, const float* a_scale, uint32_t a_scale_stride,
                     const void* W, const float* block_scale, void* C, uint32_t c_row_stride, uint32_t M,
                     uint32_t N, uint32_t K, uint32_t flags, w8a16_stream_t stream) {
-    const w8a16::W8A8Args g{A, a_row_stride, a_scale, a_scale_stride, W, block_scale, C, c_row_stride, M, N, K};
+    const w8a16::W8A8Args g{A, a_row_stride, a_scale, a_scale_stride, W, block_scale, C, c_row_stride, M, N, K, 1u};
     return run_w8a8(g, nullptr, flags, static_cast<cudaStream_t>(stream));
 }
 
@@ -591,8 +655,20 @@ int w8a16_gemm_w8a8_with_plan(const void* A, uint32_t a_row_stride, const float*
                               uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
                               const w8a16_plan_t* plan, uint32_t flags, w8a16_stream_t stream) {
     if (!plan) return fail(W8A16_ERR_NULL, "w8a16_gemm_w8a8_with_plan: NULL plan");
-    const w8a16::W8A8Args g{A, a_row_stride, a_scale, a_scale_stride, W, block_scale, C, c_row_stride, M, N, K};
+    const w8a16::W8A8Args g{A, a_row_stride, a_scale, a_scale_stride, W, block_scale, C, c_row_stride, M, N, K, 1u};
     return run_w8a8(g, plan, flags, static_cast<cudaStream_t>(stream));
+}
+
+uint64_t w8a16_workspace_bytes(uint32_t M, uint32_t K) {
+    if (M == 0 || K == 0 || K % w8a16::kKStep != 0) return 0;
+    return w8a16::split_ws_bytes(M, K);
+}
+
+int w8a16_gemm_ws(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale, void* C,
+                  uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t* plan,
+                  void* workspace, uint64_t workspace_bytes, uint32_t flags, w8a16_stream_t stream) {
+    const w8a16::GemmArgs g{A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K};
+    return run_ws(g, plan, workspace, workspace_bytes, flags, static_cast<cudaStream_t>(stream));
 }
 
 int w8a16_quantize_activations(const void* A, uint32_t a_row_stride, uint32_t M, uint32_t K, void* codes,

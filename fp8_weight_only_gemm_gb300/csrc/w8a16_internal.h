@@ -21,8 +21,11 @@ struct GemmArgs {
     uint32_t M, N, K;
 };
 
-// W8A8 operands: E4M3 activation codes [M][lda bytes] with FP32 group scales
-// [K/128][a_scale_stride], the weights and C as in GemmArgs.
+// Operands of the FP8 x FP8 kernel: E4M3 activation codes with FP32 factors per
+// token and 128-K group [K/128][a_scale_stride], the weights and C as in GemmArgs.
+// terms = 1 (W8A8): codes [M][lda bytes], factors the group scales. terms = 2 (the
+// W8A16 two-term split): codes [2M][lda bytes], hi terms in rows [0, M), lo terms
+// (x32) in rows [M, 2M); factors 2^(E-7).
 struct W8A8Args {
     const void* A;
     uint32_t lda;
@@ -33,6 +36,7 @@ struct W8A8Args {
     void* C;
     uint32_t ldc;
     uint32_t M, N, K;
+    uint32_t terms;
 };
 
 struct StatusWord {
@@ -110,21 +114,41 @@ constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) 
                               tc8_tmem_cols(tn));
 }
 
-// W8A8 variant: activation ring of 4 slots (TN x 128 codes + TN FP32 scales),
-// 4 product buffers of TN columns, 4 fold warps (8 from a 64-token tile), two MMA
-// issuers and the two producers in the first four warps.
-constexpr uint32_t w8a8_act_stages(uint32_t) { return 4u; }
-constexpr uint32_t w8a8_fold_warps(uint32_t tn) { return tn <= 32 ? 4u : 8u; }
-constexpr uint32_t w8a8_threads(uint32_t tn) { return 128u + 32u * w8a8_fold_warps(tn); }
-constexpr uint32_t w8a8_tmem_cols(uint32_t tn) { return 4u * tn < 32u ? 32u : 4u * tn; }
+// FP8 x FP8 kernel (W8A8, terms = 1; W8A16 from a two-term split, terms = 2): an
+// activation ring of SA slots (terms x TN x 128 codes + TN FP32 factors), NP
+// product buffers of terms x TN columns, 4 fold warps (8 from a 64-token tile),
+// two MMA issuers and the two producers in the first four warps. A slot is freed
+// by the fold of its step, so the ring keeps 4 slots (2 let every other step wait
+// out a whole load); the 128-token two-term tile has room in TMEM for 2 product
+// buffers of 256 columns.
+constexpr uint32_t w8a8_act_stages(uint32_t, uint32_t = 1) { return 4u; }
+constexpr uint32_t w8a8_p_bufs(uint32_t tn, uint32_t terms = 1) { return terms == 2 && tn >= 128 ? 2u : 4u; }
+// (16 for the 128-token two-term tile, whose fold reads two 128-column halves)
+constexpr uint32_t w8a8_fold_warps(uint32_t tn, uint32_t terms = 1) {
+    return tn <= 32 ? 4u : (terms == 2 && tn >= 128 ? 16u : 8u);
+}
+constexpr uint32_t w8a8_threads(uint32_t tn, uint32_t terms = 1) { return 128u + 32u * w8a8_fold_warps(tn, terms); }
+constexpr uint32_t pow2_at_least(uint32_t x, uint32_t p = 32u) { return p >= x ? p : pow2_at_least(x, 2u * p); }
+constexpr uint32_t w8a8_tmem_cols(uint32_t tn, uint32_t terms = 1) {
+    return pow2_at_least(w8a8_p_bufs(tn, terms) * terms * tn);
+}
+// Registers: the 64- and 128-token instances (384 or 640 threads) run one CTA per
+// SM; the smaller ones are built for two.
+constexpr uint32_t w8a8_max_ctas_by_regs(uint32_t tn) { return tn >= 64 ? 1u : 2u; }
 // A tensor TMA writes shared memory at 128-byte aligned addresses only: each
 // slot of TN FP32 group scales is padded to a multiple of 128 bytes.
 constexpr uint32_t w8a8_scale_slot_bytes(uint32_t tn) { return (tn * 4u + 127u) / 128u * 128u; }
-constexpr uint32_t w8a8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) {
-    return alone_if_full_tmem(1024u + stages * kTcRows * kKStep + w8a8_act_stages(tn) * tn * kKStep +
-                                  w8a8_act_stages(tn) * w8a8_scale_slot_bytes(tn) + tc_red_bytes(tn, split) +
-                                  1024u,
-                              w8a8_tmem_cols(tn));
+constexpr uint32_t w8a8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split, uint32_t terms = 1) {
+    return alone_if_full_tmem(1024u + stages * kTcRows * kKStep +
+                                  w8a8_act_stages(tn, terms) * (terms * tn * kKStep + w8a8_scale_slot_bytes(tn)) +
+                                  tc_red_bytes(tn, split) + 1024u,
+                              w8a8_tmem_cols(tn, terms));
+}
+// Workspace of the two-term split: codes [2M][K] (hi rows, then lo rows) and
+// factors [K/128][round_up(M, 4)] FP32.
+constexpr uint64_t split_ws_scale_stride(uint32_t M) { return (static_cast<uint64_t>(M) + 3u) / 4u * 4u; }
+constexpr uint64_t split_ws_bytes(uint32_t M, uint32_t K) {
+    return 2ull * M * K + 4ull * (K / kKStep) * split_ws_scale_stride(M);
 }
 
 // Kernel launchers (implemented in the kernel translation units). They assume
@@ -148,9 +172,12 @@ int launch_quantize(const void* W, bool bf16, uint32_t ldw, uint32_t N, uint32_t
                     float* scales, cudaStream_t s, std::string* err);
 int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
                 uint32_t flags, std::string* err);
-bool w8a8_supported_stages(uint32_t tn, uint32_t stages);
-int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+bool w8a8_supported_stages(uint32_t tn, uint32_t stages, uint32_t terms = 1);
+int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t terms, uint32_t cluster, uint32_t* ctas,
                           std::string* err);
+// The two-term split of BF16 activations into the workspace layout above.
+int launch_split_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* factors,
+                     uint32_t factor_stride, cudaStream_t s, std::string* err);
 cudaError_t w8a8_status_read(StatusWord* out, bool clear, cudaStream_t s);
 int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* scales,
                         uint32_t scale_stride, cudaStream_t s, std::string* err);

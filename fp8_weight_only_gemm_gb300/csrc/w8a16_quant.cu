@@ -19,6 +19,11 @@
 // runs and wait for that kernel's completion before touching memory; then they
 // let the next kernel (a W8A8 GEMM queued with W8A16_FLAG_PDL) start its weight
 // prefetch, and that kernel's own dependency wait covers these outputs.
+//
+// Two-term split (the W8A16 path through the FP8 x FP8 kernel): the same launch
+// shape, each group written as hi and lo E4M3 codes with its factor 2^(E-7)
+// (w8a16_split.cuh), into the workspace layout codes [2M][K], factors
+// [K/128][stride].
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -27,6 +32,7 @@
 
 #include "w8a16_device.cuh"
 #include "w8a16_internal.h"
+#include "w8a16_split.cuh"
 
 namespace w8a16 {
 namespace {
@@ -125,7 +131,74 @@ __global__ void __launch_bounds__(256)
     if (lane == 0) scales[static_cast<size_t>(g) * scale_stride + m] = scale;
 }
 
+// A warp per (token, group), lane l holding K 4l..4l+3: the block maximum over
+// the finite values (a non-finite value makes the lane's hi codes NaN, so the
+// token's outputs are NaN), then the split of the four values.
+__global__ void __launch_bounds__(256)
+    split_act_kernel(const uint16_t* __restrict__ A, uint32_t lda, uint32_t M, uint32_t K,
+                     uint8_t* __restrict__ codes, float* __restrict__ factors, uint32_t factor_stride) {
+    grid_dependency_wait();   // A may be the previous kernel's output; the workspace its input
+    grid_launch_dependents();
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t item = static_cast<uint64_t>(blockIdx.x) * 8u + (threadIdx.x >> 5);
+    const uint32_t groups = K / kQCols;
+    if (item >= static_cast<uint64_t>(M) * groups) return;
+    const uint32_t m = static_cast<uint32_t>(item / groups), g = static_cast<uint32_t>(item % groups);
+    const uint32_t col = g * kQCols + 4 * lane;
+    const uint2 q = *reinterpret_cast<const uint2*>(A + static_cast<size_t>(m) * lda + col);
+    float x[4] = {__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                  __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)};
+    float mx = 0.f;
+    bool bad = false;
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) {
+        const float a = fabsf(x[e]);
+        if (a <= 3.4028235e38f) mx = fmaxf(mx, a);
+        else bad = true;   // NaN or infinity
+    }
+    mx = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mx)));   // |x| orders as its bits
+    const int E = block_exponent(mx);
+    float p1, p2;
+    split_scales(E, p1, p2);
+#pragma unroll
+    for (uint32_t e = 0; e < 4; ++e) x[e] = (x[e] * p1) * p2;
+    uint32_t hw, lw;
+    two_terms4(x, hw, lw);
+    if (bad) hw = 0x7F7F7F7Fu;
+    *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(m) * K + col) = hw;
+    *reinterpret_cast<uint32_t*>(codes + (static_cast<size_t>(M) + m) * K + col) = lw;
+    if (lane == 0) factors[static_cast<size_t>(g) * factor_stride + m] = fold_factor(E, mx);
+}
+
 }  // namespace
+
+int launch_split_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* factors,
+                     uint32_t factor_stride, cudaStream_t s, std::string* err) {
+    const uint64_t items = static_cast<uint64_t>(M) * (K / kQCols);
+    const uint64_t blocks = (items + 7) / 8;
+    if (blocks > 0x7FFFFFFFull) {
+        *err = "activation split: too many groups";
+        return W8A16_ERR_RANGE;
+    }
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, split_act_kernel, static_cast<const uint16_t*>(A), lda, M, K,
+                                       static_cast<uint8_t*>(codes), factors, factor_stride);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *err = std::string("activation split launch failed: ") + cudaGetErrorString(e);
+        return W8A16_ERR_LAUNCH;
+    }
+    return W8A16_OK;
+}
 
 int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* scales,
                         uint32_t scale_stride, cudaStream_t s, std::string* err) {
@@ -147,8 +220,8 @@ int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, voi
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel, static_cast<const uint16_t*>(A), lda, M, K,
                                        static_cast<uint8_t*>(codes), scales, scale_stride);
-    if (e != cudaSuccess) cudaGetLastError();
     if (e != cudaSuccess) {
+        cudaGetLastError();
         *err = std::string("activation quantiser launch failed: ") + cudaGetErrorString(e);
         return W8A16_ERR_LAUNCH;
     }

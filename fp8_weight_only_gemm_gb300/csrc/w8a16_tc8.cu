@@ -29,6 +29,7 @@
 #include "w8a16_cluster.cuh"
 #include "w8a16_device.cuh"
 #include "w8a16_internal.h"
+#include "w8a16_split.cuh"
 
 namespace w8a16 {
 
@@ -91,21 +92,6 @@ __device__ __forceinline__ void drain_ring8(uint32_t bar_base, uint32_t depth, u
 
 
 
-// Two FP32 values to E4M3 (round to nearest even, saturating): lo in byte 0.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-// Two E4M3 codes (byte 0 and 1) back to FP32.
-__device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float& hi) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(codes)));
-    const __half2 v = *reinterpret_cast<const __half2*>(&h2);
-    lo = __low2float(v);
-    hi = __high2float(v);
-}
-
 // The four K=32 MMAs of one 128-K step: D[128 x 2TN] (FP32, TMEM) = W tile x terms.
 template <uint32_t TN>
 __device__ __forceinline__ void step_mmas(uint32_t d_tmem, uint64_t dw, uint64_t db) {
@@ -113,37 +99,6 @@ __device__ __forceinline__ void step_mmas(uint32_t d_tmem, uint64_t dw, uint64_t
 #pragma unroll
     for (uint32_t kk = 0; kk < kKStep / 32; ++kk)   // 32 bytes of K per MMA
         tc_mma_ss_f8(d_tmem, dw + 2 * kk, db + 2 * kk, idesc, kk > 0);
-}
-
-// E = floor(log2(mx)) of a block maximum from its bits (mx may be an FP32 subnormal).
-__device__ __forceinline__ int block_exponent(float mx) {
-    const uint32_t mb = __float_as_uint(mx);
-    const int ef = static_cast<int>(mb >> 23);
-    return ef != 0 ? ef - 127 : (mb != 0 ? -118 - __clz(mb) : 0);
-}
-// 2^(7-E) as two exact FP32 powers of two (7 - E spans -120..156).
-__device__ __forceinline__ void split_scales(int E, float& p1, float& p2) {
-    const int e1 = (7 - E) / 2, e2 = (7 - E) - e1;
-    p1 = __int_as_float((127 + e1) << 23);
-    p2 = __int_as_float((127 + e2) << 23);
-}
-// 2^(E-7) as FP32 (subnormal or zero for very small blocks); 0 for an all-zero block.
-__device__ __forceinline__ float fold_factor(int E, float mx) {
-    const int ie = E - 7;
-    if (!(mx > 0.f)) return 0.f;
-    return ie >= -126 ? __int_as_float((127 + ie) << 23)
-                      : (ie >= -149 ? __int_as_float(1 << (ie + 149)) : 0.f);
-}
-// hi/lo E4M3 codes of four consecutive scaled values (byte i = value i).
-__device__ __forceinline__ void two_terms4(const float* x, uint32_t& hw, uint32_t& lw) {
-    const uint32_t h0 = f32x2_to_e4m3x2(x[0], x[1]), h1 = f32x2_to_e4m3x2(x[2], x[3]);
-    float hf[4];   // the hi terms' values (exact)
-    e4m3x2_to_f32x2(h0, hf[0], hf[1]);
-    e4m3x2_to_f32x2(h1, hf[2], hf[3]);
-    const uint32_t l0 = f32x2_to_e4m3x2((x[0] - hf[0]) * 32.f, (x[1] - hf[1]) * 32.f);
-    const uint32_t l1 = f32x2_to_e4m3x2((x[2] - hf[2]) * 32.f, (x[3] - hf[3]) * 32.f);
-    hw = h0 | (h1 << 16);
-    lw = l0 | (l1 << 16);
 }
 
 // Split one token's 128-K block with the whole warp, 4 values per lane (used for

@@ -9,6 +9,13 @@
 // (w8a16_tc8.cu) but no activation split: the activation codes are the MMA's
 // B operand as TMA lands them (N = TN, one MMA per 32 K).
 //
+// The same kernel computes the W8A16 product from the two-term split of the BF16
+// activations (TERMS = 2; the split is the one w8a16_split.cuh describes, written
+// to a workspace by a pre-pass): the hi and lo codes of a token tile are the MMA's
+// B rows [0, TN) and [TN, 2 TN), one MMA of N = 2 TN computes both products, and
+// the fold takes acc += s_w * 2^(E-7) * (P_hi + P_lo / 32), as the kernel that
+// splits its own tiles does (w8a16_tc8.cu).
+//
 // Warp roles: 0 weight producer (TMA), 1 TMEM owner + MMA issuer for even steps,
 // 2 activation producer (TMA: the step's codes and its TN group scales), 3 MMA
 // issuer for odd steps, then NF fold warps. Two issuers each wait only on their
@@ -39,13 +46,14 @@ enum : uint32_t {
     kWaitDrain = 27, kWaitRed = 28
 };
 
-template <uint32_t TN, uint32_t STAGES>
+template <uint32_t TN, uint32_t STAGES, uint32_t TERMS>
 struct A8Cfg {
-    static constexpr uint32_t SA = w8a8_act_stages(TN);    // activation ring (codes + scales)
-    static constexpr uint32_t NP = 4;                      // TMEM product buffers (TN columns)
-    static constexpr uint32_t NF = w8a8_fold_warps(TN);
-    static constexpr uint32_t kTmemCols = w8a8_tmem_cols(TN);
-    static constexpr uint32_t kCodeBytes = TN * kKStep;    // one step's E4M3 activation tile
+    static constexpr uint32_t SA = w8a8_act_stages(TN, TERMS);   // activation ring (codes + factors)
+    static constexpr uint32_t NP = w8a8_p_bufs(TN, TERMS);       // TMEM product buffers
+    static constexpr uint32_t NB = TERMS * TN;                   // MMA N: B rows per step
+    static constexpr uint32_t NF = w8a8_fold_warps(TN, TERMS);
+    static constexpr uint32_t kTmemCols = w8a8_tmem_cols(TN, TERMS);
+    static constexpr uint32_t kCodeBytes = NB * kKStep;    // one step's E4M3 activation tile(s)
     static constexpr uint32_t kScaleSlot = w8a8_scale_slot_bytes(TN) / 4u;   // floats per scale slot
     static constexpr uint32_t kFold0 = 4;                  // first fold warp
     static constexpr uint32_t kTokPerFold = TN * 4 / NF;
@@ -53,7 +61,8 @@ struct A8Cfg {
     // barriers: wfull[S], xfull[SA], xempty[SA], mdone[ND], pempty[NP], done, red
     static constexpr uint32_t kNumBars = STAGES + 2 * SA + ND + NP + 2;
     static_assert(STAGES % 2 == 0 && SA % 2 == 0 && NP % 2 == 0, "rings of even depth");
-    static_assert(NP * TN <= kTmemCols, "TMEM budget");
+    static_assert(NP * NB <= kTmemCols, "TMEM budget");
+    static_assert(TERMS == 1 || TERMS == 2, "one or two activation terms");
     static_assert(kTokPerFold % 16 == 0, "fold loads are whole x16 column groups");
     static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
 };
@@ -73,18 +82,18 @@ __device__ __forceinline__ void drain_ring_a8(uint32_t bar_base, uint32_t depth,
     }
 }
 
-template <uint32_t TN, uint32_t STAGES>
-__global__ void __launch_bounds__(w8a8_threads(TN), 1)
+template <uint32_t TN, uint32_t STAGES, uint32_t TERMS>
+__global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs(TN))
     w8a16_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmS, const float* __restrict__ scale,
                       __nv_bfloat16* __restrict__ C, uint32_t ldc, uint32_t M, uint32_t N, uint32_t K,
                       uint32_t split_k, uint64_t timeout_ns) {
-    using Cfg = A8Cfg<TN, STAGES>;
+    using Cfg = A8Cfg<TN, STAGES, TERMS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sW = smem;                                        // STAGES x 16 KiB weights
-    uint8_t* sX = sW + STAGES * kWTileBytes;                   // SA x TN x 128 activation codes
+    uint8_t* sX = sW + STAGES * kWTileBytes;                   // SA x NB x 128 activation codes
     float* sS = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kCodeBytes);   // SA slots of TN scales
     float* sRed = sS + Cfg::SA * Cfg::kScaleSlot;              // split-K receive slots
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sRed) +
@@ -194,6 +203,10 @@ __global__ void __launch_bounds__(w8a8_threads(TN), 1)
                 tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes), &tmX, xfull0 + 8u * j,
                             static_cast<int32_t>((s_begin + i) * kKStep), static_cast<int32_t>(token0),
                             pol_a);
+                if (TERMS == 2)   // lo terms: rows M + token0.. of the [2M][K] codes
+                    tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes + TN * kKStep), &tmX, xfull0 + 8u * j,
+                                static_cast<int32_t>((s_begin + i) * kKStep),
+                                static_cast<int32_t>(M + token0), pol_a);
                 tma_load_2d(smem_u32(sS + j * Cfg::kScaleSlot), &tmS, xfull0 + 8u * j, static_cast<int32_t>(token0),
                             static_cast<int32_t>(s_begin + i), pol_a);
                 issued = i + 1;
@@ -203,7 +216,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN), 1)
     } else if (warp == 1 || warp == 3) {
         // ----------------------------------- MMA issuers: even steps, odd steps
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, TN);
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, Cfg::NB);
             const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
             const uint64_t dx0 = smem_desc_kmajor_sw128(smem_u32(sX));
             for (uint32_t i = (warp == 1 ? 0u : 1u); i < nsteps; i += 2) {
@@ -222,7 +235,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN), 1)
                 const uint64_t dx = dx0 + ((j * Cfg::kCodeBytes) >> 4);
 #pragma unroll
                 for (uint32_t kk = 0; kk < kKStep / 32; ++kk)   // 32 bytes of K per MMA
-                    tc_mma_ss_f8(tP + p * TN, dw + 2 * kk, dx + 2 * kk, idesc, kk > 0);
+                    tc_mma_ss_f8(tP + p * Cfg::NB, dw + 2 * kk, dx + 2 * kk, idesc, kk > 0);
                 tc_commit(mdone0 + 8u * (i % Cfg::ND));
             }
             tc_commit(done_bar);   // this thread's MMAs, before TMEM is released
@@ -253,15 +266,24 @@ __global__ void __launch_bounds__(w8a8_threads(TN), 1)
             if (!warp_wait_a8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
             tc_fence_after();
             const float sw = __shfl_sync(0xFFFFFFFFu, sc_cur, i & 31u);
-            const uint32_t pcol = tP + lane_bits + p * TN + fh * Cfg::kTokPerFold;
+            const uint32_t pcol = tP + lane_bits + p * Cfg::NB + fh * Cfg::kTokPerFold;
             const float* sa = sS + j * Cfg::kScaleSlot + fh * Cfg::kTokPerFold;
 #pragma unroll
             for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
                 float v[16];
                 tmem_ld_32x32b_x16(pcol + c, v);
-                tc_wait_ld();
+                if (TERMS == 2) {
+                    float vl[16];
+                    tmem_ld_32x32b_x16(pcol + TN + c, vl);
+                    tc_wait_ld();
 #pragma unroll
-                for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sw * sa[c + t], v[t], acc[c + t]);
+                    for (uint32_t t = 0; t < 16; ++t)
+                        acc[c + t] = fmaf(sw, fmaf(vl[t], 0.03125f, v[t]) * sa[c + t], acc[c + t]);
+                } else {
+                    tc_wait_ld();
+#pragma unroll
+                    for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sw * sa[c + t], v[t], acc[c + t]);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -338,20 +360,23 @@ __global__ void __launch_bounds__(w8a8_threads(TN), 1)
 using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*,
                             uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 struct A8Instance {
-    uint32_t tn, stages;
+    uint32_t tn, stages, terms;
     A8KernelFn fn;
 };
-#define W8A16_A8_INST(TN_, ST_) {TN_, ST_, &w8a16_w8a8_kernel<TN_, ST_>}
+#define W8A16_A8_INST(TN_, ST_, T_) {TN_, ST_, T_, &w8a16_w8a8_kernel<TN_, ST_, T_>}
 const A8Instance kA8Instances[] = {
-    W8A16_A8_INST(16, 4),  W8A16_A8_INST(16, 6),  W8A16_A8_INST(32, 4), W8A16_A8_INST(32, 6),
-    W8A16_A8_INST(64, 4),  W8A16_A8_INST(64, 6),  W8A16_A8_INST(128, 4),
+    W8A16_A8_INST(16, 4, 1), W8A16_A8_INST(16, 6, 1), W8A16_A8_INST(32, 4, 1), W8A16_A8_INST(32, 6, 1),
+    W8A16_A8_INST(64, 4, 1), W8A16_A8_INST(64, 6, 1), W8A16_A8_INST(128, 4, 1),
+    W8A16_A8_INST(16, 4, 2), W8A16_A8_INST(32, 4, 2), W8A16_A8_INST(32, 6, 2), W8A16_A8_INST(64, 4, 2),
+    W8A16_A8_INST(64, 6, 2), W8A16_A8_INST(128, 4, 2),
 };
 #undef W8A16_A8_INST
 constexpr int kNumA8 = sizeof(kA8Instances) / sizeof(kA8Instances[0]);
 
-int find_a8(uint32_t tn, uint32_t stages) {
+int find_a8(uint32_t tn, uint32_t stages, uint32_t terms) {
     for (int i = 0; i < kNumA8; ++i)
-        if (kA8Instances[i].tn == tn && kA8Instances[i].stages == stages) return i;
+        if (kA8Instances[i].tn == tn && kA8Instances[i].stages == stages && kA8Instances[i].terms == terms)
+            return i;
     return -1;
 }
 
@@ -364,7 +389,7 @@ cudaError_t ensure_attributes_a8(int inst, int device) {
     const A8Instance& k = kA8Instances[inst];
     uint32_t most = 0;
     for (uint32_t sp = 1; sp <= 16; ++sp) {
-        const uint32_t b = w8a8_smem_bytes(k.tn, k.stages, sp);
+        const uint32_t b = w8a8_smem_bytes(k.tn, k.stages, sp, k.terms);
         if (b <= kMaxDynSmem && b > most) most = b;
     }
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
@@ -379,14 +404,16 @@ cudaError_t ensure_attributes_a8(int inst, int device) {
 
 }  // namespace
 
-bool w8a8_supported_stages(uint32_t tn, uint32_t stages) { return find_a8(tn, stages) >= 0; }
+bool w8a8_supported_stages(uint32_t tn, uint32_t stages, uint32_t terms) {
+    return find_a8(tn, stages, terms) >= 0;
+}
 
 int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
                 uint32_t flags, std::string* err) {
-    const int inst = find_a8(p.token_tile, p.stages);
+    const int inst = find_a8(p.token_tile, p.stages, g.terms);
     if (inst < 0) {
-        *err = "no W8A8 kernel instance for token_tile=" + std::to_string(p.token_tile) +
-               " stages=" + std::to_string(p.stages);
+        *err = "no FP8 x FP8 kernel instance for token_tile=" + std::to_string(p.token_tile) +
+               " stages=" + std::to_string(p.stages) + " terms=" + std::to_string(g.terms);
         return W8A16_ERR_PLAN;
     }
     int dev = 0;
@@ -403,14 +430,14 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
     wg.K = g.K;
     CUtensorMap mw, mx, ms;
     if (!tc_tensor_map_w(wg, dev, &mw, err) ||
-        !tensor_map_act_codes(g.A, g.M, g.K, g.lda, p.token_tile, dev, &mx, err) ||
+        !tensor_map_act_codes(g.A, g.M * g.terms, g.K, g.lda, p.token_tile, dev, &mx, err) ||
         !tensor_map_act_scales(g.a_scale, g.M, g.K, g.a_scale_stride, p.token_tile, dev, &ms, err))
         return W8A16_ERR_LAUNCH;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
-    cfg.blockDim = dim3(w8a8_threads(p.token_tile), 1, 1);
-    cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, p.split_k);
+    cfg.blockDim = dim3(w8a8_threads(p.token_tile, g.terms), 1, 1);
+    cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, p.split_k, g.terms);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -432,9 +459,9 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
     return W8A16_OK;
 }
 
-int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
+int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t terms, uint32_t cluster, uint32_t* ctas,
                           std::string* err) {
-    const int inst = find_a8(tn, stages);
+    const int inst = find_a8(tn, stages, terms);
     if (inst < 0 || cluster < 1 || cluster > 16) {
         *err = "no W8A8 kernel instance, or cluster size outside 1..16";
         return W8A16_ERR_PLAN;
@@ -445,8 +472,8 @@ int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(cluster * 64, 1, 1);
-    cfg.blockDim = dim3(w8a8_threads(tn), 1, 1);
-    cfg.dynamicSmemBytes = w8a8_smem_bytes(tn, stages, cluster);
+    cfg.blockDim = dim3(w8a8_threads(tn, terms), 1, 1);
+    cfg.dynamicSmemBytes = w8a8_smem_bytes(tn, stages, cluster, terms);
     if (cfg.dynamicSmemBytes > kMaxDynSmem) {
         *ctas = 0;
         return W8A16_OK;

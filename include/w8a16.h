@@ -100,8 +100,13 @@ enum {
                                 as two E4M3 terms (exact for |a| >= 2^-14 of its token's
                                 128-K block maximum, within 2^-22 of it otherwise); a
                                 non-finite activation makes its token's outputs NaN */,
-    W8A16_VARIANT_W8A8 = 4   /* the W8A8 kernel (w8a16_gemm_w8a8 only): FP8 activations with
+    W8A16_VARIANT_W8A8 = 4,  /* the W8A8 kernel (w8a16_gemm_w8a8 only): FP8 activations with
                                 per-token 128-K group scales, one kind::f8f6f4 MMA per 32 K */
+    W8A16_VARIANT_PRESPLIT = 5 /* w8a16_gemm_ws only: the activations are split into the
+                                two E4M3 terms of W8A16_VARIANT_TC8 once per call, by a
+                                pre-pass into the caller's workspace, and the W8A8 kernel
+                                multiplies both terms in one MMA of N = 2 x token tile;
+                                same accuracy as W8A16_VARIANT_TC8 */
 };
 
 /*
@@ -199,6 +204,34 @@ W8A16_API int w8a16_gemm_with_plan(const void *A, uint32_t a_row_stride, const v
                                    const float *block_scale, void *C, uint32_t c_row_stride,
                                    uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t *plan,
                                    uint32_t flags, w8a16_stream_t stream);
+
+/* ---- the W8A16 product with a caller-provided workspace ------------------ */
+
+/* Bytes of workspace w8a16_gemm_ws uses for the pre-split path at (M, K): the two
+ * E4M3 terms of A ([2M][K] bytes) and one FP32 factor per token and 128-K group
+ * ([K/128][M rounded up to 4]). 0 for M = 0 or K not a positive multiple of 128. */
+W8A16_API uint64_t w8a16_workspace_bytes(uint32_t M, uint32_t K);
+
+/* w8a16_gemm with a workspace: the same operation, arguments, checks and result
+ * contract (within the tolerance of W8A16_VARIANT_TC8, whose split this path
+ * shares). With plan == NULL the library chooses: M <= 16, or no workspace of
+ * w8a16_workspace_bytes(M, K) bytes, runs exactly what w8a16_gemm runs; otherwise
+ * the pre-split path (W8A16_VARIANT_PRESPLIT): a split kernel writes the workspace,
+ * then the FP8 x FP8 kernel reads it (two launches on `stream`, queued as
+ * programmatic dependent launches of each other; W8A16_FLAG_PDL governs only the
+ * first one's overlap with the previous kernel, as for w8a16_gemm). A plan from
+ * w8a16_plan_variant forces a variant (PRESPLIT needs the workspace, else
+ * W8A16_ERR_ARG).
+ *   workspace  device memory, 16-byte aligned, owned by the caller, or NULL; it is
+ *              written by the call and must not be used by other work until the
+ *              call's kernels have finished (calls that share one workspace must
+ *              be ordered on one stream).
+ * Returns W8A16_OK once the work is queued, or a W8A16_ERR_* code (nothing queued). */
+W8A16_API int w8a16_gemm_ws(const void *A, uint32_t a_row_stride, const void *W,
+                            const float *block_scale, void *C, uint32_t c_row_stride,
+                            uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t *plan,
+                            void *workspace, uint64_t workspace_bytes, uint32_t flags,
+                            w8a16_stream_t stream);
 
 /* ---- errors and status -------------------------------------------------- */
 

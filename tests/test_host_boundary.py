@@ -200,3 +200,31 @@ def test_quantizer_constants_match_header():
     text = binding.HEADER.read_text()
     assert int(re.search(r"W8A16_WEIGHTS_F32\s*=\s*(\d+)", text).group(1)) == binding.WEIGHTS_F32
     assert int(re.search(r"W8A16_WEIGHTS_BF16\s*=\s*(\d+)", text).group(1)) == binding.WEIGHTS_BF16
+
+
+def test_workspace_bytes(lib):
+    assert binding.workspace_bytes(32, 5120) == 2 * 32 * 5120 + 4 * 40 * 32
+    assert binding.workspace_bytes(5, 256) == 2 * 5 * 256 + 4 * 2 * 8
+    assert binding.workspace_bytes(0, 256) == 0 and binding.workspace_bytes(4, 200) == 0
+
+
+def test_workspace_entry_checks(lib):
+    args = (0x1000, 256, 0x2000, 0x3000, 0x4000, 256, 32, 256, 256)
+    p = binding.plan_variant(32, 256, 256, binding.VARIANT_PRESPLIT, 1, 4)
+    assert binding.gemm_ws_ptr(*args, 0, 0, plan=p) == -13
+    assert "workspace" in binding.last_error()
+    assert binding.gemm_ws_ptr(*args, 0x5008, 1 << 20) == ERR["ALIGN"]
+    # the page's checks come first, as for w8a16_gemm
+    assert binding.gemm_ws_ptr(0x1000, 256, 0x2000, 0x3000, 0x4000, 256, 0, 256, 256, 0x5000, 1 << 20) \
+        == ERR["M_ZERO"]
+    assert binding.gemm_ws_ptr(0x1000, 260, 0x2000, 0x3000, 0x4000, 256, 32, 256, 256, 0x5000, 1 << 20) \
+        == ERR["A_PITCH_ALIGN"]
+    assert binding.gemm_ws_ptr(*args, 0x5000, 1 << 20, flags=4) == -13
+
+
+def test_presplit_plans(lib):
+    for M, tn in ((1, 16), (17, 32), (33, 64), (100, 128)):
+        p = binding.plan_variant(M, 4096, 4096, binding.VARIANT_PRESPLIT)
+        assert p.variant == binding.VARIANT_PRESPLIT and p.token_tile == tn
+        assert p.smem_bytes <= 232448 and p.tmem_cols in (128, 256, 512)
+        assert p.grid[0] == 32 * p.split_k and p.block[0] in (256, 384, 640)
