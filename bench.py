@@ -3,7 +3,9 @@
 
 One JSON line on stdout (rank 0). A step is one full W8A16 GEMM call on the
 workload (default: decode GEMV M=1, N=K=4096, the configuration the headline
-metric is quoted on). Timing: W untimed warm-up steps, then exactly K steps,
+metric is quoted on), through w8a16_gemm_ws with a workspace: up to 16 tokens
+that is one launch of the kernel that splits its own activation tiles; above,
+the split pre-pass and the FP8 x FP8 kernel (two launches). Timing: W untimed warm-up steps, then exactly K steps,
 bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on
 the launching stream. Steps rotate over B distinct input/output buffer sets
 totalling at least 3x the L2 size, so every step streams its weights from HBM.
@@ -174,8 +176,14 @@ def bench_gpu(args, ws, rank, local):
     del A0, W0, S0, C0
     w8a8 = args.path == "w8a8"
     qsets = [w8.quantize_activations(A[:, :wl.K]) for (A, _, _, _) in sets] if w8a8 else None
-    plan = (w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_W8A8, 0, 0, props.multi_processor_count).as_dict()
-            if w8a8 else w8.plan_current(wl.M, wl.N, wl.K))
+    presplit = not w8a8 and wl.M > 16
+    wss = [torch.empty(max(16, w8.workspace_bytes(wl.M, wl.K)), dtype=torch.uint8, device=dev)
+           for _ in range(nsets)] if not w8a8 else None
+    sms = props.multi_processor_count
+    plan = (w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_W8A8, 0, 0, sms).as_dict() if w8a8 else
+            w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_PRESPLIT, 0, 0, sms).as_dict() if presplit else
+            w8.plan_current(wl.M, wl.N, wl.K))
+    launches_per_step = 2 if (w8a8 or presplit) else 1
     stream = torch.cuda.Stream(dev)
     lib = w8.load()
     sh = int(stream.cuda_stream)
@@ -200,8 +208,9 @@ def bench_gpu(args, ws, rank, local):
                 raise RuntimeError(w8.last_error())
             gemm8(i, fl)
             return
-        rc = lib.w8a16_gemm_ex(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
-                               C.stride(0), wl.M, wl.N, wl.K, fl, sh)
+        ws = wss[i % nsets]
+        rc = lib.w8a16_gemm_ws(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
+                               C.stride(0), wl.M, wl.N, wl.K, None, ws.data_ptr(), ws.numel(), fl, sh)
         if rc != 0:
             raise RuntimeError(w8.last_error())
 
@@ -282,7 +291,7 @@ def bench_gpu(args, ws, rank, local):
     gbs = bytes_step * args.steps / sec / 1e9
     tflops = wl.flops() * args.steps / sec / 1e12
     hbm, bf16, bf16_sus, src = peaks()
-    traffic = recorded_traffic(args.workload + ("/w8a8" if w8a8 else ""))
+    traffic = recorded_traffic(args.workload + ("/w8a8" if w8a8 else "/presplit" if presplit else ""))
     kernel_gbs = kernel_bytes / kernel_us / 1e3
 
     # end to end through the host-buffer entry point
@@ -364,11 +373,13 @@ def bench_gpu(args, ws, rank, local):
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": kernel_gbs / hbm, "traffic": traffic,
                      "peak_source": f"{src}: hbm copy bandwidth",
-                     "kernel": "w8a16_w8a8_kernel" if w8a8 else "the planned W8A16 kernel",
+                     "kernel": ("w8a16_w8a8_kernel (terms 1), timed alone" if w8a8 else
+                                "split pre-pass + w8a16_w8a8_kernel (terms 2): the whole step" if presplit
+                                else "w8a16_tc8_kernel, one launch per step"),
                      "kernel_us": kernel_us,
                      "bytes_per_launch": kernel_bytes,
                      "tensor_frac_of_bf16_peak": tflops / bf16},
-        "gpu_launches": args.steps * (2 if w8a8 else 1),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
