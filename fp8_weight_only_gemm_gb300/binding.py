@@ -28,13 +28,15 @@ class Plan(ctypes.Structure):
                 ("split_k", ctypes.c_uint32), ("stages", ctypes.c_uint32),
                 ("ctas_per_sm", ctypes.c_uint32), ("grid", ctypes.c_uint32 * 3),
                 ("block", ctypes.c_uint32 * 3), ("cluster", ctypes.c_uint32 * 3),
-                ("smem_bytes", ctypes.c_uint32), ("tmem_cols", ctypes.c_uint32)]
+                ("smem_bytes", ctypes.c_uint32), ("tmem_cols", ctypes.c_uint32),
+                ("tail_tiles", ctypes.c_uint32), ("tail_split", ctypes.c_uint32)]
 
     def as_dict(self) -> dict:
         return {"variant": self.variant, "token_tile": self.token_tile, "split_k": self.split_k,
                 "stages": self.stages, "ctas_per_sm": self.ctas_per_sm, "grid": list(self.grid),
                 "block": list(self.block), "cluster": list(self.cluster),
-                "smem_bytes": self.smem_bytes, "tmem_cols": self.tmem_cols}
+                "smem_bytes": self.smem_bytes, "tmem_cols": self.tmem_cols,
+                "tail_tiles": self.tail_tiles, "tail_split": self.tail_split}
 
 
 class W8A16Error(RuntimeError):

@@ -271,6 +271,20 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
                                         " must be in 1..min(16, K/128=" + u(ksteps) + ")");
     w8a16_plan_t ref;
     fill_tc(p.variant, M, N, p.token_tile, p.stages, p.split_k, &ref);
+    if (p.tail_tiles != 0 || p.tail_split != 0) {
+        const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows);
+        if (!is_fp8_act_variant(p.variant) || ref.grid[1] != 1)
+            return fail(W8A16_ERR_PLAN, "a split-K tail needs the FP8 x FP8 kernel and one token tile");
+        if (p.tail_tiles < 1 || p.tail_tiles >= row_tiles || p.tail_split < 2 || p.tail_split > 16 ||
+            p.tail_split > ksteps)
+            return fail(W8A16_ERR_PLAN, "split-K tail: tail_tiles=" + u(p.tail_tiles) + " must be in 1.." +
+                                            u(row_tiles - 1) + " and tail_split=" + u(p.tail_split) +
+                                            " in 2..min(16, K/128)");
+        if (v_smem(p.variant, p.token_tile, p.stages, p.tail_split) > w8a16::kMaxDynSmem)
+            return fail(W8A16_ERR_PLAN, "split-K tail: tail_split=" + u(p.tail_split) +
+                                            " does not fit in shared memory");
+        ref.grid[0] = (row_tiles - p.tail_tiles) * p.split_k;
+    }
     if (p.grid[0] != ref.grid[0] || p.grid[1] != ref.grid[1] || p.cluster[0] != ref.cluster[0])
         return fail(W8A16_ERR_PLAN, "TC plan grid does not match the shape");
     if (ref.grid[1] > 65535u) return fail(W8A16_ERR_RANGE, "TC plan: too many token tiles");
@@ -305,6 +319,12 @@ uint32_t token_tile_for(int32_t v, uint32_t M) {
 // are not split. live[i] (NULL: model only) is the device's cluster table for
 // kA8Stages[i]; a zero entry rules that cluster size out.
 constexpr uint32_t kA8Stages[2] = {4, 6};
+// Stage counts the model may pick, from sweeps on GB300: six-stage rings did not
+// pay where two CTAs share an SM (decode, skinny), nor for 128-token tiles; the
+// 32-token two-term tile runs best one per SM with six.
+bool a8_stage_allowed(int32_t v, uint32_t tn, uint32_t st) {
+    return (v == W8A16_VARIANT_PRESPLIT && tn == 32) ? st == 6u : st == 4u;
+}
 
 void choose_w8a8(int32_t v, uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
                  uint32_t sm_count, const uint32_t* const live[2], uint32_t* split_out,
@@ -319,7 +339,7 @@ void choose_w8a8(int32_t v, uint32_t tn, uint32_t row_tiles, uint32_t token_tile
     *stages_out = kA8Stages[0];
     for (uint32_t i = 0; i < 2; ++i) {
         const uint32_t st = kA8Stages[i];
-        if (!v_supported(v, tn, st)) continue;
+        if (!v_supported(v, tn, st) || !a8_stage_allowed(v, tn, st)) continue;
         uint32_t cap[17];
         model_capacity(v, tn, st, sm_count, cap);
         for (uint32_t sp = 1; sp <= max_split; ++sp) {
@@ -341,6 +361,30 @@ void choose_w8a8(int32_t v, uint32_t tn, uint32_t row_tiles, uint32_t token_tile
     }
 }
 
+// Split-K tail for the FP8 x FP8 kernel: a plan of whole tiles (split 1, one token
+// tile) that needs a second, partial wave runs its last tiles in a second launch
+// instead, split over the largest cluster size whose CTAs all fit in one wave, so
+// that tail costs a fraction of a tile's time instead of a whole one. live (NULL:
+// model only) rules out cluster sizes the device cannot run.
+void add_tail(w8a16_plan_t* p, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, const uint32_t* live) {
+    const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows), ksteps = K / w8a16::kKStep;
+    if (!is_fp8_act_variant(p->variant) || p->split_k != 1 || ceil_div(M, p->token_tile) != 1) return;
+    uint32_t cap[17];
+    model_capacity(p->variant, p->token_tile, p->stages, sm_count, cap);
+    if (row_tiles <= cap[1] || row_tiles > 2u * cap[1]) return;
+    const uint32_t tail = row_tiles - cap[1];
+    uint32_t best = 0;
+    for (uint32_t k = 2; k <= (ksteps < 16u ? ksteps : 16u); ++k) {
+        if (v_smem(p->variant, p->token_tile, p->stages, k) > w8a16::kMaxDynSmem) continue;
+        if (live && live[k] == 0) continue;
+        if (tail * k <= cap[k]) best = k;
+    }
+    if (best < 2) return;
+    p->tail_tiles = tail;
+    p->tail_split = best;
+    p->grid[0] = cap[1];
+}
+
 // Pure planner: variant by M (or as given), token tile by M, stage count by
 // token tile, split from the wave model over `cap` (NULL: every cluster size
 // fills every SM slot). The W8A8 variant has its own model (choose_w8a8).
@@ -353,6 +397,7 @@ int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
         choose_w8a8(v, tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep, sm_count, nullptr,
                     &sp, &st);
         fill_tc(v, M, N, tn, st, sp, out);
+        add_tail(out, M, N, K, sm_count, nullptr);
         return W8A16_OK;
     }
     const uint32_t tn = token_tile_for(v, M);
@@ -429,6 +474,7 @@ int plan_live(int32_t v, uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& i
         choose_w8a8(v, tn, ceil_div(N, w8a16::kTcRows), ceil_div(M, tn), K / w8a16::kKStep,
                     static_cast<uint32_t>(info.sm_count), live, &sp, &st);
         fill_tc(v, M, N, tn, st, sp, out);
+        add_tail(out, M, N, K, static_cast<uint32_t>(info.sm_count), live[st == kA8Stages[0] ? 0 : 1]);
         return W8A16_OK;
     }
     const uint32_t stages = default_stages(v, tn);
@@ -757,6 +803,7 @@ int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint
         const uint32_t st = stages ? stages : a.stages;
         const uint32_t sp = split_k ? split_k : a.split_k;
         fill_tc(variant, M, N, a.token_tile, st, sp, &p);
+        if (!split_k) add_tail(&p, M, N, K, sm_count, nullptr);   // an explicit split has none
     } else {
         return fail(W8A16_ERR_PLAN, "w8a16_plan_variant: unknown variant " + std::to_string(variant));
     }

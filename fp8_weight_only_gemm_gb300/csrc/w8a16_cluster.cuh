@@ -14,6 +14,11 @@ namespace w8a16 {
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+// Release arrive, for a CTA whose shared memory peers may write once the barrier
+// completes (its loads and MMAs on that memory have all been waited for).
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -71,17 +71,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Acquire at cluster scope: for a barrier whose transactions are other CTAs'
+// st.async writes (their complete-tx releases at cluster scope, which a
+// CTA-scope acquire does not synchronise with).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up when the
 // CTA's abort flag is raised or the deadline passes (then raises the flag and
 // records the failure); returns false in both cases. Every wait in these
-// kernels goes through here, so no wait can spin forever.
+// kernels goes through here, so no wait can spin forever. CLUSTER: acquire at
+// cluster scope (the split-K receive barriers).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline,
                                           volatile int* abort_flag, DeviceStatus* st,
                                           unsigned int detail) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const auto try_wait = [](uint32_t b, uint32_t ph) {
+        return CLUSTER ? mbar_try_wait_cluster(b, ph) : mbar_try_wait(b, ph);
+    };
+    if (try_wait(bar, parity)) return true;
     uint32_t spins = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait(bar, parity)) return true;
         if ((++spins & 63u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() > deadline) {

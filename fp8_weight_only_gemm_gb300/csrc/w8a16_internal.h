@@ -138,10 +138,18 @@ constexpr uint32_t w8a8_max_ctas_by_regs(uint32_t tn) { return tn >= 64 ? 1u : 2
 // A tensor TMA writes shared memory at 128-byte aligned addresses only: each
 // slot of TN FP32 group scales is padded to a multiple of 128 bytes.
 constexpr uint32_t w8a8_scale_slot_bytes(uint32_t tn) { return (tn * 4u + 127u) / 128u * 128u; }
+// The split-K receive buffer reuses the rings' memory: partials are pushed only
+// after every rank of the cluster has finished its K steps.
+constexpr uint32_t w8a8_ring_bytes(uint32_t tn, uint32_t stages, uint32_t terms = 1) {
+    return stages * kTcRows * kKStep +
+           w8a8_act_stages(tn, terms) * (terms * tn * kKStep + w8a8_scale_slot_bytes(tn));
+}
 constexpr uint32_t w8a8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split, uint32_t terms = 1) {
-    return alone_if_full_tmem(1024u + stages * kTcRows * kKStep +
-                                  w8a8_act_stages(tn, terms) * (terms * tn * kKStep + w8a8_scale_slot_bytes(tn)) +
-                                  tc_red_bytes(tn, split) + 1024u,
+    return alone_if_full_tmem(1024u +
+                                  (w8a8_ring_bytes(tn, stages, terms) > tc_red_bytes(tn, split)
+                                       ? w8a8_ring_bytes(tn, stages, terms)
+                                       : tc_red_bytes(tn, split)) +
+                                  1024u,
                               w8a8_tmem_cols(tn, terms));
 }
 // Workspace of the two-term split: codes [2M][K] (hi rows, then lo rows) and

@@ -103,9 +103,10 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
 }
 
 // Warp-uniform bounded wait: every lane polls; the warp proceeds only if all did.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t deadline,
                                           volatile int* abort_flag, uint32_t detail) {
-    const bool ok = mbar_wait(bar, parity, deadline, abort_flag, &g_tc_status, detail);
+    const bool ok = mbar_wait<CLUSTER>(bar, parity, deadline, abort_flag, &g_tc_status, detail);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -315,8 +316,11 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
 #pragma unroll
             for (uint32_t c = 0; c < kChunks; ++c)
                 q[c] = *reinterpret_cast<const uint4*>(rp + (((slice * kChunks + c) ^ swz) << 4));
+            // the codes are in registers; TMA refills the slot next, so order these
+            // generic reads before that async-proxy write
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(wempty0 + 8u * s);   // the codes are in registers
+            if (lane == 0) mbar_arrive(wempty0 + 8u * s);
             uint32_t w[kChunks * 8];
 #pragma unroll
             for (uint32_t c = 0; c < kChunks; ++c) {
@@ -414,7 +418,8 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
                                    acc[4 * g + 3]);
             // This CTA's own rows: the thread holding row `row` of the tile (and
             // tokens fh*kTokPerFold..) adds the ranks' partials in rank order.
-            const bool got = warp_wait(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+            // the partials are other CTAs' st.async writes: acquire at cluster scope
+            const bool got = warp_wait<true>(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
             if (got && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
                 const uint32_t lr = row - my_row0;
                 const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats

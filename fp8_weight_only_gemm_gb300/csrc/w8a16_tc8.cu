@@ -74,9 +74,10 @@ struct T8Cfg {
 
 
 
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait8(uint32_t bar, uint32_t parity, uint64_t deadline,
                                            volatile int* abort_flag, uint32_t detail) {
-    const bool ok = mbar_wait(bar, parity, deadline, abort_flag, &g_tc8_status, detail);
+    const bool ok = mbar_wait<CLUSTER>(bar, parity, deadline, abort_flag, &g_tc8_status, detail);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -525,7 +526,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                                    acc[4 * g + 3]);
             // This CTA's own rows: the thread holding row `row` of the tile (and
             // tokens fh*kTokPerFold..) adds the ranks' partials in rank order.
-            const bool got = warp_wait8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+            // the partials are other CTAs' st.async writes: acquire at cluster scope
+            const bool got = warp_wait8<true>(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
             if (got && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
                 const uint32_t lr = row - my_row0;
                 const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats

@@ -67,9 +67,10 @@ struct A8Cfg {
     static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
 };
 
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool warp_wait_a8(uint32_t bar, uint32_t parity, uint64_t deadline,
                                              volatile int* abort_flag, uint32_t detail) {
-    const bool ok = mbar_wait(bar, parity, deadline, abort_flag, &g_w8a8_status, detail);
+    const bool ok = mbar_wait<CLUSTER>(bar, parity, deadline, abort_flag, &g_w8a8_status, detail);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     w8a16_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmS, const float* __restrict__ scale,
                       __nv_bfloat16* __restrict__ C, uint32_t ldc, uint32_t M, uint32_t N, uint32_t K,
-                      uint32_t split_k, uint64_t timeout_ns) {
+                      uint32_t split_k, uint32_t tile0, uint64_t timeout_ns) {
     using Cfg = A8Cfg<TN, STAGES, TERMS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -95,9 +96,11 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     uint8_t* sW = smem;                                        // STAGES x 16 KiB weights
     uint8_t* sX = sW + STAGES * kWTileBytes;                   // SA x NB x 128 activation codes
     float* sS = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kCodeBytes);   // SA slots of TN scales
-    float* sRed = sS + Cfg::SA * Cfg::kScaleSlot;              // split-K receive slots
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sRed) +
-                                                 tc_red_bytes(TN, split_k));
+    // split-K receive slots: the rings' memory, written by peers only once every
+    // rank of the cluster is past its last K step
+    float* sRed = reinterpret_cast<float*>(smem);
+    const uint32_t ring = w8a8_ring_bytes(TN, STAGES, TERMS), red = tc_red_bytes(TN, split_k);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (ring > red ? ring : red));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -113,8 +116,9 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     const uint32_t red_bar = done_bar + 8u;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tile = blockIdx.x / split_k;
-    const uint32_t rank = blockIdx.x - tile * split_k;
+    const uint32_t cta_tile = blockIdx.x / split_k;
+    const uint32_t rank = blockIdx.x - cta_tile * split_k;
+    const uint32_t tile = tile0 + cta_tile;                    // 128-row weight tile
     const uint32_t token0 = blockIdx.y * TN;
     const uint32_t ksteps = K / kKStep;                        // < 2^24: products fit 32 bits
     const uint32_t s_begin = rank * ksteps / split_k;
@@ -162,7 +166,6 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (split_k > 1) cluster_arrive();
     if (threadIdx.x == 0) grid_launch_dependents();
     const uint32_t tP = *tmem_slot;                            // NP x TN columns: FP32 products
     const uint32_t quarter = warp & 3;
@@ -188,6 +191,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             }
             drain_ring_a8(wfull0, STAGES, issued, timeout_ns);
         }
+        __syncwarp();
+        if (split_k > 1) cluster_arrive_release();
     } else if (warp == 2) {
         // ------------------------- activation producer (TMA): codes and scales
         if (lane == 0) {
@@ -213,6 +218,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             }
             drain_ring_a8(xfull0, Cfg::SA, issued, timeout_ns);
         }
+        __syncwarp();
+        if (split_k > 1) cluster_arrive_release();
     } else if (warp == 1 || warp == 3) {
         // ----------------------------------- MMA issuers: even steps, odd steps
         if (lane == 0) {
@@ -242,6 +249,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             volatile int never = 0;
             mbar_wait(done_bar, 0, globaltimer_ns() + timeout_ns, &never, &g_w8a8_status, kWaitDone);
         }
+        __syncwarp();
+        if (split_k > 1) cluster_arrive_release();
     } else if (is_fold) {
         // ------------------------- fold: acc += s_w * s_a[token] * P per token
         const uint32_t fh = (warp - Cfg::kFold0) >> 2;
@@ -286,6 +295,9 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 }
             }
             tc_fence_before();
+            // the slot's scales were read with generic loads and TMA refills it next:
+            // order those reads before the async-proxy write
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(pempty0 + 8u * p);
@@ -303,7 +315,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 }
             }
         } else {
-            cluster_wait();
+            cluster_arrive_release();
+            cluster_wait();   // every rank's loads and MMAs are done: the rings may be overwritten
             // the last rank r with r * 128 / split_k <= row (no division by split_k)
             const uint32_t owner = ((row + 1) * split_k - 1) / kTcRows;
             const uint32_t lrow = row - owned_row0(owner, split_k);
@@ -321,7 +334,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                                    acc[4 * g + 3]);
             // This CTA's own rows: the thread holding row `row` (and tokens
             // fh*kTokPerFold..) adds the ranks' partials in rank order.
-            const bool got = warp_wait_a8(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
+            // the partials are other CTAs' st.async writes: acquire at cluster scope
+            const bool got = warp_wait_a8<true>(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
             if (got && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
                 const uint32_t lr = row - my_row0;
                 const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats
@@ -358,7 +372,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
 }
 
 using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*,
-                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 struct A8Instance {
     uint32_t tn, stages, terms;
     A8KernelFn fn;
@@ -433,28 +447,39 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
         !tensor_map_act_codes(g.A, g.M * g.terms, g.K, g.lda, p.token_tile, dev, &mx, err) ||
         !tensor_map_act_scales(g.a_scale, g.M, g.K, g.a_scale_stride, p.token_tile, dev, &ms, err))
         return W8A16_ERR_LAUNCH;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
-    cfg.blockDim = dim3(w8a8_threads(p.token_tile, g.terms), 1, 1);
-    cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, p.split_k, g.terms);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.split_k;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, ms, g.scale,
-                           static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, p.split_k,
-                           timeout_ns);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        *err = std::string("W8A8 kernel launch failed: ") + cudaGetErrorString(e);
-        return W8A16_ERR_LAUNCH;
+    // One launch, or (a split-K tail) two: whole tiles [0, T - tail) at the plan's
+    // split, then tiles [T - tail, T) over clusters of tail_split CTAs, queued as a
+    // programmatic dependent launch of the first (which writes neither W nor its scales).
+    const uint32_t row_tiles = (g.N + kTcRows - 1) / kTcRows;
+    const uint32_t tail = p.tail_split > 1 ? p.tail_tiles : 0u;
+    for (uint32_t part = 0; part < (tail ? 2u : 1u); ++part) {
+        const uint32_t split = part == 0 ? p.split_k : p.tail_split;
+        const uint32_t tile0 = part == 0 ? 0u : row_tiles - tail;
+        const uint32_t ctas = part == 0 ? p.grid[0] : tail * p.tail_split;
+        if (ctas == 0) continue;
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(ctas, p.grid[1], 1);
+        cfg.blockDim = dim3(w8a8_threads(p.token_tile, g.terms), 1, 1);
+        cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, split, g.terms);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = (part == 1 || (flags & W8A16_FLAG_PDL)) ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, ms, g.scale,
+                               static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, split, tile0,
+                               timeout_ns);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            *err = std::string("W8A8 kernel launch failed: ") + cudaGetErrorString(e);
+            return W8A16_ERR_LAUNCH;
+        }
     }
     return W8A16_OK;
 }

@@ -170,6 +170,12 @@ typedef struct {
     uint32_t cluster[3];
     uint32_t smem_bytes;   /* dynamic shared memory per CTA */
     uint32_t tmem_cols;    /* tensor-memory columns per CTA (TC) */
+    uint32_t tail_tiles;   /* FP8 x FP8 kernel (W8A8, PRESPLIT), one token tile: the last
+                              tail_tiles 128-row weight tiles run in a second launch, split
+                              over clusters of tail_split CTAs, so that a partial second
+                              wave of whole tiles becomes a short wave of split ones
+                              (grid[0] then counts the first launch's CTAs); 0 = none */
+    uint32_t tail_split;   /* split-K of that second launch (>= 2 when tail_tiles > 0) */
 } w8a16_plan_t;
 
 /* The page's checks plus this library's (pointers may be NULL here: only sizes,

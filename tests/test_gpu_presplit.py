@@ -76,6 +76,59 @@ def test_forced_plans(M, N, K, lda, tile, split, stages):
     assert np.array_equal(got, run_ws(case, plan=p)), "same plan, different bits"
 
 
+def _tail_plan(M, N, K, token_tile, stages, tail_tiles, tail_split, variant=PRESPLIT):
+    """Whole tiles in a first launch, the last `tail_tiles` split over `tail_split` CTAs."""
+    from fp8_weight_only_gemm_gb300 import binding
+    p = binding.plan_variant(token_tile, N, K, variant, 1, stages)
+    p.tail_tiles, p.tail_split = tail_tiles, tail_split
+    p.grid[0] = (N + 127) // 128 - tail_tiles
+    return p
+
+
+@pytest.mark.parametrize("M,N,K,tile,stages,tail,tsplit", [
+    (20, 640, 1024, 32, 4, 2, 3), (100, 1000, 1280, 128, 4, 3, 2), (64, 384, 2048, 64, 6, 1, 16),
+    (9, 300, 512, 16, 4, 2, 4),
+])
+def test_split_k_tail(M, N, K, tile, stages, tail, tsplit):
+    case = workloads.make_case("strided_m32_n14336_k5120", M=M, N=N, K=K, a_row_stride=K + 64,
+                               c_row_stride=N + 5, seed=M + N + K + tail, outlier_frac=0.01)
+    p = _tail_plan(M, N, K, tile, stages, tail, tsplit)
+    got = run_ws(case, plan=p)
+    ref, exact, absum = oracle_full(case)
+    compare(case, got, ref, exact, absum, split_k=tsplit, label=f"tail M{M} N{N} tail{tail}x{tsplit}",
+            variant=3)
+    assert np.array_equal(got, run_ws(case, plan=p)), "same plan, different bits"
+
+
+@pytest.mark.parametrize("tile,split,stages", [(32, 2, 4), (32, 4, 4), (64, 2, 4)])
+def test_split_k_at_scale_repeated(tile, split, stages):
+    """Many clusters at once (two CTAs per SM where the plan allows), five runs,
+    each checked against the oracle and bit-identical to the first."""
+    case = workloads.make_case("strided_m32_n14336_k5120", M=32 if tile == 32 else 64)
+    wl = case.wl
+    p = _plan(wl.M, wl.N, wl.K, tile, split, stages)
+    ref, exact, absum = oracle_full(case)
+    first = None
+    for rep in range(5):
+        got = run_ws(case, plan=p)
+        if first is None:
+            compare(case, got, ref, exact, absum, split_k=split, label=f"scale tn{tile} s{split}", variant=3)
+            first = got
+        else:
+            assert np.array_equal(got, first), f"run {rep} differs from run 0"
+
+
+def test_planner_uses_a_tail_when_tiles_overflow_one_wave():
+    from fp8_weight_only_gemm_gb300 import binding
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = binding.plan_variant(128, 128 * (sms + sms // 2), 1024, PRESPLIT, 0, 0, sms)
+    assert p.split_k == 1 and p.tail_tiles == sms // 2 and p.tail_split == 2 and p.grid[0] == sms
+    case = workloads.make_case("tiny_m1_n256_k256", M=128, N=128 * (sms + sms // 2), K=1024, seed=88)
+    got = run_ws(case, plan=p)
+    ref, exact, absum = oracle_full(case)
+    compare(case, got, ref, exact, absum, split_k=2, label="planned tail", variant=3)
+
+
 @pytest.mark.parametrize("M,N,K", [(3, 256, 512), (40, 384, 1024)])
 def test_every_code_and_scale_range(M, N, K):
     case = workloads.random_codes_case(M, N, K, seed=M + N + K + 5)

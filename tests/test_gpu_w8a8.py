@@ -169,6 +169,54 @@ def test_w8a8_matches_oracle(o, M, N, K, apad, cpad, plan):
     assert binding.device_status() == (0, 0, 0)
 
 
+@pytest.mark.parametrize("tile,split,stages", [(32, 2, 4), (32, 4, 4), (64, 2, 4), (16, 8, 4)])
+def test_w8a8_split_k_at_scale_repeated(o, tile, split, stages):
+    """Split-K over many clusters, two CTAs per SM where the plan allows, five runs:
+    the owners' sums of the other ranks' pushed partials must see every push (a
+    receive wait without cluster-scope acquire read stale partials now and then)."""
+    from fp8_weight_only_gemm_gb300 import binding
+    M, N, K = tile if tile < 64 else 64, 14336, 5120
+    case = workloads.make_case(workloads.Workload(f"w8a8scale_{tile}", M, N, K, seed=tile + split))
+    Aq, a_scale = o.quantize_activations(case.A_np(), M, K)
+    Ad, Sd = _device_w8a8_inputs(Aq, a_scale, M, K, K, (M + 3) // 4 * 4)
+    p = _forced_plan(M, N, K, tile, split, stages)
+    Wd, Sw = case.W.cuda(), case.scale.cuda()
+    first = None
+    for rep in range(5):
+        C = case.C0.cuda()
+        binding.gemm_w8a8(Ad, Sd, Wd, Sw, C[:, :N], plan=p)
+        torch.cuda.synchronize()
+        got = C.cpu().view(torch.int16).numpy().view(np.uint16)
+        if first is None:
+            _w8a8_check(o, Aq, a_scale, case.W_np(), case.scale_np(), M, N, K, got, case.C0_np(), N, split,
+                        f"w8a8 scale tn{tile} s{split}")
+            first = got
+        else:
+            assert np.array_equal(got, first), f"run {rep} differs from run 0 (tn{tile} s{split})"
+    assert binding.device_status() == (0, 0, 0)
+
+
+@pytest.mark.parametrize("M,N,K,tile,tail,tsplit", [(30, 640, 1024, 32, 2, 4), (128, 900, 1536, 128, 3, 2)])
+def test_w8a8_split_k_tail(o, M, N, K, tile, tail, tsplit):
+    """Whole weight tiles in a first launch, the last ones split over clusters in a second."""
+    from fp8_weight_only_gemm_gb300 import binding
+    case = workloads.make_case(workloads.Workload(f"w8a8tail_m{M}", M, N, K, seed=M + N + tail,
+                                                  outlier_frac=0.01))
+    Aq, a_scale = o.quantize_activations(case.A_np(), M, K)
+    Ad, Sd = _device_w8a8_inputs(Aq, a_scale, M, K, K, (M + 3) // 4 * 4)
+    p = binding.plan_variant(tile, N, K, binding.VARIANT_W8A8, 1, 4)
+    p.grid[1] = (M + tile - 1) // tile
+    p.tail_tiles, p.tail_split = tail, tsplit
+    p.grid[0] = (N + 127) // 128 - tail
+    C = case.C0.cuda()
+    binding.gemm_w8a8(Ad, Sd, case.W.cuda(), case.scale.cuda(), C[:, :N], plan=p)
+    torch.cuda.synchronize()
+    got = C.cpu().view(torch.int16).numpy().view(np.uint16)
+    _w8a8_check(o, Aq, a_scale, case.W_np(), case.scale_np(), M, N, K, got, case.C0_np(), N, tsplit,
+                f"w8a8 tail M={M} N={N}")
+    assert binding.device_status() == (0, 0, 0)
+
+
 def test_w8a8_every_code(o):
     """Every finite E4M3 code on both sides (subnormals, -0, +-448) with group and
     block scales spread over 2^-8..2^8."""
