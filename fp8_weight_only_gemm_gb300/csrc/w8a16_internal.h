@@ -138,19 +138,35 @@ constexpr uint32_t w8a8_max_ctas_by_regs(uint32_t tn) { return tn >= 64 ? 1u : 2
 // A tensor TMA writes shared memory at 128-byte aligned addresses only: each
 // slot of TN FP32 group scales is padded to a multiple of 128 bytes.
 constexpr uint32_t w8a8_scale_slot_bytes(uint32_t tn) { return (tn * 4u + 127u) / 128u * 128u; }
-// The split-K receive buffer reuses the rings' memory: partials are pushed only
-// after every rank of the cluster has finished its K steps.
 constexpr uint32_t w8a8_ring_bytes(uint32_t tn, uint32_t stages, uint32_t terms = 1) {
     return stages * kTcRows * kKStep +
            w8a8_act_stages(tn, terms) * (terms * tn * kKStep + w8a8_scale_slot_bytes(tn));
 }
+// The split-K receive buffer normally follows the rings. Where that would not fit,
+// or would cost CTAs per SM, it reuses the rings' memory instead ("alias"): then
+// partials are pushed only after every rank of the cluster is past its K steps (a
+// cluster barrier at the end of the loops rather than at set-up).
+constexpr uint32_t w8a8_min3(uint32_t a, uint32_t b, uint32_t c) { return a < b ? (a < c ? a : c) : (b < c ? b : c); }
+constexpr uint32_t w8a8_ctas_for(uint32_t bytes, uint32_t tn, uint32_t terms) {
+    return w8a8_min3(233472u / (alone_if_full_tmem(bytes, w8a8_tmem_cols(tn, terms)) + 1024u),
+                     512u / w8a8_tmem_cols(tn, terms), w8a8_max_ctas_by_regs(tn));
+}
+constexpr bool w8a8_red_alias(uint32_t tn, uint32_t stages, uint32_t split, uint32_t terms = 1) {
+    return split > 1 &&
+           (2048u + w8a8_ring_bytes(tn, stages, terms) + tc_red_bytes(tn, split) > kMaxDynSmem ||
+            w8a8_ctas_for(2048u + w8a8_ring_bytes(tn, stages, terms) + tc_red_bytes(tn, split), tn, terms) <
+                w8a8_ctas_for(2048u + (w8a8_ring_bytes(tn, stages, terms) > tc_red_bytes(tn, split)
+                                           ? w8a8_ring_bytes(tn, stages, terms)
+                                           : tc_red_bytes(tn, split)),
+                              tn, terms));
+}
 constexpr uint32_t w8a8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split, uint32_t terms = 1) {
-    return alone_if_full_tmem(1024u +
-                                  (w8a8_ring_bytes(tn, stages, terms) > tc_red_bytes(tn, split)
-                                       ? w8a8_ring_bytes(tn, stages, terms)
-                                       : tc_red_bytes(tn, split)) +
-                                  1024u,
-                              w8a8_tmem_cols(tn, terms));
+    return alone_if_full_tmem(
+        2048u + (!w8a8_red_alias(tn, stages, split, terms)
+                     ? w8a8_ring_bytes(tn, stages, terms) + tc_red_bytes(tn, split)
+                     : (w8a8_ring_bytes(tn, stages, terms) > tc_red_bytes(tn, split) ? w8a8_ring_bytes(tn, stages, terms)
+                                                                                     : tc_red_bytes(tn, split))),
+        w8a8_tmem_cols(tn, terms));
 }
 // Workspace of the two-term split: codes [2M][K] (hi rows, then lo rows) and
 // factors [K/128][round_up(M, 4)] FP32.

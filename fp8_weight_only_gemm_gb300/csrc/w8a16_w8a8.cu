@@ -96,11 +96,12 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     uint8_t* sW = smem;                                        // STAGES x 16 KiB weights
     uint8_t* sX = sW + STAGES * kWTileBytes;                   // SA x NB x 128 activation codes
     float* sS = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kCodeBytes);   // SA slots of TN scales
-    // split-K receive slots: the rings' memory, written by peers only once every
-    // rank of the cluster is past its last K step
-    float* sRed = reinterpret_cast<float*>(smem);
+    // split-K receive slots: after the rings, or (alias) in the rings' memory, then
+    // written by peers only once every rank of the cluster is past its last K step
+    const bool alias = w8a8_red_alias(TN, STAGES, split_k, TERMS);
     const uint32_t ring = w8a8_ring_bytes(TN, STAGES, TERMS), red = tc_red_bytes(TN, split_k);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (ring > red ? ring : red));
+    float* sRed = reinterpret_cast<float*>(alias ? smem : smem + ring);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (alias ? (ring > red ? ring : red) : ring + red));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -166,6 +167,10 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Without aliasing, peers may push as soon as this CTA's receive barrier is
+    // initialised: a relaxed arrive (fence.mbarrier_init released the
+    // initialisation to the cluster), which does not wait for in-flight loads.
+    if (split_k > 1 && !alias) cluster_arrive();
     if (threadIdx.x == 0) grid_launch_dependents();
     const uint32_t tP = *tmem_slot;                            // NP x TN columns: FP32 products
     const uint32_t quarter = warp & 3;
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             drain_ring_a8(wfull0, STAGES, issued, timeout_ns);
         }
         __syncwarp();
-        if (split_k > 1) cluster_arrive_release();
+        if (split_k > 1 && alias) cluster_arrive_release();
     } else if (warp == 2) {
         // ------------------------- activation producer (TMA): codes and scales
         if (lane == 0) {
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             drain_ring_a8(xfull0, Cfg::SA, issued, timeout_ns);
         }
         __syncwarp();
-        if (split_k > 1) cluster_arrive_release();
+        if (split_k > 1 && alias) cluster_arrive_release();
     } else if (warp == 1 || warp == 3) {
         // ----------------------------------- MMA issuers: even steps, odd steps
         if (lane == 0) {
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             mbar_wait(done_bar, 0, globaltimer_ns() + timeout_ns, &never, &g_w8a8_status, kWaitDone);
         }
         __syncwarp();
-        if (split_k > 1) cluster_arrive_release();
+        if (split_k > 1 && alias) cluster_arrive_release();
     } else if (is_fold) {
         // ------------------------- fold: acc += s_w * s_a[token] * P per token
         const uint32_t fh = (warp - Cfg::kFold0) >> 2;
@@ -315,8 +320,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 }
             }
         } else {
-            cluster_arrive_release();
-            cluster_wait();   // every rank's loads and MMAs are done: the rings may be overwritten
+            if (alias) cluster_arrive_release();
+            cluster_wait();   // (alias) every rank's loads and MMAs are done: the rings may be overwritten
             // the last rank r with r * 128 / split_k <= row (no division by split_k)
             const uint32_t owner = ((row + 1) * split_k - 1) / kTcRows;
             const uint32_t lrow = row - owned_row0(owner, split_k);
