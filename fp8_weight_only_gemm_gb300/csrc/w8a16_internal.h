@@ -115,12 +115,11 @@ constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) 
 }
 
 // FP8 x FP8 kernel (W8A8, terms = 1; W8A16 from a two-term split, terms = 2): an
-// activation ring of SA slots (terms x TN x 128 codes + TN FP32 factors), NP
-// product buffers of terms x TN columns, 4 fold warps (8 from a 64-token tile),
-// two MMA issuers and the two producers in the first four warps. A slot is freed
-// by the fold of its step, so the ring keeps 4 slots (2 let every other step wait
-// out a whole load); the 128-token two-term tile has room in TMEM for 2 product
-// buffers of 256 columns.
+// activation ring of SA slots (terms x TN x 128 codes), NP product buffers of
+// terms x TN columns, 4 fold warps (8 from a 64-token tile), two MMA issuers and
+// the two producers in the first four warps; each fold warp stages its tokens'
+// FP32 factors of a step in a private buffer. The 128-token two-term tile has
+// room in TMEM for 2 product buffers of 256 columns.
 constexpr uint32_t w8a8_act_stages(uint32_t, uint32_t = 1) { return 4u; }
 constexpr uint32_t w8a8_p_bufs(uint32_t tn, uint32_t terms = 1) { return terms == 2 && tn >= 128 ? 2u : 4u; }
 // (16 for the 128-token two-term tile, whose fold reads two 128-column halves)
@@ -135,12 +134,10 @@ constexpr uint32_t w8a8_tmem_cols(uint32_t tn, uint32_t terms = 1) {
 // Registers: the 64- and 128-token instances (384 or 640 threads) run one CTA per
 // SM; the smaller ones are built for two.
 constexpr uint32_t w8a8_max_ctas_by_regs(uint32_t tn) { return tn >= 64 ? 1u : 2u; }
-// A tensor TMA writes shared memory at 128-byte aligned addresses only: each
-// slot of TN FP32 group scales is padded to a multiple of 128 bytes.
-constexpr uint32_t w8a8_scale_slot_bytes(uint32_t tn) { return (tn * 4u + 127u) / 128u * 128u; }
+// The fold warps' factor buffers: kTokPerFold FP32 per warp, 4 x TN in all.
+constexpr uint32_t w8a8_factor_bytes(uint32_t tn) { return 16u * tn; }
 constexpr uint32_t w8a8_ring_bytes(uint32_t tn, uint32_t stages, uint32_t terms = 1) {
-    return stages * kTcRows * kKStep +
-           w8a8_act_stages(tn, terms) * (terms * tn * kKStep + w8a8_scale_slot_bytes(tn));
+    return stages * kTcRows * kKStep + w8a8_act_stages(tn, terms) * terms * tn * kKStep + w8a8_factor_bytes(tn);
 }
 // The split-K receive buffer normally follows the rings. Where that would not fit,
 // or would cost CTAs per SM, it reuses the rings' memory instead ("alias"): then

@@ -17,10 +17,13 @@
 // splits its own tiles does (w8a16_tc8.cu).
 //
 // Warp roles: 0 weight producer (TMA), 1 TMEM owner + MMA issuer for even steps,
-// 2 activation producer (TMA: the step's codes and its TN group scales), 3 MMA
-// issuer for odd steps, then NF fold warps. Two issuers each wait only on their
-// own steps' slots (every ring has an even number of slots), so one thread's
-// waits overlap the other's MMAs.
+// 2 activation producer (TMA: the step's codes), 3 MMA issuer for odd steps, then
+// NF fold warps. Two issuers each wait only on their own steps' slots (every ring
+// has an even number of slots), so one thread's waits overlap the other's MMAs.
+// Both rings hold only MMA operands and are freed by MMA completion. The per-token
+// factors come from global memory: each fold warp loads its tokens' factors one
+// step ahead (lane l, token l) and stages them in its own shared buffer with
+// ordinary stores, so no generic access meets TMA-written memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,12 +57,12 @@ struct A8Cfg {
     static constexpr uint32_t NF = w8a8_fold_warps(TN, TERMS);
     static constexpr uint32_t kTmemCols = w8a8_tmem_cols(TN, TERMS);
     static constexpr uint32_t kCodeBytes = NB * kKStep;    // one step's E4M3 activation tile(s)
-    static constexpr uint32_t kScaleSlot = w8a8_scale_slot_bytes(TN) / 4u;   // floats per scale slot
     static constexpr uint32_t kFold0 = 4;                  // first fold warp
     static constexpr uint32_t kTokPerFold = TN * 4 / NF;
     static constexpr uint32_t ND = STAGES > SA ? (STAGES > NP ? STAGES : NP) : (SA > NP ? SA : NP);
-    // barriers: wfull[S], xfull[SA], xempty[SA], mdone[ND], pempty[NP], done, red
-    static constexpr uint32_t kNumBars = STAGES + 2 * SA + ND + NP + 2;
+    // barriers: wfull[S], xfull[SA], mdone[ND], pempty[NP], done, red
+    static constexpr uint32_t kNumBars = STAGES + SA + ND + NP + 2;
+    static constexpr uint32_t kFactorRegs = (kTokPerFold + 31) / 32;   // per lane
     static_assert(STAGES % 2 == 0 && SA % 2 == 0 && NP % 2 == 0, "rings of even depth");
     static_assert(NP * NB <= kTmemCols, "TMEM budget");
     static_assert(TERMS == 1 || TERMS == 2, "one or two activation terms");
@@ -86,7 +89,7 @@ __device__ __forceinline__ void drain_ring_a8(uint32_t bar_base, uint32_t depth,
 template <uint32_t TN, uint32_t STAGES, uint32_t TERMS>
 __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs(TN))
     w8a16_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ CUtensorMap tmS, const float* __restrict__ scale,
+                      const float* __restrict__ a_scale, uint32_t a_stride, const float* __restrict__ scale,
                       __nv_bfloat16* __restrict__ C, uint32_t ldc, uint32_t M, uint32_t N, uint32_t K,
                       uint32_t split_k, uint32_t tile0, uint64_t timeout_ns) {
     using Cfg = A8Cfg<TN, STAGES, TERMS>;
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* sW = smem;                                        // STAGES x 16 KiB weights
     uint8_t* sX = sW + STAGES * kWTileBytes;                   // SA x NB x 128 activation codes
-    float* sS = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kCodeBytes);   // SA slots of TN scales
+    float* sF = reinterpret_cast<float*>(sX + Cfg::SA * Cfg::kCodeBytes);   // fold warps' factors
     // split-K receive slots: after the rings, or (alias) in the rings' memory, then
     // written by peers only once every rank of the cluster is past its last K step
     const bool alias = w8a8_red_alias(TN, STAGES, split_k, TERMS);
@@ -106,12 +109,11 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     // mdone[i % ND] completes when step i's MMAs have: it frees weight slot
-    // i % STAGES and fills product buffer i % NP. The fold of step i frees
-    // activation slot i % SA (it reads the scales; the MMAs read the codes first).
+    // i % STAGES and activation slot i % SA and fills product buffer i % NP.
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t wfull0 = bar0;
-    const uint32_t xfull0 = wfull0 + 8u * STAGES, xempty0 = xfull0 + 8u * Cfg::SA;
-    const uint32_t mdone0 = xempty0 + 8u * Cfg::SA;
+    const uint32_t xfull0 = wfull0 + 8u * STAGES;
+    const uint32_t mdone0 = xfull0 + 8u * Cfg::SA;
     const uint32_t pempty0 = mdone0 + 8u * Cfg::ND;
     const uint32_t done_bar = pempty0 + 8u * Cfg::NP;
     const uint32_t red_bar = done_bar + 8u;
@@ -136,8 +138,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
             const uint32_t addr = bar0 + 8u * b;
             uint32_t count = 1;
-            if (addr >= xempty0 && addr < mdone0) count = Cfg::NF;          // fold warps
-            else if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;   // fold warps
+            if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;        // fold warps
             else if (addr == done_bar) count = 2;                           // MMA issuers
             mbar_init(addr, count);
         }
@@ -158,7 +159,6 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                         static_cast<int32_t>(tile * kTcRows), pol_w);
         }
         tma_prefetch_desc(&tmX);
-        tma_prefetch_desc(&tmS);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -206,10 +206,11 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             uint32_t issued = 0;
             for (uint32_t i = 0; i < nsteps; ++i) {
                 const uint32_t j = i % Cfg::SA;
-                if (i >= Cfg::SA && !mbar_wait(xempty0 + 8u * j, ((i / Cfg::SA) - 1) & 1, deadline,
+                const uint32_t q = i - Cfg::SA;   // slot j last held step q
+                if (i >= Cfg::SA && !mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline,
                                                abort_flag, &g_w8a8_status, kWaitXEmpty))
                     break;
-                mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kCodeBytes + TN * 4u);
+                mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kCodeBytes);
                 tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes), &tmX, xfull0 + 8u * j,
                             static_cast<int32_t>((s_begin + i) * kKStep), static_cast<int32_t>(token0),
                             pol_a);
@@ -217,8 +218,6 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                     tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes + TN * kKStep), &tmX, xfull0 + 8u * j,
                                 static_cast<int32_t>((s_begin + i) * kKStep),
                                 static_cast<int32_t>(M + token0), pol_a);
-                tma_load_2d(smem_u32(sS + j * Cfg::kScaleSlot), &tmS, xfull0 + 8u * j, static_cast<int32_t>(token0),
-                            static_cast<int32_t>(s_begin + i), pol_a);
                 issued = i + 1;
             }
             drain_ring_a8(xfull0, Cfg::SA, issued, timeout_ns);
@@ -266,22 +265,41 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         // this CTA's weight block scales, 32 per register (lane l: step 32c + l)
         float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
         float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
+        // this warp's per-token factors of a step: lane l holds token r*32 + l of the
+        // warp's tokens in fnext[r], loaded a step ahead (after the dependency wait:
+        // the factors may be the previous grid's output; L2 only, never a stale L1)
+        float* fbuf = sF + (warp - Cfg::kFold0) * Cfg::kTokPerFold;
+        const uint32_t tokf = token0 + fh * Cfg::kTokPerFold;
+        const auto load_factors = [&](uint32_t step, float (&f)[Cfg::kFactorRegs]) {
+#pragma unroll
+            for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r) {
+                const uint32_t t = r * 32u + lane;
+                f[r] = (t < Cfg::kTokPerFold && tokf + t < M)
+                           ? __ldcg(a_scale + static_cast<size_t>(s_begin + step) * a_stride + tokf + t)
+                           : 0.f;
+            }
+        };
+        grid_dependency_wait();
+        float fnext[Cfg::kFactorRegs];
+        load_factors(0, fnext);
         for (uint32_t i = 0; i < nsteps; ++i) {
             if (i != 0 && (i & 31u) == 0) {
                 sc_cur = sc_next;
                 sc_next = i + 32u + lane < nsteps ? __ldg(srow + i + 32u + lane) : 0.f;
             }
-            const uint32_t p = i % Cfg::NP, j = i % Cfg::SA;
+            const uint32_t p = i % Cfg::NP;
+            __syncwarp();   // the previous step's reads of fbuf are done
+#pragma unroll
+            for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r)
+                if (r * 32u + lane < Cfg::kTokPerFold) fbuf[r * 32u + lane] = fnext[r];
+            __syncwarp();   // ... and this step's factors are visible to the whole warp
+            if (i + 1 < nsteps) load_factors(i + 1, fnext);
             if (!warp_wait_a8(mdone0 + 8u * (i % Cfg::ND), (i / Cfg::ND) & 1, deadline, abort_flag,
                               kWaitMdone))
                 break;
-            // the slot's scales were written by TMA: observe its completion here too
-            // (already complete; the slot is not refilled before this warp frees it)
-            if (!warp_wait_a8(xfull0 + 8u * j, (i / Cfg::SA) & 1, deadline, abort_flag, kWaitX)) break;
             tc_fence_after();
             const float sw = __shfl_sync(0xFFFFFFFFu, sc_cur, i & 31u);
             const uint32_t pcol = tP + lane_bits + p * Cfg::NB + fh * Cfg::kTokPerFold;
-            const float* sa = sS + j * Cfg::kScaleSlot + fh * Cfg::kTokPerFold;
 #pragma unroll
             for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
                 float v[16];
@@ -292,22 +310,16 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                     tc_wait_ld();
 #pragma unroll
                     for (uint32_t t = 0; t < 16; ++t)
-                        acc[c + t] = fmaf(sw, fmaf(vl[t], 0.03125f, v[t]) * sa[c + t], acc[c + t]);
+                        acc[c + t] = fmaf(sw, fmaf(vl[t], 0.03125f, v[t]) * fbuf[c + t], acc[c + t]);
                 } else {
                     tc_wait_ld();
 #pragma unroll
-                    for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sw * sa[c + t], v[t], acc[c + t]);
+                    for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sw * fbuf[c + t], v[t], acc[c + t]);
                 }
             }
             tc_fence_before();
-            // the slot's scales were read with generic loads and TMA refills it next:
-            // order those reads before the async-proxy write
-            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(pempty0 + 8u * p);
-                mbar_arrive(xempty0 + 8u * j);
-            }
+            if (lane == 0) mbar_arrive(pempty0 + 8u * p);
         }
         if (split_k == 1) {
             if (row < rows_valid) {
@@ -376,7 +388,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     }
 }
 
-using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*,
+using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, uint32_t, const float*, __nv_bfloat16*,
                             uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 struct A8Instance {
     uint32_t tn, stages, terms;
@@ -447,10 +459,9 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
     wg.W = g.W;
     wg.N = g.N;
     wg.K = g.K;
-    CUtensorMap mw, mx, ms;
+    CUtensorMap mw, mx;
     if (!tc_tensor_map_w(wg, dev, &mw, err) ||
-        !tensor_map_act_codes(g.A, g.M * g.terms, g.K, g.lda, p.token_tile, dev, &mx, err) ||
-        !tensor_map_act_scales(g.a_scale, g.M, g.K, g.a_scale_stride, p.token_tile, dev, &ms, err))
+        !tensor_map_act_codes(g.A, g.M * g.terms, g.K, g.lda, p.token_tile, dev, &mx, err))
         return W8A16_ERR_LAUNCH;
     // One launch, or (a split-K tail) two: whole tiles [0, T - tail) at the plan's
     // split, then tiles [T - tail, T) over clusters of tail_split CTAs, queued as a
@@ -477,7 +488,7 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
         attr[1].val.programmaticStreamSerializationAllowed = (part == 1 || (flags & W8A16_FLAG_PDL)) ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, ms, g.scale,
+        e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, g.a_scale, g.a_scale_stride, g.scale,
                                static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, split, tile0,
                                timeout_ns);
         if (e != cudaSuccess) {
