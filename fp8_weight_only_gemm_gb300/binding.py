@@ -63,6 +63,8 @@ _SIGS = {
     "w8a16_quantize_weights": (_INT, [_VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP]),
     "w8a16_quantize_activations": (_INT, [_VP, _U32, _U32, _U32, _VP, _VP, _U32, _VP]),
     "w8a16_workspace_bytes": (_U64, [_U32, _U32]),
+    "w8a16_gemm_noalloc": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32, _VP]),
+    "w8a16_noalloc_scratch_bytes": (_U64, []),
     "w8a16_gemm_ws": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, ctypes.POINTER(Plan), _VP,
                              _U64, _U32, _VP]),
     "w8a16_gemm_w8a8": (_INT, [_VP, _U32, _VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32,
@@ -236,6 +238,35 @@ def gemm_ws(A, W, scale, C=None, *, workspace=None, stream=None, plan: Plan | No
                                ws_ptr, ws_bytes, flags, _stream_handle(stream))
     _check(rc)
     return C
+
+
+def gemm_noalloc(A, W, scale, C=None, *, stream=None, flags: int = 0):
+    """gemm() through w8a16_gemm_noalloc (the library's fixed scratch buffer; calls
+    must not overlap in time)."""
+    import torch
+    M, N, K = _shapes(A, W, scale, C)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N:
+        raise ValueError("C must be bfloat16 [M, >=N]")
+    if not (A.is_cuda and W.is_cuda and scale.is_cuda and C.is_cuda):
+        raise ValueError("all tensors must be on a CUDA device")
+    with torch.cuda.device(A.device):
+        rc = load().w8a16_gemm_noalloc(A.data_ptr(), A.stride(0), W.data_ptr(), scale.data_ptr(),
+                                       C.data_ptr(), C.stride(0), M, N, K, flags, _stream_handle(stream))
+    _check(rc)
+    return C
+
+
+def gemm_noalloc_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, stream=0,
+                     flags: int = 0) -> int:
+    """Raw-pointer w8a16_gemm_noalloc (returns the library's code; does not raise)."""
+    return load().w8a16_gemm_noalloc(A_ptr or None, a_row_stride, W_ptr or None, scale_ptr or None,
+                                     C_ptr or None, c_row_stride, M, N, K, flags, stream or None)
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load().w8a16_noalloc_scratch_bytes())
 
 
 def gemm_ws_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, ws_ptr, ws_bytes,

@@ -589,6 +589,36 @@ int run_ws(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, void* ws, uint6
     return run_presplit(g, plan, ws, ts.ns, stream);
 }
 
+// Scratch of the allocation-free entry point: a fixed device array in this
+// module, so a call allocates nothing; its address is looked up once per device.
+// Calls that overlap in time (other streams, other host threads) share it and race.
+constexpr uint64_t kNoAllocScratchBytes = 32ull << 20;
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+int noalloc_scratch(void** out, std::string* err) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        *err = "no usable CUDA device for the scratch buffer";
+        return W8A16_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            addr[dev] = nullptr;
+            *err = std::string("scratch buffer address: ") + cudaGetErrorString(e);
+            return W8A16_ERR_DEVICE;
+        }
+    }
+    *out = addr[dev];
+    return W8A16_OK;
+}
+
 int run_w8a8(const w8a16::W8A8Args& g, const w8a16_plan_t* forced, uint32_t flags,
              cudaStream_t stream) {
     if (flags & ~static_cast<uint32_t>(W8A16_FLAG_PDL))
@@ -709,6 +739,31 @@ uint64_t w8a16_workspace_bytes(uint32_t M, uint32_t K) {
     if (M == 0 || K == 0 || K % w8a16::kKStep != 0) return 0;
     return w8a16::split_ws_bytes(M, K);
 }
+
+int w8a16_gemm_noalloc(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale,
+                       void* C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K, uint32_t flags,
+                       w8a16_stream_t stream) {
+    int rc = check_sizes(a_row_stride, c_row_stride, M, N, K);
+    if (rc) return rc;
+    const uint64_t need = w8a16::split_ws_bytes(M, K);
+    if (M > 16 && need > kNoAllocScratchBytes)
+        return fail(W8A16_ERR_RANGE, "w8a16_gemm_noalloc: M=" + u(M) + ", K=" + u(K) + " need " +
+                                         std::to_string(need) + " bytes of scratch, above the fixed " +
+                                         std::to_string(kNoAllocScratchBytes));
+    rc = check_ptrs(A, W, block_scale, C);
+    if (rc) return rc;
+    void* scratch = nullptr;
+    if (M > 16) {
+        std::string err;
+        rc = noalloc_scratch(&scratch, &err);
+        if (rc) return fail(rc, err);
+    }
+    const w8a16::GemmArgs g{A, a_row_stride, W, block_scale, C, c_row_stride, M, N, K};
+    return run_ws(g, nullptr, scratch, scratch ? kNoAllocScratchBytes : 0, flags,
+                  static_cast<cudaStream_t>(stream));
+}
+
+uint64_t w8a16_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int w8a16_gemm_ws(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale, void* C,
                   uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t* plan,

@@ -239,6 +239,22 @@ W8A16_API int w8a16_gemm_ws(const void *A, uint32_t a_row_stride, const void *W,
                             void *workspace, uint64_t workspace_bytes, uint32_t flags,
                             w8a16_stream_t stream);
 
+/* The product without a caller's workspace and without any allocation (the paper
+ * has no counterpart): w8a16_gemm_ws on a fixed 32 MiB device buffer that is part of
+ * the library's module (w8a16_noalloc_scratch_bytes() bytes), whose address is
+ * looked up once per device. Same arguments, checks and results as w8a16_gemm_ws
+ * with plan = NULL; M <= 16 uses no scratch. W8A16_ERR_RANGE when M > 16 and
+ * w8a16_workspace_bytes(M, K) exceeds the buffer. Every value the kernels read
+ * from the buffer is written earlier in the same call, so nothing needs clearing.
+ * The buffer is shared: calls whose kernels may overlap in time (on other streams,
+ * or from other host threads without ordering) race on it and must not be issued;
+ * calls ordered on one stream are safe. */
+W8A16_API int w8a16_gemm_noalloc(const void *A, uint32_t a_row_stride, const void *W,
+                                 const float *block_scale, void *C, uint32_t c_row_stride,
+                                 uint32_t M, uint32_t N, uint32_t K, uint32_t flags,
+                                 w8a16_stream_t stream);
+W8A16_API uint64_t w8a16_noalloc_scratch_bytes(void);
+
 /* ---- errors and status -------------------------------------------------- */
 
 /* Message of the last failed call on this host thread ("" if none). */
