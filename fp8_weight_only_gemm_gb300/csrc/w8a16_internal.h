@@ -183,12 +183,9 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
 // device when launched in clusters of `cluster` CTAs.
 int tc_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_t* ctas,
                         std::string* err);
-// W8A8 operands: E4M3 activation codes [M][row_stride bytes] and FP32 activation
-// scales [K/128][scale_stride] (K-group major).
+// E4M3 activation codes [M][row_stride bytes] of the FP8 x FP8 kernel.
 bool tensor_map_act_codes(const void* codes, uint32_t M, uint32_t K, uint32_t row_stride,
                           uint32_t token_tile, int device, CUtensorMap* out, std::string* err);
-bool tensor_map_act_scales(const float* scales, uint32_t M, uint32_t K, uint32_t scale_stride,
-                           uint32_t token_tile, int device, CUtensorMap* out, std::string* err);
 int launch_quantize(const void* W, bool bf16, uint32_t ldw, uint32_t N, uint32_t K, void* codes,
                     float* scales, cudaStream_t s, std::string* err);
 int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,

@@ -521,21 +521,17 @@ bool get_map(const MapKey& key, int device, CUtensorMap* out, std::string* err) 
     }
     CUtensorMap m;
     std::memset(&m, 0, sizeof m);
-    // kinds: 0 E4M3 weights and 2 E4M3 activation codes (128-byte rows of a box,
-    // swizzled), 1 BF16 activations (64-value rows, swizzled), 3 FP32 activation
-    // scales (a box is box_rows consecutive tokens of one K group, no swizzle)
-    const bool u8 = key.kind == 0 || key.kind == 2, f32 = key.kind == 3;
+    // kinds: 0 E4M3 weights and 2 E4M3 activation codes (128-byte rows of a box),
+    // 1 BF16 activations (64-value rows); all with the 128-byte swizzle
+    const bool u8 = key.kind == 0 || key.kind == 2;
     const cuuint64_t dims[2] = {key.cols, key.rows};
     const cuuint64_t strides[1] = {key.stride};
-    const cuuint32_t box[2] = {u8 ? 128u : f32 ? key.box_rows : 64u, f32 ? 1u : key.box_rows};
+    const cuuint32_t box[2] = {u8 ? 128u : 64u, key.box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&m,
-                     u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                        : f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                     2, reinterpret_cast<void*>(key.ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(&m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     reinterpret_cast<void*>(key.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *err = "cuTensorMapEncodeTiled failed (CUresult " + std::to_string(static_cast<int>(r)) + ")";
         return false;
@@ -660,13 +656,6 @@ bool tensor_map_act_codes(const void* codes, uint32_t M, uint32_t K, uint32_t ro
                           uint32_t token_tile, int device, CUtensorMap* out, std::string* err) {
     return get_map({reinterpret_cast<uint64_t>(codes), M, K, row_stride, token_tile, 2}, device, out,
                    err);
-}
-
-bool tensor_map_act_scales(const float* scales, uint32_t M, uint32_t K, uint32_t scale_stride,
-                           uint32_t token_tile, int device, CUtensorMap* out, std::string* err) {
-    return get_map({reinterpret_cast<uint64_t>(scales), K / kKStep, M,
-                    static_cast<uint64_t>(scale_stride) * 4u, token_tile, 3},
-                   device, out, err);
 }
 
 bool tc_tensor_map_a(const GemmArgs& g, uint32_t token_tile, int device, CUtensorMap* out,

@@ -228,3 +228,30 @@ def test_presplit_plans(lib):
         assert p.variant == binding.VARIANT_PRESPLIT and p.token_tile == tn
         assert p.smem_bytes <= 232448 and p.tmem_cols in (128, 256, 512)
         assert p.grid[0] == 32 * p.split_k and p.block[0] in (256, 384, 640)
+
+
+def test_split_k_tail_plans_are_validated(lib):
+    """A tail needs the FP8 x FP8 kernel, one token tile, 1 <= tail_tiles < row tiles,
+    2 <= tail_split <= min(16, K/128) and a first launch of the remaining tiles; the
+    checks run before any device work."""
+    p = binding.plan_variant(128, 1280, 1024, binding.VARIANT_PRESPLIT, 1, 4)
+    args = (0x1000, 1024, 0x2000, 0x3000, 0x4000, 1280, 128, 1280, 1024)
+    ws = (0x5000, 1 << 24)
+    for tail, tsplit, grid0 in ((2, 1, 8), (10, 2, 0), (2, 9, 8), (2, 2, 10)):
+        p.tail_tiles, p.tail_split, p.grid[0] = tail, tsplit, grid0
+        rc = binding.gemm_ws_ptr(*args, *ws, plan=p)
+        assert rc == ERR["PLAN"], (tail, tsplit, grid0, rc, binding.last_error())
+    q = binding.plan_variant(8, 1280, 1024, binding.VARIANT_TC8, 1, 4)
+    q.tail_tiles, q.tail_split, q.grid[0] = 2, 2, 8
+    rc = binding.gemm_ws_ptr(0x1000, 1024, 0x2000, 0x3000, 0x4000, 1280, 8, 1280, 1024, *ws, plan=q)
+    assert rc == ERR["PLAN"] and "tail" in binding.last_error()
+
+
+def test_planner_adds_a_tail_only_past_one_wave(lib):
+    sms = 152
+    p = binding.plan_variant(128, 128 * 224, 8192, binding.VARIANT_PRESPLIT, 0, 0, sms)
+    assert (p.split_k, p.tail_tiles, p.tail_split, p.grid[0]) == (1, 72, 2, 152)
+    p = binding.plan_variant(128, 128 * 152, 8192, binding.VARIANT_PRESPLIT, 0, 0, sms)
+    assert p.tail_tiles == 0 and p.grid[0] == 152
+    p = binding.plan_variant(128, 128 * 224, 8192, binding.VARIANT_PRESPLIT, 1, 0, sms)
+    assert p.tail_tiles == 0, "an explicit split has no tail"
