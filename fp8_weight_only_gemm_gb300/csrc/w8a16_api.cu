@@ -320,11 +320,9 @@ uint32_t token_tile_for(int32_t v, uint32_t M) {
 // kA8Stages[i]; a zero entry rules that cluster size out.
 constexpr uint32_t kA8Stages[2] = {4, 6};
 // Stage counts the model may pick, from sweeps on GB300: six-stage rings did not
-// pay where two CTAs share an SM (decode, skinny), nor for 128-token tiles; the
-// 32-token two-term tile runs best one per SM with six.
-bool a8_stage_allowed(int32_t v, uint32_t tn, uint32_t st) {
-    return (v == W8A16_VARIANT_PRESPLIT && tn == 32) ? st == 6u : st == 4u;
-}
+// pay where two CTAs share an SM (decode, skinny, 32-token tiles), nor for
+// 128-token tiles.
+bool a8_stage_allowed(int32_t, uint32_t, uint32_t st) { return st == 4u; }
 
 void choose_w8a8(int32_t v, uint32_t tn, uint32_t row_tiles, uint32_t token_tiles, uint32_t ksteps,
                  uint32_t sm_count, const uint32_t* const live[2], uint32_t* split_out,

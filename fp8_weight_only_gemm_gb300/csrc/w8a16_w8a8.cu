@@ -266,8 +266,9 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
         float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
         // this warp's per-token factors of a step: lane l holds token r*32 + l of the
-        // warp's tokens in fnext[r], loaded a step ahead (after the dependency wait:
-        // the factors may be the previous grid's output; L2 only, never a stale L1)
+        // warp's tokens, loaded kAhead steps ahead into a queue of registers (a step
+        // can be shorter than an L2 round trip), after the dependency wait (the
+        // factors may be the previous grid's output; L2 only, never a stale L1)
         float* fbuf = sF + (warp - Cfg::kFold0) * Cfg::kTokPerFold;
         const uint32_t tokf = token0 + fh * Cfg::kTokPerFold;
         const auto load_factors = [&](uint32_t step, float (&f)[Cfg::kFactorRegs]) {
@@ -279,9 +280,18 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                            : 0.f;
             }
         };
+        constexpr uint32_t kAhead = 4;
         grid_dependency_wait();
-        float fnext[Cfg::kFactorRegs];
-        load_factors(0, fnext);
+        float fq[kAhead][Cfg::kFactorRegs];
+#pragma unroll
+        for (uint32_t d = 0; d < kAhead; ++d) {
+            if (d < nsteps) {
+                load_factors(d, fq[d]);
+            } else {
+#pragma unroll
+                for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r) fq[d][r] = 0.f;
+            }
+        }
         for (uint32_t i = 0; i < nsteps; ++i) {
             if (i != 0 && (i & 31u) == 0) {
                 sc_cur = sc_next;
@@ -291,9 +301,13 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             __syncwarp();   // the previous step's reads of fbuf are done
 #pragma unroll
             for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r)
-                if (r * 32u + lane < Cfg::kTokPerFold) fbuf[r * 32u + lane] = fnext[r];
+                if (r * 32u + lane < Cfg::kTokPerFold) fbuf[r * 32u + lane] = fq[0][r];
             __syncwarp();   // ... and this step's factors are visible to the whole warp
-            if (i + 1 < nsteps) load_factors(i + 1, fnext);
+#pragma unroll
+            for (uint32_t d = 0; d + 1 < kAhead; ++d)
+#pragma unroll
+                for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r) fq[d][r] = fq[d + 1][r];
+            if (i + kAhead < nsteps) load_factors(i + kAhead, fq[kAhead - 1]);
             if (!warp_wait_a8(mdone0 + 8u * (i % Cfg::ND), (i / Cfg::ND) & 1, deadline, abort_flag,
                               kWaitMdone))
                 break;
