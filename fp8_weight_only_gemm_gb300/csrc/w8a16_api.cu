@@ -273,8 +273,8 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
     fill_tc(p.variant, M, N, p.token_tile, p.stages, p.split_k, &ref);
     if (p.tail_tiles != 0 || p.tail_split != 0) {
         const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows);
-        if (!is_fp8_act_variant(p.variant) || ref.grid[1] != 1)
-            return fail(W8A16_ERR_PLAN, "a split-K tail needs the FP8 x FP8 kernel and one token tile");
+        if (!(is_fp8_act_variant(p.variant) || p.variant == W8A16_VARIANT_TC) || ref.grid[1] != 1)
+            return fail(W8A16_ERR_PLAN, "a split-K tail needs the BF16 or FP8 x FP8 kernel and one token tile");
         if (p.tail_tiles < 1 || p.tail_tiles >= row_tiles || p.tail_split < 2 || p.tail_split > 16 ||
             p.tail_split > ksteps)
             return fail(W8A16_ERR_PLAN, "split-K tail: tail_tiles=" + u(p.tail_tiles) + " must be in 1.." +
@@ -366,7 +366,9 @@ void choose_w8a8(int32_t v, uint32_t tn, uint32_t row_tiles, uint32_t token_tile
 // model only) rules out cluster sizes the device cannot run.
 void add_tail(w8a16_plan_t* p, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, const uint32_t* live) {
     const uint32_t row_tiles = ceil_div(N, w8a16::kTcRows), ksteps = K / w8a16::kKStep;
-    if (!is_fp8_act_variant(p->variant) || p->split_k != 1 || ceil_div(M, p->token_tile) != 1) return;
+    if (!(is_fp8_act_variant(p->variant) || p->variant == W8A16_VARIANT_TC) || p->split_k != 1 ||
+        ceil_div(M, p->token_tile) != 1)
+        return;
     uint32_t cap[17];
     model_capacity(p->variant, p->token_tile, p->stages, sm_count, cap);
     if (row_tiles <= cap[1] || row_tiles > 2u * cap[1]) return;
@@ -418,6 +420,7 @@ int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
                                ? 1u
                                : choose_split(row_tiles, token_tiles, ksteps, usable);
     fill_tc(v, M, N, tn, stages, split, out);
+    add_tail(out, M, N, K, sm_count, cap);
     return W8A16_OK;
 }
 

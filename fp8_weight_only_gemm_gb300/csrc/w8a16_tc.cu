@@ -126,7 +126,8 @@ template <uint32_t TN, uint32_t STAGES>
 __global__ void __launch_bounds__(tc_threads(TN), 1)
     w8a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                     const float* __restrict__ scale, __nv_bfloat16* __restrict__ C, uint32_t ldc,
-                    uint32_t M, uint32_t N, uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
+                    uint32_t M, uint32_t N, uint32_t K, uint32_t split_k, uint32_t tile0,
+                    uint64_t timeout_ns) {
     using Cfg = TcCfg<TN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     const uint32_t red_bar = done_bar + 8u;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tile = blockIdx.x / split_k;     // cluster = split_k consecutive CTAs
+    const uint32_t tile = tile0 + blockIdx.x / split_k;   // cluster = split_k consecutive CTAs
     const uint32_t rank = blockIdx.x % split_k;     // == rank in the cluster
     const uint32_t token0 = blockIdx.y * TN;
     const uint32_t ksteps = K / kKStep;
@@ -543,7 +544,7 @@ bool get_map(const MapKey& key, int device, CUtensorMap* out, std::string* err) 
 }
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*, uint32_t,
-                           uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+                           uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 
 struct TcInstance {
     uint32_t tn, stages;
@@ -622,28 +623,38 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
                  dev, &ma, err))
         return W8A16_ERR_LAUNCH;
 
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(p.grid[0], p.grid[1], 1);
-    cfg.blockDim = dim3(tc_threads(p.token_tile), 1, 1);
-    cfg.dynamicSmemBytes = tc_smem_bytes(p.token_tile, p.stages, p.split_k);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.split_k;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, kTcInstances[inst].fn, mw, ma, g.scale,
-                           static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, p.split_k,
-                           timeout_ns);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        *err = std::string("TC kernel launch failed: ") + cudaGetErrorString(e);
-        return W8A16_ERR_LAUNCH;
+    // One launch, or (a split-K tail) two: whole tiles [0, T - tail) at the plan's
+    // split, then tiles [T - tail, T) over clusters of tail_split CTAs, queued as a
+    // programmatic dependent launch of the first (which writes neither W nor its scales).
+    const uint32_t row_tiles = (g.N + kTcRows - 1) / kTcRows;
+    const uint32_t tail = p.tail_split > 1 ? p.tail_tiles : 0u;
+    for (uint32_t part = 0; part < (tail ? 2u : 1u); ++part) {
+        const uint32_t split = part == 0 ? p.split_k : p.tail_split;
+        const uint32_t ctas = part == 0 ? p.grid[0] : tail * p.tail_split;
+        if (ctas == 0) continue;
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(ctas, p.grid[1], 1);
+        cfg.blockDim = dim3(tc_threads(p.token_tile), 1, 1);
+        cfg.dynamicSmemBytes = tc_smem_bytes(p.token_tile, p.stages, split);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = (part == 1 || (flags & W8A16_FLAG_PDL)) ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kTcInstances[inst].fn, mw, ma, g.scale,
+                               static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, split,
+                               part == 0 ? 0u : row_tiles - tail, timeout_ns);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            *err = std::string("TC kernel launch failed: ") + cudaGetErrorString(e);
+            return W8A16_ERR_LAUNCH;
+        }
     }
     return W8A16_OK;
 }

@@ -254,3 +254,20 @@ def test_live_plan_and_capacity():
     assert cap[p["split_k"]] > 0, (p, cap)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert p["grid"][0] * p["grid"][1] <= sms * p["ctas_per_sm"], p
+
+
+@pytest.mark.parametrize("M,N,K,stages,tail,tsplit", [
+    (100, 1000, 1280, 4, 3, 2), (40, 640, 2048, 4, 2, 4), (20, 900, 1024, 4, 4, 3)])
+def test_bf16_kernel_split_k_tail(M, N, K, stages, tail, tsplit):
+    """BF16 kernel: whole weight tiles in a first launch, the last ones split over
+    clusters in a second (programmatic dependent) launch; twice, bit for bit."""
+    from fp8_weight_only_gemm_gb300 import binding
+    case = workloads.make_case("strided_m32_n14336_k5120", M=M, N=N, K=K, a_row_stride=K + 64,
+                               c_row_stride=N + 3, seed=M + N + tail)
+    p = _plan(M, N, K, binding.VARIANT_TC, split_k=1, stages=stages)
+    p.tail_tiles, p.tail_split = tail, tsplit
+    p.grid[0] = -(-N // 128) - tail
+    got = run_gpu(case, plan=p)
+    ref, exact, absum = oracle_full(case)
+    compare(case, got, ref, exact, absum, split_k=tsplit, label=f"bf16 tail M{M} {tail}x{tsplit}")
+    assert np.array_equal(got, run_gpu(case, plan=p))

@@ -105,7 +105,11 @@ def test_plans_for_the_workloads(lib, M, N, K, tn):
     assert p["token_tile"] == tn
     ksteps = K // 128
     assert 1 <= p["split_k"] <= min(16, ksteps)
-    assert p["grid"][0] == -(-N // 128) * p["split_k"]
+    # a split-K tail moves the last tail_tiles weight tiles to a second launch
+    assert p["grid"][0] == (-(-N // 128) - p["tail_tiles"]) * p["split_k"]
+    if p["tail_tiles"]:
+        assert p["split_k"] == 1 and 2 <= p["tail_split"] <= min(16, ksteps)
+        assert p["grid"][0] == 152 and p["tail_tiles"] * p["tail_split"] <= 152
     assert p["grid"][1] == -(-M // tn)
     assert p["cluster"][0] == p["split_k"]
     if p["variant"] == binding.VARIANT_TC8:
