@@ -183,7 +183,9 @@ def bench_gpu(args, ws, rank, local):
     plan = (w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_W8A8, 0, 0, sms).as_dict() if w8a8 else
             w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_PRESPLIT, 0, 0, sms).as_dict() if presplit else
             w8.plan_current(wl.M, wl.N, wl.K))
-    launches_per_step = 2 if (w8a8 or presplit) else 1
+    # kernel launches per step: the quantiser or split pre-pass (W8A8, pre-split), then
+    # the GEMM, which is two launches when the plan has a split-K tail
+    launches_per_step = (1 if (w8a8 or presplit) else 0) + (2 if plan.get("tail_tiles") else 1)
     stream = torch.cuda.Stream(dev)
     lib = w8.load()
     sh = int(stream.cuda_stream)
