@@ -45,7 +45,7 @@ namespace {
 constexpr uint32_t kWTileBytes = kTcRows * kKStep;   // 16 KiB of E4M3 weights per stage
 
 enum : uint32_t {
-    kWaitW = 21, kWaitX = 22, kWaitXEmpty = 23, kWaitMdone = 24, kWaitPEmpty = 25, kWaitDone = 26,
+    kWaitW = 21, kWaitX = 22, kWaitXSlot = 23, kWaitMdone = 24, kWaitPEmpty = 25, kWaitDone = 26,
     kWaitDrain = 27, kWaitRed = 28
 };
 
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         __syncwarp();
         if (split_k > 1 && alias) cluster_arrive_release();
     } else if (warp == 2) {
-        // ------------------------- activation producer (TMA): codes and scales
+        // ------------------------------------ activation producer (TMA): codes
         if (lane == 0) {
             const uint64_t pol_a = l2_policy_evict_last();
             grid_dependency_wait();   // the activations may be the previous grid's output
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 const uint32_t j = i % Cfg::SA;
                 const uint32_t q = i - Cfg::SA;   // slot j last held step q
                 if (i >= Cfg::SA && !mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline,
-                                               abort_flag, &g_w8a8_status, kWaitXEmpty))
+                                               abort_flag, &g_w8a8_status, kWaitXSlot))
                     break;
                 mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kCodeBytes);
                 tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes), &tmX, xfull0 + 8u * j,
