@@ -67,6 +67,18 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's);
+    the value itself with one rank."""
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -268,12 +280,9 @@ def bench_gpu(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         if clk.samples == [] and args.steps > 0:
             time.sleep(0.25)
-    ms = start.elapsed_time(end)
+    ms = max_over_ranks(start.elapsed_time(end), ws, dev)
     if ws > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     kernel_bytes, kernel_us = wl.roofline_bytes(), ms * 1e3 / args.steps
     if w8a8:
