@@ -247,3 +247,24 @@ def test_programmatic_chain_through_the_workspace():
     ref_bits = chain(0)
     for _ in range(3):
         assert np.array_equal(chain(binding.FLAG_PDL), ref_bits)
+
+
+def test_split_k_tail_with_shared_receive_buffer_repeated():
+    """The 128-token two-term tile's split-K tail reuses the rings' shared memory for
+    the partials (the end-of-loop cluster barrier orders it): at full size, five runs
+    bit-identical, the first against the oracle."""
+    from fp8_weight_only_gemm_gb300 import binding
+    case = workloads.make_case("multitile_m128_n28672_k8192")
+    wl = case.wl
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = binding.plan_variant(wl.M, wl.N, wl.K, PRESPLIT, 0, 0, sms)
+    assert p.tail_tiles > 0 and p.tail_split >= 2
+    first = None
+    for rep in range(5):
+        got = run_ws(case, plan=p)
+        if first is None:
+            ref, exact, absum = oracle_full(case)
+            compare(case, got, ref, exact, absum, split_k=p.tail_split, label="tail alias", variant=3)
+            first = got
+        else:
+            assert np.array_equal(got, first), f"run {rep} differs from run 0"
