@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     w8a16_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                     const float* __restrict__ scale, __nv_bfloat16* __restrict__ C, uint32_t ldc,
                     uint32_t M, uint32_t N, uint32_t K, uint32_t split_k, uint32_t tile0,
-                    uint64_t timeout_ns) {
+                    uint32_t tok_major, uint64_t timeout_ns) {
     using Cfg = TcCfg<TN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -152,9 +152,12 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     const uint32_t red_bar = done_bar + 8u;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tile = tile0 + blockIdx.x / split_k;   // cluster = split_k consecutive CTAs
-    const uint32_t rank = blockIdx.x % split_k;     // == rank in the cluster
-    const uint32_t token0 = blockIdx.y * TN;
+    // tok_major (no split): the token tiles of one weight tile are consecutive CTAs, so
+    // beyond 128 tokens the later ones find the tile's weights in L2
+    const uint32_t bx = tok_major ? blockIdx.y : blockIdx.x, by = tok_major ? blockIdx.x : blockIdx.y;
+    const uint32_t tile = tile0 + bx / split_k;   // cluster = split_k consecutive CTAs
+    const uint32_t rank = bx % split_k;           // == rank in the cluster
+    const uint32_t token0 = by * TN;
     const uint32_t ksteps = K / kKStep;
     const uint32_t s_begin = static_cast<uint32_t>(static_cast<uint64_t>(rank) * ksteps / split_k);
     const uint32_t s_end = static_cast<uint32_t>(static_cast<uint64_t>(rank + 1) * ksteps / split_k);
@@ -544,7 +547,7 @@ bool get_map(const MapKey& key, int device, CUtensorMap* out, std::string* err) 
 }
 
 using TcKernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, __nv_bfloat16*, uint32_t,
-                           uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+                           uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 
 struct TcInstance {
     uint32_t tn, stages;
@@ -632,9 +635,10 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
         const uint32_t split = part == 0 ? p.split_k : p.tail_split;
         const uint32_t ctas = part == 0 ? p.grid[0] : tail * p.tail_split;
         if (ctas == 0) continue;
+        const uint32_t tok_major = (split == 1 && p.grid[1] > 1 && ctas <= 65535u) ? 1u : 0u;
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(ctas, p.grid[1], 1);
+        cfg.gridDim = tok_major ? dim3(p.grid[1], ctas, 1) : dim3(ctas, p.grid[1], 1);
         cfg.blockDim = dim3(tc_threads(p.token_tile), 1, 1);
         cfg.dynamicSmemBytes = tc_smem_bytes(p.token_tile, p.stages, split);
         cfg.stream = s;
@@ -649,7 +653,7 @@ int launch_tc(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t
         cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, kTcInstances[inst].fn, mw, ma, g.scale,
                                static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, split,
-                               part == 0 ? 0u : row_tiles - tail, timeout_ns);
+                               part == 0 ? 0u : row_tiles - tail, tok_major, timeout_ns);
         if (e != cudaSuccess) {
             cudaGetLastError();
             *err = std::string("TC kernel launch failed: ") + cudaGetErrorString(e);

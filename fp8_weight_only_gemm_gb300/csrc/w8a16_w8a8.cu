@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     w8a16_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const float* __restrict__ a_scale, uint32_t a_stride, const float* __restrict__ scale,
                       __nv_bfloat16* __restrict__ C, uint32_t ldc, uint32_t M, uint32_t N, uint32_t K,
-                      uint32_t split_k, uint32_t tile0, uint64_t timeout_ns) {
+                      uint32_t split_k, uint32_t tile0, uint32_t tok_major, uint64_t timeout_ns) {
     using Cfg = A8Cfg<TN, STAGES, TERMS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -119,10 +119,13 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     const uint32_t red_bar = done_bar + 8u;
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t cta_tile = blockIdx.x / split_k;
-    const uint32_t rank = blockIdx.x - cta_tile * split_k;
+    // tok_major (no split): the token tiles of one weight tile are consecutive CTAs, so
+    // beyond the token tile the later ones find the tile's weights in L2
+    const uint32_t bx = tok_major ? blockIdx.y : blockIdx.x, by = tok_major ? blockIdx.x : blockIdx.y;
+    const uint32_t cta_tile = bx / split_k;
+    const uint32_t rank = bx - cta_tile * split_k;
     const uint32_t tile = tile0 + cta_tile;                    // 128-row weight tile
-    const uint32_t token0 = blockIdx.y * TN;
+    const uint32_t token0 = by * TN;
     const uint32_t ksteps = K / kKStep;                        // < 2^24: products fit 32 bits
     const uint32_t s_begin = rank * ksteps / split_k;
     const uint32_t s_end = (rank + 1) * ksteps / split_k;
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
 }
 
 using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, uint32_t, const float*, __nv_bfloat16*,
-                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
 struct A8Instance {
     uint32_t tn, stages, terms;
     A8KernelFn fn;
@@ -487,9 +490,10 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
         const uint32_t tile0 = part == 0 ? 0u : row_tiles - tail;
         const uint32_t ctas = part == 0 ? p.grid[0] : tail * p.tail_split;
         if (ctas == 0) continue;
+        const uint32_t tok_major = (split == 1 && p.grid[1] > 1 && ctas <= 65535u) ? 1u : 0u;
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(ctas, p.grid[1], 1);
+        cfg.gridDim = tok_major ? dim3(p.grid[1], ctas, 1) : dim3(ctas, p.grid[1], 1);
         cfg.blockDim = dim3(w8a8_threads(p.token_tile, g.terms), 1, 1);
         cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, split, g.terms);
         cfg.stream = s;
@@ -504,7 +508,7 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
         cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, g.a_scale, g.a_scale_stride, g.scale,
                                static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, split, tile0,
-                               timeout_ns);
+                               tok_major, timeout_ns);
         if (e != cudaSuccess) {
             cudaGetLastError();
             *err = std::string("W8A8 kernel launch failed: ") + cudaGetErrorString(e);
