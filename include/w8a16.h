@@ -124,6 +124,8 @@ enum {
  * stream       CUDA stream for the work
  *
  * Returns W8A16_OK once the work is queued, or a W8A16_ERR_* code (nothing queued).
+ * The work is one kernel launch, or two when the plan has a split-K tail
+ * (w8a16_plan_t.tail_tiles; the second is a programmatic dependent of the first).
  * C may alias neither A, W nor block_scale.
  */
 W8A16_API int w8a16_gemm(const void *A, uint32_t a_row_stride, const void *W, const float *block_scale,
@@ -223,9 +225,10 @@ W8A16_API uint64_t w8a16_workspace_bytes(uint32_t M, uint32_t K);
  * shares). With plan == NULL the library chooses: M <= 16, or no workspace of
  * w8a16_workspace_bytes(M, K) bytes, runs exactly what w8a16_gemm runs; otherwise
  * the pre-split path (W8A16_VARIANT_PRESPLIT): a split kernel writes the workspace,
- * then the FP8 x FP8 kernel reads it (two launches on `stream`, queued as
- * programmatic dependent launches of each other; W8A16_FLAG_PDL governs only the
- * first one's overlap with the previous kernel, as for w8a16_gemm). A plan from
+ * then the FP8 x FP8 kernel reads it (one launch, or two when the plan has a split-K
+ * tail; all on `stream`, each queued as a programmatic dependent launch of the one
+ * before; W8A16_FLAG_PDL governs only the split kernel's overlap with the previous
+ * kernel, as for w8a16_gemm). A plan from
  * w8a16_plan_variant forces a variant (PRESPLIT needs the workspace, else
  * W8A16_ERR_ARG).
  *   workspace  device memory, 16-byte aligned, owned by the caller, or NULL; it is
