@@ -259,3 +259,37 @@ def test_planner_adds_a_tail_only_past_one_wave(lib):
     assert p.tail_tiles == 0 and p.grid[0] == 152
     p = binding.plan_variant(128, 128 * 224, 8192, binding.VARIANT_PRESPLIT, 1, 0, sms)
     assert p.tail_tiles == 0, "an explicit split has no tail"
+
+
+@pytest.mark.parametrize("variant", [0, 2, 3, 4, 5])
+def test_planner_invariants_over_shapes(lib, variant):
+    """Every plan the pure planner emits fits one SM's resources, covers the shape
+    exactly once (grid x split x tail) and keeps its split and tail in range."""
+    Ms = [1, 2, 7, 16, 17, 31, 32, 33, 64, 65, 100, 128, 129, 200, 256, 1000]
+    Ns = [1, 100, 128, 129, 1000, 4096, 12288, 28672, 38912]
+    Ks = [128, 256, 1280, 4096, 8192]
+    for M in Ms:
+        for N in Ns:
+            for K in Ks:
+                try:
+                    p = binding.plan_variant(M, N, K, variant, 0, 0, 152)
+                except binding.W8A16Error as e:
+                    pytest.fail(f"no plan for M={M} N={N} K={K} v={variant}: {e}")
+                d = p.as_dict()
+                if d["variant"] == binding.VARIANT_SIMT:
+                    continue
+                ksteps, row_tiles = K // 128, -(-N // 128)
+                assert 1 <= d["split_k"] <= min(16, ksteps)
+                assert d["smem_bytes"] <= 232448 and d["tmem_cols"] in (32, 64, 128, 256, 512)
+                assert d["ctas_per_sm"] >= 1
+                assert d["tmem_cols"] * d["ctas_per_sm"] <= 512
+                assert (d["smem_bytes"] + 1024) * d["ctas_per_sm"] <= 233472
+                assert d["block"][0] * d["ctas_per_sm"] <= 2048
+                assert d["grid"][1] == -(-M // d["token_tile"]) and d["grid"][1] <= 65535
+                tail = d["tail_tiles"]
+                assert d["grid"][0] == (row_tiles - tail) * d["split_k"]
+                if tail:
+                    assert d["grid"][1] == 1 and d["split_k"] == 1
+                    assert 2 <= d["tail_split"] <= min(16, ksteps)
+                    assert 0 < tail < row_tiles
+                    assert tail * d["tail_split"] <= 152 * d["ctas_per_sm"]
