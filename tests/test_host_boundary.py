@@ -293,3 +293,42 @@ def test_planner_invariants_over_shapes(lib, variant):
                     assert 2 <= d["tail_split"] <= min(16, ksteps)
                     assert 0 < tail < row_tiles
                     assert tail * d["tail_split"] <= 152 * d["ctas_per_sm"]
+
+
+@pytest.mark.parametrize("args,code,needle", [
+    # (lda, a_scale_stride, ldc, M, N, K)
+    ((256, 8, 256, 0, 256, 256), ERR["M_ZERO"], "m=0"),
+    ((256, 8, 256, 8, 256, 200), ERR["K_BLOCK"], "K=200"),
+    ((200, 8, 256, 8, 256, 256), ERR["PITCH"], "a=200"),
+    ((256, 4, 256, 8, 256, 256), ERR["PITCH"], "a_scale=4"),
+    ((264, 8, 256, 8, 256, 256), ERR["A_PITCH_ALIGN"], "a_row_stride=264"),
+    ((256, 10, 256, 8, 256, 256), ERR["A_PITCH_ALIGN"], "a_scale_stride=10"),
+    ((256, 8, 256, 8, 0, 256), ERR["N_ZERO"], "n=0"),
+])
+def test_w8a8_checks(lib, args, code, needle):
+    lda, sst, ldc, M, N, K = args
+    rc = binding.gemm_w8a8_ptr(0x1000, lda, 0x2000, sst, 0x3000, 0x4000, 0x5000, ldc, M, N, K)
+    assert rc == code and needle in binding.last_error(), (rc, binding.last_error())
+
+
+def test_w8a8_pointer_and_flag_checks(lib):
+    good = (0x1000, 256, 0x2000, 8, 0x3000, 0x4000, 0x5000, 256, 8, 256, 256)
+    assert binding.gemm_w8a8_ptr(0, *good[1:]) == ERR["NULL"]
+    assert binding.gemm_w8a8_ptr(0x1008, *good[1:]) == ERR["ALIGN"]
+    assert binding.gemm_w8a8_ptr(*good[:2], 0x2008, *good[3:]) == ERR["ALIGN"]
+    assert binding.gemm_w8a8_ptr(*good, flags=2) == -13
+
+
+@pytest.mark.parametrize("args,code,needle", [
+    # (a_row_stride, M, K, scale_stride)
+    ((256, 0, 256, 4), ERR["M_ZERO"], "m=0"),
+    ((256, 4, 200, 4), ERR["K_BLOCK"], "K=200"),
+    ((200, 4, 256, 4), ERR["PITCH"], "a_row_stride=200"),
+    ((256, 5, 256, 4), ERR["PITCH"], "scale_stride=4"),
+    ((260, 4, 256, 4), ERR["A_PITCH_ALIGN"], "a_row_stride=260"),
+    ((256, 4, 256, 6), ERR["A_PITCH_ALIGN"], "scale_stride=6"),
+])
+def test_activation_quantiser_checks(lib, args, code, needle):
+    lda, M, K, sst = args
+    rc = binding.load().w8a16_quantize_activations(0x1000, lda, M, K, 0x2000, 0x3000, sst, None)
+    assert rc == code and needle in binding.last_error(), (rc, binding.last_error())
