@@ -59,14 +59,23 @@ double oracle_e4m3_to_double(uint8_t code)
     if (e == 0xF && m == 0x7)
         return NAN;
     if (e == 0)
+#if ORACLE_MUTANT == 9
+        mag = ldexp(8.0 + m, -10); /* mutant: subnormals given the implicit leading one */
+#else
         mag = ldexp((double)m, -9); /* m/8 * 2^-6 */
+#endif
     else
 #if ORACLE_MUTANT == 1
         mag = ldexp(8.0 + m, e - 7 - 2); /* mutant: exponent bias off by one */
 #else
         mag = ldexp(8.0 + m, e - 7 - 3); /* (1 + m/8) * 2^(e-7) */
 #endif
+#if ORACLE_MUTANT == 14
+    (void)sign;
+    return mag; /* mutant: sign bit dropped */
+#else
     return sign ? -mag : mag;
+#endif
 }
 
 /* ---- BF16 <-> FP64 -------------------------------------------------------
@@ -103,6 +112,8 @@ uint16_t oracle_double_to_bf16_rne(double x)
             q = -133; /* subnormal range: fixed quantum */
 #if ORACLE_MUTANT == 2
         const double r = floor(ldexp(a, -q)); /* mutant: truncation instead of RNE */
+#elif ORACLE_MUTANT == 15
+        const double r = round(ldexp(a, -q)); /* mutant: ties away from zero */
 #else
         const double r = nearbyint(ldexp(a, -q)); /* default mode: ties to even */
 #endif
@@ -144,10 +155,19 @@ static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_
                        double *abs_out)
 {
     const uint32_t kb_count = j->K / 128;
+#if ORACLE_MUTANT == 10
+    const uint16_t *arow = j->A ? j->A + (uint64_t)m * j->K : NULL; /* mutant: pitch ignored */
+#else
     const uint16_t *arow = j->A ? j->A + (uint64_t)m * j->a_row_stride : NULL;
+#endif
     const uint8_t *wrow = j->W + (uint64_t)n * j->K;
     const float *srow = j->scale + (uint64_t)(n / 128) * kb_count;
+#if ORACLE_MUTANT == 17
+    float sum = 0.0f; /* mutant: the sum carried in FP32 */
+    double asum = 0.0;
+#else
     double sum = 0.0, asum = 0.0;
+#endif
     for (uint32_t k = 0; k < j->K; ++k) {
 #if ORACLE_MUTANT == 3
         const double s = (double)srow[0]; /* mutant: first K block's scale everywhere */
@@ -167,8 +187,13 @@ static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_
 #else
         const uint64_t ai = (uint64_t)(k / 128) * j->M + m;
 #endif
+#if ORACLE_MUTANT == 16
+        const double a = j->Aq ? j->dec[j->Aq[(uint64_t)m * j->a_row_stride + k]] + 0.0 * (double)ai
+                               : oracle_bf16_to_double(arow[k]); /* mutant: activation scale ignored */
+#else
         const double a = j->Aq ? j->dec[j->Aq[(uint64_t)m * j->a_row_stride + k]] * (double)j->a_scale[ai]
                                : oracle_bf16_to_double(arow[k]);
+#endif
 #if ORACLE_MUTANT == 6
         if (k == j->K - 1)
             continue; /* mutant: last term dropped */
@@ -325,6 +350,10 @@ uint8_t oracle_e4m3_encode_rne(float x)
         return 0x7F;
     const uint8_t sign = signbit(x) ? 0x80 : 0x00;
     const double a = fabs((double)x);
+#if ORACLE_MUTANT == 12
+    if (a > 448.0)
+        return sign | 0x7F; /* mutant: out-of-range values become NaN instead of saturating */
+#endif
     if (a >= 448.0)
         return sign | 0x7E;
     int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) */
@@ -343,7 +372,11 @@ uint8_t oracle_e4m3_encode_rne(float x)
     else if (dhi < dlo)
         code = hi;
     else
+#if ORACLE_MUTANT == 11
+        code = hi; /* mutant: ties away from zero */
+#else
         code = (lo & 1) ? hi : lo; /* tie: even mantissa */
+#endif
     return sign | (uint8_t)code;
 }
 
@@ -406,7 +439,11 @@ int oracle_quantize_activations(const uint16_t *A, uint32_t a_row_stride, uint32
     for (uint32_t m = 0; m < M; ++m)
         for (uint32_t g = 0; g < K / 128; ++g) {
             float amax = 0.0f;
+#if ORACLE_MUTANT == 13
+            for (uint32_t k = 0; k < K; ++k) { /* mutant: one amax over the whole row */
+#else
             for (uint32_t k = g * 128; k < g * 128 + 128; ++k) {
+#endif
                 const float v = fabsf((float)oracle_bf16_to_double(A[(size_t)m * a_row_stride + k]));
                 if (v > amax)
                     amax = v;
