@@ -12,7 +12,10 @@ What pins what:
     torch's binary32 -> bfloat16 cast on binary32 inputs (a single rounding);
   * the GEMM: a hand-worked example (tests/golden/hand_worked_k256_n130.json),
     identity and all-ones closed forms, exact brute force with rational
-    arithmetic on tiny shapes, zero blocks, pad columns, linearity, NaN flow.
+    arithmetic on tiny shapes, zero blocks, pad columns, linearity, sums on exact
+    BF16 midpoints, NaN flow;
+  * the quantisers and W8A8: torch restatements, each block's or group's maximum
+    mapping to +-448, rational brute force, unit-code closed forms.
 """
 from __future__ import annotations
 
@@ -253,6 +256,25 @@ def pin_linearity(o):
     assert np.all(np.abs(e3 - e1) <= K * 2.0 ** -52 * ab)
 
 
+def pin_output_rounding_ties(o):
+    """Sums that land exactly on a midpoint between two BF16 neighbours round to the
+    one with an even last bit: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 (-> 1),
+    1 + 3*2^-8 halfway between 1 + 2^-7 and 1 + 2^-6 (-> 1 + 2^-6); the same with
+    the sign flipped. Closed forms of round-to-nearest-even on the GEMM's output."""
+    M, N, K = 4, 128, 128
+    A = np.zeros((M, K), dtype=np.float32)
+    A[0, :2] = [1.0, 2.0 ** -8]
+    A[1, :2] = [1.0, 3 * 2.0 ** -8]
+    A[2, :2] = [-1.0, -(2.0 ** -8)]
+    A[3, :2] = [-1.0, -3 * 2.0 ** -8]
+    W = np.full((N, K), 0x38, dtype=np.uint8)                 # every weight 1.0
+    C, _, _ = o.gemm(_codes(torch.from_numpy(A).to(torch.bfloat16)), W,
+                     np.ones((1, 1), np.float32), M, N, K)
+    want = [0x3F80, 0x3F82, 0xBF80, 0xBF82]                     # 1, 1 + 2^-6, -1, -(1 + 2^-6)
+    for m in range(M):
+        assert np.all(C[m] == want[m]), (m, hex(int(C[m, 0])))
+
+
 def pin_nan_propagation(o):
     gen = torch.Generator().manual_seed(19)
     M, N, K = 2, 128, 128
@@ -355,6 +377,28 @@ def pin_act_quantizer_vs_torch(o):
     assert scales[1, 2] == 0 and not codes[2, 128:256].any()
 
 
+def pin_act_quantizer_group_maximum(o):
+    """Each (token, 128-group) gets its own scale fl32(amax) / 448 and its largest
+    |a| encodes as +-448, while groups with a much smaller maximum keep their own
+    finer scale (a closed form of the per-group rule)."""
+    g = torch.Generator().manual_seed(44)
+    M, K = 3, 384
+    a = torch.randn(M, K, generator=g)
+    a[:, 128:256] *= 1e-3                                       # a quiet middle group
+    a[1, 300] = 50.0                                            # a loud entry in the last group
+    a = a.to(torch.bfloat16)
+    codes, scales = o.quantize_activations(_codes(a), M, K)
+    af = a.float()
+    for m in range(M):
+        for gi in range(K // 128):
+            grp = af[m, gi * 128:(gi + 1) * 128]
+            amax = float(grp.abs().max())
+            assert scales[gi, m] == np.float32(np.float32(amax) / np.float32(448.0)), (m, gi)
+            j = int(grp.abs().argmax())
+            assert codes[m, gi * 128 + j] & 0x7F == 0x7E, (m, gi)
+    assert np.all(scales[1] < 1e-2 * scales[0])                # the quiet group's own scale
+
+
 def pin_w8a8_reduces_to_w8a16(o):
     """With unit activation scales the W8A8 product is the W8A16 product of the
     activations' E4M3 values (exact in BF16), bit for bit."""
@@ -394,13 +438,32 @@ def pin_w8a8_brute_force_tiny(o):
             assert got[m, n] == _rne_bf16_exact(tot), (m, n)
 
 
+def pin_w8a8_scales_closed_form(o):
+    """With every code 1.0, the W8A8 output is sum over K groups of 128 * a_scale *
+    w_scale; powers of two keep every term and sum exact, so the value is known in
+    closed form and each activation scale must enter exactly once."""
+    g = torch.Generator().manual_seed(45)
+    M, N, K = 3, 256, 512
+    aq = np.full((M, K), 0x38, dtype=np.uint8)
+    wq = np.full((N, K), 0x38, dtype=np.uint8)
+    sa = (2.0 ** torch.randint(-4, 5, (K // 128, M), generator=g)).numpy().astype(np.float32)
+    sw = (2.0 ** torch.randint(-4, 5, (N // 128, K // 128), generator=g)).numpy().astype(np.float32)
+    _, exact, _ = o.w8a8_gemm(aq, sa, wq, sw, M, N, K, want_exact=True)
+    for m in range(M):
+        for n in (0, 127, 128, 255):
+            want = sum(128.0 * float(sa[kb, m]) * float(sw[n // 128, kb]) for kb in range(K // 128))
+            assert exact[m, n] == want, (m, n)
+
+
 PINS = [pin_e4m3_fixed_points, pin_e4m3_all_codes_vs_torch, pin_bf16_fixed_points,
         pin_bf16_vs_torch_on_binary32, pin_hand_worked_example, pin_identity_weights,
         pin_all_ones_closed_form, pin_brute_force_tiny, pin_zero_block,
-        pin_pads_untouched_and_ignored, pin_linearity, pin_nan_propagation,
+        pin_pads_untouched_and_ignored, pin_linearity, pin_output_rounding_ties,
+        pin_nan_propagation,
         pin_e4m3_encode_round_trip, pin_e4m3_encode_ties_vs_torch, pin_quantizer_vs_recipe,
         pin_quantizer_block_maximum,
-        pin_act_quantizer_vs_torch, pin_w8a8_reduces_to_w8a16, pin_w8a8_brute_force_tiny]
+        pin_act_quantizer_vs_torch, pin_act_quantizer_group_maximum, pin_w8a8_reduces_to_w8a16,
+        pin_w8a8_brute_force_tiny, pin_w8a8_scales_closed_form]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
