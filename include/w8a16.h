@@ -161,22 +161,24 @@ W8A16_API int w8a16_gemm_host(const void *A_host, uint32_t a_row_stride, const v
 /* ---- planning (pure host code; no device work) -------------------------- */
 
 typedef struct {
-    int32_t variant;       /* W8A16_VARIANT_SIMT or W8A16_VARIANT_TC */
-    uint32_t token_tile;   /* tokens (rows of A/C) per CTA: the MMA N of the TC variant */
+    int32_t variant;       /* one of W8A16_VARIANT_SIMT, _TC, _TC8, _W8A8, _PRESPLIT */
+    uint32_t token_tile;   /* tokens (rows of A/C) per CTA: the MMA N of the tensor-core
+                              variants */
     uint32_t split_k;      /* CTAs (one cluster) sharing a 128-row weight tile, each on a
                               contiguous range of 128-K steps; 1 = no split */
-    uint32_t stages;       /* depth of the shared-memory ring (TC) */
+    uint32_t stages;       /* depth of the shared-memory weight ring (tensor-core variants) */
     uint32_t ctas_per_sm;  /* residency the plan assumes */
     uint32_t grid[3];
     uint32_t block[3];
     uint32_t cluster[3];
     uint32_t smem_bytes;   /* dynamic shared memory per CTA */
-    uint32_t tmem_cols;    /* tensor-memory columns per CTA (TC) */
-    uint32_t tail_tiles;   /* FP8 x FP8 kernel (W8A8, PRESPLIT), one token tile: the last
-                              tail_tiles 128-row weight tiles run in a second launch, split
-                              over clusters of tail_split CTAs, so that a partial second
-                              wave of whole tiles becomes a short wave of split ones
-                              (grid[0] then counts the first launch's CTAs); 0 = none */
+    uint32_t tmem_cols;    /* tensor-memory columns per CTA (tensor-core variants) */
+    uint32_t tail_tiles;   /* TC, W8A8 and PRESPLIT plans with split_k 1 and one token
+                              tile: the last tail_tiles 128-row weight tiles run in a
+                              second launch, split over clusters of tail_split CTAs, so
+                              that a partial second wave of whole tiles becomes a short
+                              wave of split ones (grid[0] then counts the first launch's
+                              CTAs); 0 = none */
     uint32_t tail_split;   /* split-K of that second launch (>= 2 when tail_tiles > 0) */
 } w8a16_plan_t;
 
