@@ -9,7 +9,7 @@ the split pre-pass and the FP8 x FP8 kernel (two launches). Timing: W untimed wa
 bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on
 the launching stream. Steps rotate over B distinct input/output buffer sets
 totalling at least 3x the L2 size, so every step streams its weights from HBM.
-The K steps are replayed from CUDA graphs (one kernel per step).
+The K steps are replayed from CUDA graphs.
 
   value    = algorithmic bytes of all steps / timed seconds  (GB/s, whole job)
   e2e      = the same metric through the host-buffer entry point: per step the
@@ -24,15 +24,21 @@ activation quantiser followed by the FP8 x FP8 block-scaled GEMM (two launches);
 is the GEMM kernel alone (its own algorithmic bytes: FP8 activation codes and
 group scales instead of BF16 activations), timed from a graph of GEMM launches.
 
+--tokens M runs a workload at another token count, e.g. the multi-tile workload at
+M=256 (two 128-token tiles: one weight pass from HBM, the second token tile of each
+weight tile reading it from L2); the JSON line then names it multitile_m256_...
+
 --impl reference times the CPU oracle (the reference arm: there is no runnable
 reference implementation) on the same workload and metric.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -168,6 +174,17 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- our arm --
+def resolve_workload(args):
+    """The named workload, or with --tokens the same workload at another token
+    count M; its name then carries the new count (multitile_m128_... at 256
+    tokens is multitile_m256_...), and so do its traffic record and JSON line."""
+    wl = workloads.CONFIGS[args.workload]
+    if args.tokens is None or args.tokens == wl.M:
+        return args.workload, wl
+    name = re.sub(r"_m\d+_", f"_m{args.tokens}_", args.workload, count=1)
+    return name, dataclasses.replace(wl, name=name, M=args.tokens)
+
+
 def bench_gpu(args, ws, rank, local):
     import torch
     import fp8_weight_only_gemm_gb300 as w8
@@ -178,7 +195,7 @@ def bench_gpu(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
-    wl = workloads.CONFIGS[args.workload]
+    name, wl = resolve_workload(args)
     case = workloads.make_case(wl)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     set_bytes = wl.N * wl.K + case.A.numel() * 2 + case.C0.numel() * 2 + case.scale.numel() * 4
@@ -302,7 +319,7 @@ def bench_gpu(args, ws, rank, local):
     gbs = bytes_step * args.steps / sec / 1e9
     tflops = wl.flops() * args.steps / sec / 1e12
     hbm, bf16, bf16_sus, src = peaks()
-    traffic = recorded_traffic(args.workload + ("/w8a8" if w8a8 else "/presplit" if presplit else ""))
+    traffic = recorded_traffic(name + ("/w8a8" if w8a8 else "/presplit" if presplit else ""))
     kernel_gbs = kernel_bytes / kernel_us / 1e3
 
     # end to end through the host-buffer entry point
@@ -371,7 +388,7 @@ def bench_gpu(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8" if w8a8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K,
+        "config": {"workload": name, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K,
                    "a_row_stride": wl.lda, "c_row_stride": wl.ldc, "seed": wl.seed,
                    "l2": f"inputs rotate over {nsets} buffer sets ({nsets * set_bytes / 1e6:.0f} MB, "
                          f">= 3x the {l2 / 1e6:.0f} MB L2): weights stream from HBM every step",
@@ -433,7 +450,7 @@ def oracle_rate(wl, seconds: float, threads: int | None = None, path: str = "w8a
 
 
 def bench_reference(args):
-    wl = workloads.CONFIGS[args.workload]
+    name, wl = resolve_workload(args)
     threads = os.cpu_count() or 1
     step = oracle_step(wl, args.path, threads)
 
@@ -448,9 +465,9 @@ def bench_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": args.workload, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K},
+            "config": {"workload": name, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{args.steps} full calls of {args.workload} on the CPU oracle "
+                             "sample": f"{args.steps} full calls of {name} on the CPU oracle "
                                        f"({'quantiser + W8A8 product, ' if args.path == 'w8a8' else ''}"
                                        "FP64, plain k-order loops)"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -465,6 +482,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="run the workload at this token count M instead of its own")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path", choices=["w8a16", "w8a8"], default="w8a16",
                     help="w8a8: activation quantiser + W8A8 GEMM per step")
@@ -473,6 +492,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="bounded CPU-oracle sample for cpu_baseline")
     args = ap.parse_args()
+    if args.tokens is not None and not 1 <= args.tokens <= 4096:
+        ap.error("--tokens must be in 1..4096")
     ws, rank, local = dist_env()
     if args.impl == "reference":
         if args.steps is None:
@@ -495,10 +516,10 @@ def main():
     line = bench_gpu(args, ws, rank, local)
     if rank == 0:
         if args.cpu_seconds > 0:
-            v, dt, reps, thr = oracle_rate(workloads.CONFIGS[args.workload], args.cpu_seconds,
-                                           path=args.path)
+            name, wl = resolve_workload(args)
+            v, dt, reps, thr = oracle_rate(wl, args.cpu_seconds, path=args.path)
             line["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle",
-                                    "sample": f"{reps} full calls of {args.workload} "
+                                    "sample": f"{reps} full calls of {name} "
                                               f"{'(quantiser + W8A8 product) ' if args.path == 'w8a8' else ''}"
                                               f"({dt * 1e3:.1f} ms each) on the CPU oracle"}
         print(json.dumps(line), flush=True)
