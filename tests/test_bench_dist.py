@@ -65,3 +65,26 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["config"]["workload"] == "tiny_m1_n256_k256"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
+
+
+def test_tokens_override_names_the_workload():
+    sys.path.insert(0, str(ROOT))
+    import argparse
+    import bench
+    name, wl = bench.resolve_workload(argparse.Namespace(workload="multitile_m128_n28672_k8192", tokens=256))
+    assert name == "multitile_m256_n28672_k8192" and wl.M == 256 and (wl.N, wl.K) == (28672, 8192)
+    assert wl.outlier_frac == 0.01 and wl.seed == 4                 # the rest of the recipe is kept
+    name, wl = bench.resolve_workload(argparse.Namespace(workload="decode_gemv_m1_n4096_k4096", tokens=None))
+    assert name == "decode_gemv_m1_n4096_k4096" and wl.M == 1
+
+
+def test_reference_arm_with_tokens():
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
+           "--workload", "tiny_m1_n256_k256", "--tokens", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][0])
+    assert d["config"]["workload"] == "tiny_m3_n256_k256" and d["config"]["M"] == 3
+    bad = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--tokens", "0"], cwd=ROOT,
+                         capture_output=True, text=True, timeout=300)
+    assert bad.returncode != 0 and "--tokens" in bad.stderr
