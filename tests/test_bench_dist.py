@@ -1,6 +1,8 @@
 """The multi-process parts of bench.py on CPU with the gloo backend (world size 2):
 the job time is the slowest rank's, and under torchrun the reference arm prints one
-JSON line from rank 0 while the other rank exits without work."""
+JSON line from rank 0 while the other rank exits without work. Also the host side of
+--tokens (a workload at another token count keeps its recipe and carries the new
+count in its name)."""
 from __future__ import annotations
 
 import json
