@@ -164,6 +164,34 @@ def plan_variant(M, N, K, variant=VARIANT_TC, split_k=0, stages=0, sm_count=152)
 
 
 # ----------------------------------------------------------- device calls --
+# The library sees plain pointers and cannot tell host memory, another device's
+# memory or a short buffer from a good one; a kernel handed any of them would
+# fault. So every tensor entry point checks placement, dtypes and extents here,
+# before it calls the library.
+_CODE_DTYPES = ("uint8", "float8_e4m3fn")
+
+
+def _on_one_gpu(*tensors):
+    dev = tensors[0].device
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be on a CUDA device")
+        if t.device != dev:
+            raise ValueError(f"all tensors must be on one device (got {dev} and {t.device})")
+
+
+def _scale_shape(scale, N, K, name="block_scale"):
+    """Block scales cover the [N, K] weights: [ceil(N/128), K/128]. Checked when K
+    is a multiple of 128; otherwise the library reports K itself."""
+    want = ((N + 127) // 128, K // 128)
+    if K % 128 == 0 and tuple(scale.shape) != want:
+        raise ValueError(f"{name} must be {list(want)} for N={N}, K={K}; got {list(scale.shape)}")
+
+
+def _is_codes(t) -> bool:
+    return str(t.dtype).rsplit(".", 1)[-1] in _CODE_DTYPES
+
+
 def _shapes(A, W, scale, C):
     import torch
     if A.dim() != 2 or W.dim() != 2:
@@ -182,6 +210,7 @@ def _shapes(A, W, scale, C):
     N, Kw = W.shape
     if Kw != K:
         raise ValueError(f"A has K={K} columns, W has {Kw}")
+    _scale_shape(scale, N, K)
     return M, N, K
 
 
@@ -195,8 +224,7 @@ def gemm(A, W, scale, C=None, *, stream=None, plan: Plan | None = None, flags: i
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N:
         raise ValueError("C must be bfloat16 [M, >=N]")
-    if not (A.is_cuda and W.is_cuda and scale.is_cuda and C.is_cuda):
-        raise ValueError("all tensors must be on a CUDA device")
+    _on_one_gpu(A, W, scale, C)
     lib = load()
     args = (A.data_ptr(), A.stride(0), W.data_ptr(), scale.data_ptr(), C.data_ptr(), C.stride(0),
             M, N, K)
@@ -226,8 +254,11 @@ def gemm_ws(A, W, scale, C=None, *, workspace=None, stream=None, plan: Plan | No
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N:
         raise ValueError("C must be bfloat16 [M, >=N]")
-    if not (A.is_cuda and W.is_cuda and scale.is_cuda and C.is_cuda):
-        raise ValueError("all tensors must be on a CUDA device")
+    _on_one_gpu(A, W, scale, C)
+    if workspace is not None and workspace is not False:
+        if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 tensor")
+        _on_one_gpu(A, workspace)
     lib = load()
     if workspace is None:
         workspace = torch.empty(max(16, workspace_bytes(M, K)), dtype=torch.uint8, device=A.device)
@@ -249,8 +280,7 @@ def gemm_noalloc(A, W, scale, C=None, *, stream=None, flags: int = 0):
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N:
         raise ValueError("C must be bfloat16 [M, >=N]")
-    if not (A.is_cuda and W.is_cuda and scale.is_cuda and C.is_cuda):
-        raise ValueError("all tensors must be on a CUDA device")
+    _on_one_gpu(A, W, scale, C)
     with torch.cuda.device(A.device):
         rc = load().w8a16_gemm_noalloc(A.data_ptr(), A.stride(0), W.data_ptr(), scale.data_ptr(),
                                        C.data_ptr(), C.stride(0), M, N, K, flags, _stream_handle(stream))
@@ -291,9 +321,23 @@ def gemm_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K
 def gemm_host(A_host, W_host, scale_host, C_host, dA, dW, dScale, dC, *, copy_weights=True,
               stream=None):
     """Host-buffer call: the library queues H2D copies, the GEMM and the D2H copy.
-    Host tensors should be pinned; device tensors have the same shapes/pitches."""
+    Host tensors should be pinned; the device buffers take A and C at the host
+    tensors' row pitches (dA, dC), W as [N, K] and the scales at their shape."""
     import torch
     M, N, K = _shapes(A_host, W_host, scale_host, C_host)
+    if C_host.dtype != torch.bfloat16 or C_host.shape[0] != M or C_host.shape[1] < N:
+        raise ValueError("C_host must be bfloat16 [M, >=N]")
+    if any(t.is_cuda for t in (A_host, W_host, scale_host, C_host)):
+        raise ValueError("A_host, W_host, scale_host and C_host must be in host memory")
+    _on_one_gpu(dA, dW, dScale, dC)
+    for name, d, h, rows, cols in (("dA", dA, A_host, M, K), ("dC", dC, C_host, M, N)):
+        if (d.dtype != torch.bfloat16 or d.dim() != 2 or d.stride(1) != 1 or d.stride(0) != h.stride(0)
+                or d.shape[0] < rows or d.shape[1] < cols):
+            raise ValueError(f"{name} must be bfloat16 with at least [{rows}, {cols}] at row pitch {h.stride(0)}")
+    if not _is_codes(dW) or not dW.is_contiguous() or tuple(dW.shape) != (N, K):
+        raise ValueError(f"dW must be contiguous E4M3 codes [{N}, {K}]")
+    if dScale.dtype != torch.float32 or not dScale.is_contiguous() or dScale.shape != scale_host.shape:
+        raise ValueError(f"dScale must be contiguous float32 {list(scale_host.shape)}")
     with torch.cuda.device(dA.device):
         rc = load().w8a16_gemm_host(
             A_host.data_ptr(), A_host.stride(0), W_host.data_ptr(), scale_host.data_ptr(),
@@ -353,10 +397,23 @@ def gemm_w8a8(A_codes, a_scale, W, scale, C=None, *, stream=None, plan: Plan | N
     [K/128, >=M] (row pitch a multiple of 4); W: uint8 [N, K]; scale: float32
     [ceil(N/128), K/128]; C: optional bf16 [M, >=N]."""
     import torch
+    if A_codes.dim() != 2 or not _is_codes(A_codes) or A_codes.stride(1) != 1:
+        raise ValueError("A_codes must be 2-D E4M3 codes (uint8 or float8_e4m3fn) with contiguous rows")
     M, K = A_codes.shape
+    if (a_scale.dim() != 2 or a_scale.dtype != torch.float32 or a_scale.stride(1) != 1
+            or a_scale.shape[0] < K // 128 or a_scale.shape[1] < M):
+        raise ValueError(f"a_scale must be float32 with at least [{K // 128}, {M}] and contiguous rows")
+    if W.dim() != 2 or not _is_codes(W) or not W.is_contiguous() or W.shape[1] != K:
+        raise ValueError(f"W must be contiguous E4M3 codes [N, {K}]")
     N = W.shape[0]
+    if scale.dtype != torch.float32 or not scale.is_contiguous():
+        raise ValueError("block_scale must be contiguous float32")
+    _scale_shape(scale, N, K)
     if C is None:
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A_codes.device)
+    if C.dtype != torch.bfloat16 or C.dim() != 2 or C.stride(1) != 1 or C.shape[0] != M or C.shape[1] < N:
+        raise ValueError("C must be bfloat16 [M, >=N] with contiguous rows")
+    _on_one_gpu(A_codes, a_scale, W, scale, C)
     args = (A_codes.data_ptr(), A_codes.stride(0), a_scale.data_ptr(), a_scale.stride(0), W.data_ptr(),
             scale.data_ptr(), C.data_ptr(), C.stride(0), M, N, K)
     with torch.cuda.device(A_codes.device):

@@ -332,3 +332,61 @@ def test_activation_quantiser_checks(lib, args, code, needle):
     lda, M, K, sst = args
     rc = binding.load().w8a16_quantize_activations(0x1000, lda, M, K, 0x2000, 0x3000, sst, None)
     assert rc == code and needle in binding.last_error(), (rc, binding.last_error())
+
+
+# ---- the binding's own checks: placement, dtypes and extents, before any call ----
+
+def _cpu_operands(M=4, N=200, K=256):
+    import torch
+    A = torch.zeros((M, K), dtype=torch.bfloat16)
+    W = torch.zeros((N, K), dtype=torch.uint8)
+    S = torch.ones(((N + 127) // 128, K // 128), dtype=torch.float32)
+    C = torch.zeros((M, N), dtype=torch.bfloat16)
+    return A, W, S, C
+
+
+def test_binding_refuses_host_tensors_for_device_calls(lib):
+    A, W, S, C = _cpu_operands()
+    for call in (lambda: binding.gemm(A, W, S, C), lambda: binding.gemm_ws(A, W, S, C, workspace=False),
+                 lambda: binding.gemm_noalloc(A, W, S, C)):
+        with pytest.raises(ValueError, match="CUDA device"):
+            call()
+
+
+def test_binding_checks_block_scale_extent(lib):
+    import torch
+    A, W, S, C = _cpu_operands(N=200, K=256)
+    for bad in (torch.ones((1, 2)), torch.ones((2, 1)), torch.ones((2, 3))):
+        with pytest.raises(ValueError, match=r"block_scale must be \[2, 2\]"):
+            binding.gemm(A, W, bad, C)
+
+
+def test_binding_checks_w8a8_operands(lib):
+    import torch
+    M, N, K = 4, 200, 256
+    q = torch.zeros((M, K), dtype=torch.uint8)
+    qs = torch.ones((K // 128, 4), dtype=torch.float32)
+    W = torch.zeros((N, K), dtype=torch.uint8)
+    S = torch.ones((2, 2), dtype=torch.float32)
+    C = torch.zeros((M, N), dtype=torch.bfloat16)
+    cases = [
+        ((q.to(torch.bfloat16), qs, W, S, C), "A_codes"),
+        ((q, torch.ones((1, 4)), W, S, C), "a_scale"),
+        ((q, torch.ones((2, 3)), W, S, C), "a_scale"),
+        ((q, qs, W[:, :128].contiguous(), S, C), "W must"),
+        ((q, qs, W, torch.ones((2, 1)), C), "block_scale must be"),
+        ((q, qs, W, S, C.float()), "C must"),
+        ((q, qs, W, S, C), "CUDA device"),
+    ]
+    for args, needle in cases:
+        with pytest.raises(ValueError, match=needle):
+            binding.gemm_w8a8(*args)
+
+
+def test_binding_checks_host_call_buffers(lib):
+    import torch
+    A, W, S, C = _cpu_operands()
+    with pytest.raises(ValueError, match="C_host"):
+        binding.gemm_host(A, W, S, C.float(), A, W, S, C)
+    with pytest.raises(ValueError, match="CUDA device"):
+        binding.gemm_host(A, W, S, C, A, W, S, C)
