@@ -390,3 +390,13 @@ def test_binding_checks_host_call_buffers(lib):
         binding.gemm_host(A, W, S, C.float(), A, W, S, C)
     with pytest.raises(ValueError, match="CUDA device"):
         binding.gemm_host(A, W, S, C, A, W, S, C)
+
+
+def test_binding_quantisers_refuse_host_tensors(lib):
+    import torch
+    with pytest.raises(ValueError, match="CUDA device"):
+        binding.quantize_weights(torch.zeros((128, 256), dtype=torch.float32))
+    with pytest.raises(TypeError, match="float32 or bfloat16"):
+        binding.quantize_weights(torch.zeros((128, 256), dtype=torch.float16))
+    with pytest.raises(ValueError, match="CUDA bfloat16"):
+        binding.quantize_activations(torch.zeros((4, 256), dtype=torch.bfloat16))
