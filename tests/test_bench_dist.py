@@ -90,3 +90,13 @@ def test_reference_arm_with_tokens():
     bad = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--tokens", "0"], cwd=ROOT,
                          capture_output=True, text=True, timeout=300)
     assert bad.returncode != 0 and "--tokens" in bad.stderr
+
+
+def test_cpu_baseline_all_cores_and_one():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    import workloads
+    d = bench.cpu_baseline(workloads.CONFIGS["tiny_m1_n256_k256"], "tiny_m1_n256_k256", "w8a16", 0.3)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1
+    if d["cores"] > 1:
+        assert d["single_core"]["cores"] == 1 and d["single_core"]["value"] > 0
