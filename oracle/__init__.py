@@ -37,41 +37,50 @@ _BUILD = _HERE / "_build"
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
-_u32p = ctypes.POINTER(ctypes.c_uint32)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 
 
-def _src_tag(mutant: int) -> str:
-    h = hashlib.sha1(_SRC.read_bytes()).hexdigest()[:12]
-    return f"{h}_{platform.machine()}_m{mutant}"
+def _src_tag(source: bytes) -> str:
+    h = hashlib.sha1(source).hexdigest()[:12]
+    return f"{h}_{platform.machine()}"
 
 
-def build(mutant: int = 0, outdir: Path | None = None) -> Path:
-    """Compile the oracle with gcc (no fast-math, no FP contraction).
+def build(outdir: Path | None = None, source: str | None = None) -> Path:
+    """Compile the oracle with gcc (no fast-math, no FP contraction) and return
+    the path of the shared library.
 
-    ``mutant`` > 0 builds a copy with one planted mistake; only the mutation
-    tests ask for that. Returns the path of the shared library.
+    ``source`` replaces the text of w8a16_oracle.c; only the mutation tests pass
+    one (a copy with one planted mistake, compiled into their own directory).
     """
     outdir = Path(outdir) if outdir is not None else _BUILD
     outdir.mkdir(parents=True, exist_ok=True)
-    lib = outdir / f"liboracle_w8a16_{_src_tag(mutant)}.so"
+    text = _SRC.read_bytes() if source is None else source.encode()
+    lib = outdir / f"liboracle_w8a16_{_src_tag(text)}.so"
     if lib.exists():
         return lib
+    src = _SRC
+    if source is not None:
+        src = outdir / f"w8a16_oracle_{_src_tag(text)}.c"
+        src.write_bytes(text)
     tmp = lib.with_suffix(f".tmp{os.getpid()}.so")
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-pthread", f"-DORACLE_MUTANT={int(mutant)}",
-           str(_SRC), "-o", str(tmp), "-lm"]
+           "-fno-fast-math", "-pthread", str(src), "-o", str(tmp), "-lm"]
     subprocess.run(cmd, check=True, capture_output=True)
     os.replace(tmp, lib)
     return lib
 
 
+def source_text() -> str:
+    """The oracle's C source."""
+    return _SRC.read_text()
+
+
 class Oracle:
     """One loaded build of the oracle."""
 
-    def __init__(self, mutant: int = 0, outdir: Path | None = None):
-        self.path = build(mutant, outdir)
+    def __init__(self, outdir: Path | None = None, source: str | None = None):
+        self.path = build(outdir, source)
         lib = ctypes.CDLL(str(self.path))
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = ctypes.c_double
@@ -83,10 +92,6 @@ class Oracle:
             _u16p, ctypes.c_uint32, _u8p, _f32p, _u16p, ctypes.c_uint32,
             ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, _f64p, _f64p, ctypes.c_int]
         lib.oracle_w8a16_gemm.restype = ctypes.c_int
-        lib.oracle_w8a16_gemm_samples.argtypes = [
-            _u16p, ctypes.c_uint32, _u8p, _f32p, ctypes.c_uint32, ctypes.c_uint32,
-            ctypes.c_uint32, _u32p, _u32p, ctypes.c_uint64, _u16p, _f64p, _f64p, ctypes.c_int]
-        lib.oracle_w8a16_gemm_samples.restype = ctypes.c_int
         lib.oracle_e4m3_encode_rne.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_encode_rne.restype = ctypes.c_uint8
         lib.oracle_quantize_weights.argtypes = [_f32p, ctypes.c_uint32, ctypes.c_uint32,
@@ -218,28 +223,6 @@ class Oracle:
                 exact.reshape(M, N) if exact is not None else None,
                 absum.reshape(M, N) if absum is not None else None)
 
-    def gemm_samples(self, A, W, scale, M, N, K, ms, ns, a_row_stride=None, threads=None):
-        """BF16 codes, exact sums and |term| sums of C at the listed (m, n)."""
-        a_row_stride = K if a_row_stride is None else int(a_row_stride)
-        A = np.ascontiguousarray(A, dtype=np.uint16).reshape(-1)
-        W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
-        scale = np.ascontiguousarray(scale, dtype=np.float32).reshape(-1)
-        ms = np.ascontiguousarray(ms, dtype=np.uint32)
-        ns = np.ascontiguousarray(ns, dtype=np.uint32)
-        cnt = ms.size
-        out = np.zeros(cnt, dtype=np.uint16)
-        exact = np.zeros(cnt, dtype=np.float64)
-        absum = np.zeros(cnt, dtype=np.float64)
-        rc = self.lib.oracle_w8a16_gemm_samples(
-            A.ctypes.data_as(_u16p), a_row_stride, W.ctypes.data_as(_u8p),
-            scale.ctypes.data_as(_f32p), M, N, K, ms.ctypes.data_as(_u32p),
-            ns.ctypes.data_as(_u32p), cnt, out.ctypes.data_as(_u16p),
-            exact.ctypes.data_as(_f64p), absum.ctypes.data_as(_f64p),
-            int(threads or os.cpu_count() or 1))
-        if rc != 0:
-            raise ValueError("oracle rejected the sample request")
-        return out, exact, absum
-
 
 _DEFAULT: Oracle | None = None
 
@@ -248,5 +231,5 @@ def get() -> Oracle:
     """The unmutated oracle, built on first use."""
     global _DEFAULT
     if _DEFAULT is None:
-        _DEFAULT = Oracle(0)
+        _DEFAULT = Oracle()
     return _DEFAULT

@@ -42,10 +42,6 @@
 #include <stdlib.h>
 #include <string.h>
 
-#ifndef ORACLE_MUTANT
-#define ORACLE_MUTANT 0 /* >0 only in the mutation tests, which plant one known mistake */
-#endif
-
 /* ---- E4M3 (FN) decode, from the format definition ------------------------
  * 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits. Exponent field 0 is
  * subnormal: (m/8) * 2^(1-7). Exponent 15 with mantissa 7 is NaN; there is no
@@ -59,23 +55,10 @@ double oracle_e4m3_to_double(uint8_t code)
     if (e == 0xF && m == 0x7)
         return NAN;
     if (e == 0)
-#if ORACLE_MUTANT == 9
-        mag = ldexp(8.0 + m, -10); /* mutant: subnormals given the implicit leading one */
-#else
         mag = ldexp((double)m, -9); /* m/8 * 2^-6 */
-#endif
     else
-#if ORACLE_MUTANT == 1
-        mag = ldexp(8.0 + m, e - 7 - 2); /* mutant: exponent bias off by one */
-#else
         mag = ldexp(8.0 + m, e - 7 - 3); /* (1 + m/8) * 2^(e-7) */
-#endif
-#if ORACLE_MUTANT == 14
-    (void)sign;
-    return mag; /* mutant: sign bit dropped */
-#else
     return sign ? -mag : mag;
-#endif
 }
 
 /* ---- BF16 <-> FP64 -------------------------------------------------------
@@ -110,13 +93,7 @@ uint16_t oracle_double_to_bf16_rne(double x)
         int q = (e - 1) - 7; /* weight of the last of 8 significant bits */
         if (q < -133)
             q = -133; /* subnormal range: fixed quantum */
-#if ORACLE_MUTANT == 2
-        const double r = floor(ldexp(a, -q)); /* mutant: truncation instead of RNE */
-#elif ORACLE_MUTANT == 15
-        const double r = round(ldexp(a, -q)); /* mutant: ties away from zero */
-#else
         const double r = nearbyint(ldexp(a, -q)); /* default mode: ties to even */
-#endif
         const double v = ldexp(r, q);
         if (v >= 0x1p128) {
             mag = 0x7F80;
@@ -132,72 +109,43 @@ uint16_t oracle_double_to_bf16_rne(double x)
 
 /* ---- the GEMM -------------------------------------------------------------- */
 
-typedef struct {
-    const uint16_t *A;
+typedef struct oracle_job oracle_job;
+
+/* The sum of one output element: *sum_out = sum_k of its terms (FP64, k order),
+ * *abs_out = sum_k of their magnitudes (an input of the tests' error bound). */
+typedef void (*oracle_output_fn)(const oracle_job *j, uint32_t m, uint32_t n, double *sum_out,
+                                 double *abs_out);
+
+struct oracle_job {
+    const uint16_t *A;    /* W8A16: BF16 activation codes [M][a_row_stride] */
+    const uint8_t *Aq;    /* W8A8: E4M3 activation codes [M][a_row_stride] */
+    const float *a_scale; /* W8A8: activation group scales [K/128][M] */
     uint32_t a_row_stride;
     const uint8_t *W;
     const float *scale;
     uint16_t *C;
     uint32_t c_row_stride;
     uint32_t M, N, K;
-    double *exact; /* optional [M*N] pre-rounding sums */
-    double *absum; /* optional [M*N] sums of |terms| (error-bound input) */
-    const uint32_t *sm, *sn; /* sampled mode: output indices */
-    uint16_t *sout;          /* sampled mode: [count] BF16 results */
-    uint64_t begin, end;     /* this thread's share */
-    const double *dec;       /* 256-entry E4M3 table */
-    const uint8_t *Aq;       /* W8A8: E4M3 activation codes [M][a_row_stride] (A unused) */
-    const float *a_scale;    /* W8A8: activation group scales [K/128][M] */
-} oracle_job;
+    double *exact;        /* optional [M*N] pre-rounding sums */
+    double *absum;        /* optional [M*N] sums of |terms| */
+    uint64_t begin, end;  /* this thread's share of the M*N outputs */
+    const double *dec;    /* 256-entry E4M3 table */
+    oracle_output_fn output;
+};
 
-/* One output element, exactly as the definition reads. */
-static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_out,
-                       double *abs_out)
+/* One W8A16 output element, exactly as the definition reads:
+ * sum_k A[m][k] * (e4m3(W[n][k]) * scale[n/128][k/128]). */
+static void w8a16_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_out,
+                         double *abs_out)
 {
-    const uint32_t kb_count = j->K / 128;
-#if ORACLE_MUTANT == 10
-    const uint16_t *arow = j->A ? j->A + (uint64_t)m * j->K : NULL; /* mutant: pitch ignored */
-#else
-    const uint16_t *arow = j->A ? j->A + (uint64_t)m * j->a_row_stride : NULL;
-#endif
+    const uint16_t *arow = j->A + (uint64_t)m * j->a_row_stride;
     const uint8_t *wrow = j->W + (uint64_t)n * j->K;
-    const float *srow = j->scale + (uint64_t)(n / 128) * kb_count;
-#if ORACLE_MUTANT == 17
-    float sum = 0.0f; /* mutant: the sum carried in FP32 */
-    double asum = 0.0;
-#else
+    const float *srow = j->scale + (uint64_t)(n / 128) * (j->K / 128);
     double sum = 0.0, asum = 0.0;
-#endif
     for (uint32_t k = 0; k < j->K; ++k) {
-#if ORACLE_MUTANT == 3
-        const double s = (double)srow[0]; /* mutant: first K block's scale everywhere */
-#elif ORACLE_MUTANT == 4
-        const double s = (double)j->scale[(uint64_t)(k / 128) * ((j->N + 127) / 128) + n / 128];
-        /* mutant: scale grid read transposed */
-#else
-        const double s = (double)srow[k / 128];
-#endif
-#if ORACLE_MUTANT == 5
-        const double w = j->dec[j->W[(uint64_t)k * j->N + n]]; /* mutant: W read as [K][N] */
-#else
+        const double a = oracle_bf16_to_double(arow[k]);
         const double w = j->dec[wrow[k]];
-#endif
-#if ORACLE_MUTANT == 8
-        const uint64_t ai = (uint64_t)m * (j->K / 128) + k / 128; /* mutant: token-major scales */
-#else
-        const uint64_t ai = (uint64_t)(k / 128) * j->M + m;
-#endif
-#if ORACLE_MUTANT == 16
-        const double a = j->Aq ? j->dec[j->Aq[(uint64_t)m * j->a_row_stride + k]] + 0.0 * (double)ai
-                               : oracle_bf16_to_double(arow[k]); /* mutant: activation scale ignored */
-#else
-        const double a = j->Aq ? j->dec[j->Aq[(uint64_t)m * j->a_row_stride + k]] * (double)j->a_scale[ai]
-                               : oracle_bf16_to_double(arow[k]);
-#endif
-#if ORACLE_MUTANT == 6
-        if (k == j->K - 1)
-            continue; /* mutant: last term dropped */
-#endif
+        const double s = (double)srow[k / 128];
         const double t = a * (w * s);
         sum += t;
         asum += fabs(t);
@@ -206,7 +154,28 @@ static void one_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_
     *abs_out = asum;
 }
 
-static void *run_full(void *arg)
+/* One W8A8 output element: sum_k (e4m3(Aq[m][k]) * a_scale[k/128][m]) *
+ * (e4m3(W[n][k]) * scale[n/128][k/128]). */
+static void w8a8_output(const oracle_job *j, uint32_t m, uint32_t n, double *sum_out,
+                        double *abs_out)
+{
+    const uint8_t *arow = j->Aq + (uint64_t)m * j->a_row_stride;
+    const uint8_t *wrow = j->W + (uint64_t)n * j->K;
+    const float *srow = j->scale + (uint64_t)(n / 128) * (j->K / 128);
+    double sum = 0.0, asum = 0.0;
+    for (uint32_t k = 0; k < j->K; ++k) {
+        const double a = j->dec[arow[k]] * (double)j->a_scale[(uint64_t)(k / 128) * j->M + m];
+        const double w = j->dec[wrow[k]];
+        const double s = (double)srow[k / 128];
+        const double t = a * (w * s);
+        sum += t;
+        asum += fabs(t);
+    }
+    *sum_out = sum;
+    *abs_out = asum;
+}
+
+static void *run_share(void *arg)
 {
     const oracle_job *j = (const oracle_job *)arg;
     for (uint64_t idx = j->begin; idx < j->end; ++idx) {
@@ -214,7 +183,7 @@ static void *run_full(void *arg)
         const uint32_t n = (uint32_t)(idx / j->M);
         const uint32_t m = (uint32_t)(idx % j->M);
         double sum, asum;
-        one_output(j, m, n, &sum, &asum);
+        j->output(j, m, n, &sum, &asum);
         j->C[(uint64_t)m * j->c_row_stride + n] = oracle_double_to_bf16_rne(sum);
         if (j->exact)
             j->exact[(uint64_t)m * j->N + n] = sum;
@@ -224,23 +193,11 @@ static void *run_full(void *arg)
     return NULL;
 }
 
-static void *run_samples(void *arg)
+/* All M*N outputs, split evenly over nthreads POSIX threads (each output is
+ * computed by one thread, so the thread count never changes a result). */
+static int run_threads(oracle_job *base, int nthreads)
 {
-    const oracle_job *j = (const oracle_job *)arg;
-    for (uint64_t i = j->begin; i < j->end; ++i) {
-        double sum, asum;
-        one_output(j, j->sm[i], j->sn[i], &sum, &asum);
-        j->sout[i] = oracle_double_to_bf16_rne(sum);
-        if (j->exact)
-            j->exact[i] = sum;
-        if (j->absum)
-            j->absum[i] = asum;
-    }
-    return NULL;
-}
-
-static int run_threads(oracle_job *base, uint64_t total, int nthreads, void *(*fn)(void *))
-{
+    const uint64_t total = (uint64_t)base->M * base->N;
     double dec[256];
     for (int c = 0; c < 256; ++c)
         dec[c] = oracle_e4m3_to_double((uint8_t)c);
@@ -251,9 +208,11 @@ static int run_threads(oracle_job *base, uint64_t total, int nthreads, void *(*f
         nthreads = total ? (int)total : 1;
     oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
     pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
-    if (!jobs || !tids) {
+    char *joined = (char *)calloc((size_t)nthreads, 1);
+    if (!jobs || !tids || !joined) {
         free(jobs);
         free(tids);
+        free(joined);
         return -1;
     }
     for (int t = 0; t < nthreads; ++t) {
@@ -261,19 +220,13 @@ static int run_threads(oracle_job *base, uint64_t total, int nthreads, void *(*f
         jobs[t].begin = total * (uint64_t)t / (uint64_t)nthreads;
         jobs[t].end = total * (uint64_t)(t + 1) / (uint64_t)nthreads;
     }
-    char *joined = (char *)calloc((size_t)nthreads, 1);
-    if (!joined) {
-        free(jobs);
-        free(tids);
-        return -1;
-    }
     for (int t = 1; t < nthreads; ++t) {
-        if (pthread_create(&tids[t], NULL, fn, &jobs[t]) == 0)
+        if (pthread_create(&tids[t], NULL, run_share, &jobs[t]) == 0)
             joined[t] = 1;
         else
-            fn(&jobs[t]); /* no thread available: run the share inline */
+            run_share(&jobs[t]); /* no thread available: run the share inline */
     }
-    fn(&jobs[0]);
+    run_share(&jobs[0]);
     for (int t = 1; t < nthreads; ++t)
         if (joined[t])
             pthread_join(tids[t], NULL);
@@ -306,36 +259,8 @@ int oracle_w8a16_gemm(const uint16_t *A, uint32_t a_row_stride, const uint8_t *W
     j.K = K;
     j.exact = exact;
     j.absum = absum;
-    return run_threads(&j, (uint64_t)M * N, nthreads, run_full);
-}
-
-/* Sampled product: out[i] = C[sm[i]][sn[i]] for i < count, with the same
- * definition; exact/absum (optional) are [count]. */
-int oracle_w8a16_gemm_samples(const uint16_t *A, uint32_t a_row_stride, const uint8_t *W,
-                              const float *scale, uint32_t M, uint32_t N, uint32_t K,
-                              const uint32_t *sm, const uint32_t *sn, uint64_t count,
-                              uint16_t *out, double *exact, double *absum, int nthreads)
-{
-    if (M == 0 || N == 0 || K == 0 || K % 128 != 0 || a_row_stride < K)
-        return -1;
-    for (uint64_t i = 0; i < count; ++i)
-        if (sm[i] >= M || sn[i] >= N)
-            return -1;
-    oracle_job j;
-    memset(&j, 0, sizeof j);
-    j.A = A;
-    j.a_row_stride = a_row_stride;
-    j.W = W;
-    j.scale = scale;
-    j.M = M;
-    j.N = N;
-    j.K = K;
-    j.sm = sm;
-    j.sn = sn;
-    j.sout = out;
-    j.exact = exact;
-    j.absum = absum;
-    return run_threads(&j, count, nthreads, run_samples);
+    j.output = w8a16_output;
+    return run_threads(&j, nthreads);
 }
 
 /* ---- E4M3 (FN) encode, round to nearest, ties to even, saturating ----------
@@ -350,10 +275,6 @@ uint8_t oracle_e4m3_encode_rne(float x)
         return 0x7F;
     const uint8_t sign = signbit(x) ? 0x80 : 0x00;
     const double a = fabs((double)x);
-#if ORACLE_MUTANT == 12
-    if (a > 448.0)
-        return sign | 0x7F; /* mutant: out-of-range values become NaN instead of saturating */
-#endif
     if (a >= 448.0)
         return sign | 0x7E;
     int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) */
@@ -372,11 +293,7 @@ uint8_t oracle_e4m3_encode_rne(float x)
     else if (dhi < dlo)
         code = hi;
     else
-#if ORACLE_MUTANT == 11
-        code = hi; /* mutant: ties away from zero */
-#else
         code = (lo & 1) ? hi : lo; /* tie: even mantissa */
-#endif
     return sign | (uint8_t)code;
 }
 
@@ -399,11 +316,7 @@ int oracle_quantize_weights(const float *W, uint32_t w_row_stride, uint32_t N, u
                     if (v > amax)
                         amax = v;
                 }
-#if ORACLE_MUTANT == 7
-            const float scale = amax / 447.0f; /* mutant: wrong range */
-#else
             const float scale = amax / 448.0f;
-#endif
             scales[(size_t)nb * kb_cols + kb] = scale;
             for (uint32_t r = nb * 128; r < r1; ++r)
                 for (uint32_t k = kb * 128; k < kb * 128 + 128; ++k) {
@@ -439,11 +352,7 @@ int oracle_quantize_activations(const uint16_t *A, uint32_t a_row_stride, uint32
     for (uint32_t m = 0; m < M; ++m)
         for (uint32_t g = 0; g < K / 128; ++g) {
             float amax = 0.0f;
-#if ORACLE_MUTANT == 13
-            for (uint32_t k = 0; k < K; ++k) { /* mutant: one amax over the whole row */
-#else
             for (uint32_t k = g * 128; k < g * 128 + 128; ++k) {
-#endif
                 const float v = fabsf((float)oracle_bf16_to_double(A[(size_t)m * a_row_stride + k]));
                 if (v > amax)
                     amax = v;
@@ -485,5 +394,6 @@ int oracle_w8a8_gemm(const uint8_t *Aq, uint32_t a_row_stride, const float *a_sc
     j.K = K;
     j.exact = exact;
     j.absum = absum;
-    return run_threads(&j, (uint64_t)M * N, nthreads, run_full);
+    j.output = w8a8_output;
+    return run_threads(&j, nthreads);
 }

@@ -469,20 +469,3 @@ PINS = [pin_e4m3_fixed_points, pin_e4m3_all_codes_vs_torch, pin_bf16_fixed_point
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
 def test_pin(pin, oracle_lib):
     pin(oracle_lib)
-
-
-def test_sampled_matches_full(oracle_lib):
-    import workloads
-    c = workloads.make_case("strided_m32_n14336_k5120", N=640, K=1024, a_row_stride=1088,
-                            c_row_stride=700)
-    wl = c.wl
-    C, exact, _ = oracle_lib.gemm(c.A_np(), c.W_np(), c.scale_np(), wl.M, wl.N, wl.K,
-                                  a_row_stride=wl.lda, C=c.C0_np(), c_row_stride=wl.ldc,
-                                  want_exact=True)
-    rng = np.random.default_rng(0)
-    ms = rng.integers(0, wl.M, 200)
-    ns = rng.integers(0, wl.N, 200)
-    out, ex, _ = oracle_lib.gemm_samples(c.A_np(), c.W_np(), c.scale_np(), wl.M, wl.N, wl.K,
-                                         ms, ns, a_row_stride=wl.lda)
-    assert np.array_equal(out, C[ms, ns])
-    assert np.array_equal(ex, exact[ms, ns])
