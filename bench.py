@@ -5,24 +5,37 @@ One JSON line on stdout (rank 0). A step is one full W8A16 GEMM call on the
 workload (default: decode GEMV M=1, N=K=4096, the configuration the headline
 metric is quoted on), through w8a16_gemm_ws with a workspace: up to 16 tokens
 that is one launch of the kernel that splits its own activation tiles; above,
-the split pre-pass and the FP8 x FP8 kernel (two launches). Timing: W untimed warm-up steps, then exactly K steps,
-bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on
-the launching stream. Steps rotate over B distinct input/output buffer sets
-totalling at least 3x the L2 size, so every step streams its weights from HBM.
-The K steps are replayed from CUDA graphs.
+the split pre-pass and the FP8 x FP8 kernel.
 
-  value    = algorithmic bytes of all steps / timed seconds  (GB/s, whole job)
+Timing. Steps rotate over B distinct input/output buffer sets totalling at least
+3x the L2 size, so every step streams its weights from HBM. The steps are
+replayed from CUDA graphs; every graph is replayed once, and then W warm-up
+steps are run, before anything is timed. A timed region is exactly K steps
+between two CUDA events on the launching stream, preceded by a short spin kernel
+so that the host has queued the whole region before the GPU reaches its first
+event (no host gap inside a region). Regions are repeated (at least 5 times, and
+until the GPU has spent `--min-seconds` in them, so the clock sampler sees the
+GPU under load), the whole set bracketed by a barrier and
+torch.cuda.synchronize(); ms_per_step is the MEDIAN region / K. The job time
+of N ranks is the slowest rank's.
+
+  value    = algorithmic bytes of K steps / median region time (GB/s, whole job)
+  configs  = every workload of the metric measured the same way (the headline
+             one included), with GB/s, TFLOP/s, % of the HBM roofline, and for
+             the multi-tile workload the BF16 tensor bound as well
+  roofline = the dominant kernel alone: its own launches replayed back to back
+             from a graph and timed with events (for the pre-split path, the
+             FP8 x FP8 GEMM without its split pre-pass, which is timed apart)
   e2e      = the same metric through the host-buffer entry point: per step the
              pinned host->device copies of A, W and block_scale, the GEMM, and the
              device->host copy of C
-  roofline = the dominant (only) kernel against the measured HBM copy bandwidth
   cpu_baseline = the CPU oracle on the host cores, on a bounded sample
 
 --path w8a8 times the W8A8 variant instead: a step is the per-token 128-group
 activation quantiser followed by the FP8 x FP8 block-scaled GEMM (two launches);
 `value` still counts the BF16-activation problem's bytes, and the roofline entry
 is the GEMM kernel alone (its own algorithmic bytes: FP8 activation codes and
-group scales instead of BF16 activations), timed from a graph of GEMM launches.
+group scales instead of BF16 activations).
 
 --tokens M runs a workload at another token count, e.g. the multi-tile workload at
 M=256 (two 128-token tiles: one weight pass from HBM, the second token tile of each
@@ -37,6 +50,7 @@ import argparse
 import dataclasses
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -54,16 +68,32 @@ import workloads  # noqa: E402
 METRIC = "W8A16 GEMM achieved HBM GB/s and TFLOP/s at M=1..32; % of GB300 HBM roofline"
 METRIC_W8A8 = ("W8A8 variant (activation quantiser + FP8xFP8 GEMM) achieved HBM GB/s of the W8A16 "
                "problem; % of GB300 HBM roofline")
-
-
-def w8a8_gemm_bytes(wl) -> int:
-    """Algorithmic bytes of one W8A8 GEMM launch: E4M3 weights, block scales,
-    E4M3 activation codes, FP32 group scales, BF16 output, each once."""
-    kb = wl.K // 128
-    return wl.N * wl.K + 4 * ((wl.N + 127) // 128) * kb + wl.M * wl.K + 4 * wl.M * kb + 2 * wl.M * wl.N
 DEFAULT_WORKLOAD = "decode_gemv_m1_n4096_k4096"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# GPU cycles of the spin kernel queued before each timed region (~30 us at 2 GHz):
+# long enough for the host to queue the region's events and graph replays.
+PREROLL_CYCLES = 60000
+# Longest timed region of a workload that is not the headline (its K is capped so).
+CONFIG_REGION_SECONDS = 0.02
+
+ARITHMETIC = {
+    "two_term": "BF16 activations as two E4M3 terms (hi + lo/32 per 128-K block, exact for |a| >= "
+                "2^-14 of the block maximum) x E4M3 weights on the tensor cores, FP32 accumulate, "
+                "one FP32 block-scale fold per 128-K step, BF16 output",
+    "w8a8": "E4M3 activations (per-token 128-K group scales) x E4M3 weights on the tensor cores, "
+            "FP32 accumulate, BF16 output",
+    "oracle": "FP64 products and plain k-order FP64 sum, one BF16 rounding (the CPU oracle)",
+}
+
+
+def w8a8_gemm_bytes(wl, terms: int = 1) -> int:
+    """Algorithmic bytes of one FP8 x FP8 GEMM launch: E4M3 weights, block scales,
+    `terms` E4M3 activation codes per value, FP32 factors per token and 128-K
+    group, BF16 output, each once."""
+    kb = wl.K // 128
+    return (wl.N * wl.K + 4 * ((wl.N + 127) // 128) * kb + terms * wl.M * wl.K + 4 * wl.M * kb
+            + 2 * wl.M * wl.N)
 
 
 def dist_env():
@@ -122,6 +152,12 @@ def recorded_traffic(workload: str):
     return None
 
 
+def config_dict(name: str, wl, path: str) -> dict:
+    """The workload's description, identical in both arms."""
+    return {"workload": name, "path": path, "M": wl.M, "N": wl.N, "K": wl.K, "a_row_stride": wl.lda,
+            "c_row_stride": wl.ldc, "seed": wl.seed}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
 
@@ -159,9 +195,10 @@ class ClockSampler:
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
         sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
         mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        pw = [float(s[3]) for s in self.samples if s[3].replace(".", "").isdigit()]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for s in self.samples:
@@ -170,7 +207,9 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(self.samples)}
+                "samples": len(self.samples),
+                "power_w_median": statistics.median(pw) if pw else None,
+                "note": "every sample was taken while timed regions were running"}
 
 
 # --------------------------------------------------------------- our arm --
@@ -185,19 +224,79 @@ def resolve_workload(args):
     return name, dataclasses.replace(wl, name=name, M=args.tokens)
 
 
-def bench_gpu(args, ws, rank, local):
-    import torch
-    import fp8_weight_only_gemm_gb300 as w8
-    from fp8_weight_only_gemm_gb300.build import build_library
+def graph_split(K: int, nsets: int, cap: int = 512):
+    """A graph of G steps replayed q times plus a graph of the r = K - q*G rest:
+    G = K up to `cap` steps, else the largest multiple of the buffer-set count
+    that fits, so every replay of the full graph walks whole rotations."""
+    if K <= cap:
+        return K, 1, 0
+    G = max(nsets, cap // nsets * nsets)
+    q, r = divmod(K, G)
+    return G, q, r
 
-    build_library()
-    w8.load()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(dev)
-    name, wl = resolve_workload(args)
+
+class Runner:
+    """Graph capture and event timing on one stream."""
+
+    def __init__(self, torch, dev, stream, ws):
+        self.torch, self.dev, self.stream, self.ws = torch, dev, stream, ws
+
+    def capture(self, fn, count: int):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(count):
+                    fn(i)
+        return g
+
+    def barrier(self):
+        if self.ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def regions(self, replays, min_seconds: float, min_reps: int = 5, max_reps: int = 50000,
+                batch: int = 32):
+        """Time repeated regions; each region is `replays` (a list of graphs, replayed
+        in order) between two events, after a pre-roll spin. Returns the region times
+        in ms (at least min_reps of them, and at least min_seconds of GPU time in
+        all, unless max_reps is reached)."""
+        torch = self.torch
+        times = []
+        self.barrier()
+        torch.cuda.synchronize(self.dev)
+        with torch.cuda.stream(self.stream):
+            while True:
+                evs = []
+                for _ in range(batch):
+                    torch.cuda._sleep(PREROLL_CYCLES)
+                    s = torch.cuda.Event(enable_timing=True)
+                    e = torch.cuda.Event(enable_timing=True)
+                    s.record(self.stream)
+                    for g in replays:
+                        g.replay()
+                    e.record(self.stream)
+                    evs.append((s, e))
+                torch.cuda.synchronize(self.dev)
+                times += [s.elapsed_time(e) for s, e in evs]
+                if len(times) >= max_reps or (len(times) >= min_reps and sum(times) / 1e3 >= min_seconds):
+                    break
+                # grow the batch once the region length is known (fewer host syncs)
+                per = max(statistics.median(times), 1e-3)
+                batch = int(min(512, max(batch, 0.05 / (per / 1e3 + 30e-6))))
+        self.barrier()
+        return times
+
+
+def measure_workload(name, wl, args, ctx, K: int, headline: bool):
+    """Time one workload through the product entry point; returns its entry of
+    the JSON line (and, for the headline, the clock record and e2e)."""
+    torch, w8, lib = ctx["torch"], ctx["w8"], ctx["lib"]
+    dev, stream, sh, flags, l2, sms = (ctx["dev"], ctx["stream"], ctx["sh"], ctx["flags"], ctx["l2"],
+                                       ctx["sms"])
+    runner = ctx["runner"]
+    hbm, bf16, bf16_sus, src = peaks()
     case = workloads.make_case(wl)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     set_bytes = wl.N * wl.K + case.A.numel() * 2 + case.C0.numel() * 2 + case.scale.numel() * 4
     nsets = max(2, -(-3 * l2 // set_bytes))
     A0, W0, S0, C0 = (case.A.to(dev), case.W.to(dev), case.scale.to(dev), case.C0.to(dev))
@@ -206,211 +305,264 @@ def bench_gpu(args, ws, rank, local):
     w8a8 = args.path == "w8a8"
     qsets = [w8.quantize_activations(A[:, :wl.K]) for (A, _, _, _) in sets] if w8a8 else None
     presplit = not w8a8 and wl.M > 16
-    wss = [torch.empty(max(16, w8.workspace_bytes(wl.M, wl.K)), dtype=torch.uint8, device=dev)
-           for _ in range(nsets)] if not w8a8 else None
-    sms = props.multi_processor_count
+    wsb = max(16, w8.workspace_bytes(wl.M, wl.K))
+    wss = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(nsets)] if not w8a8 else None
     plan = (w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_W8A8, 0, 0, sms).as_dict() if w8a8 else
             w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_PRESPLIT, 0, 0, sms).as_dict() if presplit else
             w8.plan_current(wl.M, wl.N, wl.K))
-    # kernel launches per step: the quantiser or split pre-pass (W8A8, pre-split), then
-    # the GEMM, which is two launches when the plan has a split-K tail
-    launches_per_step = (1 if (w8a8 or presplit) else 0) + (2 if plan.get("tail_tiles") else 1)
-    stream = torch.cuda.Stream(dev)
-    lib = w8.load()
-    sh = int(stream.cuda_stream)
-    flags = w8.FLAG_PDL if args.pdl == "on" else 0
+    gemm_launches = 2 if plan.get("tail_tiles") else 1
+    launches_per_step = (1 if (w8a8 or presplit) else 0) + gemm_launches
 
-    def gemm8(i, fl):
-        A, W, S, C = sets[i % nsets]
-        q, qs = qsets[i % nsets]
-        rc = lib.w8a16_gemm_w8a8(q.data_ptr(), q.stride(0), qs.data_ptr(), qs.stride(0), W.data_ptr(),
-                                 S.data_ptr(), C.data_ptr(), C.stride(0), wl.M, wl.N, wl.K, fl, sh)
+    def ck(rc):
         if rc != 0:
             raise RuntimeError(w8.last_error())
+
+    def gemm8(i, fl=None):
+        A, W, S, C = sets[i % nsets]
+        q, qs = qsets[i % nsets]
+        ck(lib.w8a16_gemm_w8a8(q.data_ptr(), q.stride(0), qs.data_ptr(), qs.stride(0), W.data_ptr(),
+                               S.data_ptr(), C.data_ptr(), C.stride(0), wl.M, wl.N, wl.K,
+                               flags if fl is None else fl, sh))
+
+    def split_only(i):
+        A, _, _, _ = sets[i % nsets]
+        ws_ = wss[i % nsets]
+        ck(lib.w8a16_split_activations(A.data_ptr(), A.stride(0), wl.M, wl.K, ws_.data_ptr(), ws_.numel(), sh))
+
+    def terms_only(i):
+        _, W, S, C = sets[i % nsets]
+        ws_ = wss[i % nsets]
+        ck(lib.w8a16_gemm_split_terms(ws_.data_ptr(), ws_.numel(), W.data_ptr(), S.data_ptr(), C.data_ptr(),
+                                      C.stride(0), wl.M, wl.N, wl.K, flags, sh))
 
     def call(i, fl=None):
         A, W, S, C = sets[i % nsets]
         fl = flags if fl is None else fl
         if w8a8:
             q, qs = qsets[i % nsets]
-            rc = lib.w8a16_quantize_activations(A.data_ptr(), A.stride(0), wl.M, wl.K, q.data_ptr(),
-                                                qs.data_ptr(), qs.stride(0), sh)
-            if rc != 0:
-                raise RuntimeError(w8.last_error())
+            ck(lib.w8a16_quantize_activations(A.data_ptr(), A.stride(0), wl.M, wl.K, q.data_ptr(),
+                                              qs.data_ptr(), qs.stride(0), sh))
             gemm8(i, fl)
             return
-        ws = wss[i % nsets]
-        rc = lib.w8a16_gemm_ws(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
-                               C.stride(0), wl.M, wl.N, wl.K, None, ws.data_ptr(), ws.numel(), fl, sh)
-        if rc != 0:
-            raise RuntimeError(w8.last_error())
+        ws_ = wss[i % nsets]
+        ck(lib.w8a16_gemm_ws(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
+                             C.stride(0), wl.M, wl.N, wl.K, None, ws_.data_ptr(), ws_.numel(), fl, sh))
 
-    # graphs of G steps (one kernel each); K = q*G + r
-    G = min(args.steps, max(nsets, 64) // nsets * nsets) if args.steps >= nsets else args.steps
-    G = max(1, G)
-    q, r = divmod(args.steps, G)
-    graphs = {}
+    # ---- graphs: a region of exactly K steps = q replays of G steps + r steps
+    G, q, r = graph_split(K, nsets)
     with torch.cuda.stream(stream):
-        for (n, cnt) in [("full", G), ("rest", r)]:
-            if cnt == 0:
-                continue
-            for i in range(cnt):        # warm the launch path outside capture
-                call(i)
-            torch.cuda.synchronize(dev)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(cnt):
-                    call(i)
-            graphs[n] = g
-        if w8a8:   # the GEMM kernel alone, for its roofline entry
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(G):
-                    gemm8(i, flags)
-            graphs["gemm"] = g
-    torch.cuda.synchronize(dev)
-
-    def run_steps(k):
-        full, rest = divmod(k, G)
-        for _ in range(full):
-            graphs["full"].replay()
-        for i in range(rest):
+        for i in range(min(G, 2 * nsets)):   # the launch path and the planner's caches, outside capture
             call(i)
-
-    with torch.cuda.stream(stream):
-        run_steps(args.warmup)
+        if presplit:                          # the kernel-only entry points too (set 0 holds a split)
+            split_only(0)
+            terms_only(0)
+        elif w8a8:
+            gemm8(0)
     torch.cuda.synchronize(dev)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            # make the timed region long enough for the clock sampler when K is tiny
-            torch.cuda.synchronize(dev)
-            start.record(stream)
-            for _ in range(q):
-                graphs["full"].replay()
-            if r:
-                graphs["rest"].replay()
-            end.record(stream)
-        torch.cuda.synchronize(dev)
-        if clk.samples == [] and args.steps > 0:
-            time.sleep(0.25)
-    ms = max_over_ranks(start.elapsed_time(end), ws, dev)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    kernel_bytes, kernel_us = wl.roofline_bytes(), ms * 1e3 / args.steps
-    if w8a8:
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                graphs["gemm"].replay()
-            s1, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = max(1, args.steps // G)
-            s1.record(stream)
-            for _ in range(reps):
-                graphs["gemm"].replay()
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        kernel_bytes, kernel_us = w8a8_gemm_bytes(wl), s1.elapsed_time(e1) * 1e3 / (reps * G)
-    sec = ms / 1e3
+    full = runner.capture(call, G)
+    rest = runner.capture(call, r) if r else None
+    region = [full] * q + ([rest] if rest else [])
+    # kernel-only graphs of the dominant kernel (and of the pre-pass)
+    kgraphs = {}
+    if presplit:
+        kgraphs["gemm"] = runner.capture(terms_only, G)
+        kgraphs["split"] = runner.capture(split_only, G)
+    elif w8a8:
+        kgraphs["gemm"] = runner.capture(gemm8, G)
+    torch.cuda.synchronize(dev)
+
+    # ---- warm-up: every graph once, then at least W steps in whole replays
+    with torch.cuda.stream(stream):
+        for g in [full] + ([rest] if rest else []) + list(kgraphs.values()):
+            g.replay()
+        for _ in range(max(1, -(-args.warmup // G))):
+            full.replay()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed regions
+    min_seconds = args.min_seconds if headline else args.config_seconds
+    clk = ClockSampler(ctx["local"]) if headline else None
+    if clk:
+        clk.__enter__()
+    try:
+        times = runner.regions(region, min_seconds)
+    finally:
+        if clk:
+            clk.__exit__()
+    med_ms = max_over_ranks(statistics.median(times), runner.ws, dev)
+    step_s = med_ms / 1e3 / K
     bytes_step = wl.roofline_bytes()
-    gbs = bytes_step * args.steps / sec / 1e9
-    tflops = wl.flops() * args.steps / sec / 1e12
-    hbm, bf16, bf16_sus, src = peaks()
-    traffic = recorded_traffic(name + ("/w8a8" if w8a8 else "/presplit" if presplit else ""))
-    kernel_gbs = kernel_bytes / kernel_us / 1e3
+    out = {
+        "M": wl.M, "N": wl.N, "K": wl.K,
+        "steps_per_region": K, "regions": len(times),
+        "us_per_step": step_s * 1e6,
+        "region_ms": {"min": min(times), "median": statistics.median(times), "max": max(times)},
+        "gbs": bytes_step / step_s / 1e9,
+        "tflops": wl.flops() / step_s / 1e12,
+        "frac_hbm": bytes_step / step_s / 1e9 / hbm,
+        "roofline_bytes": bytes_step,
+        "path": ("activation quantiser + W8A8 GEMM" if w8a8 else
+                 "w8a16_gemm_ws: split pre-pass + FP8 x FP8 GEMM on two terms" if presplit else
+                 "w8a16_gemm_ws: one launch of the two-term FP8 kernel" if plan["variant"] == 3 else
+                 "w8a16_gemm_ws: one launch of the BF16 kernel"),
+        "launches_per_step": launches_per_step,
+        "plan": plan,
+    }
+    # both bounds where the tensor work is not negligible
+    t_hbm = bytes_step / (hbm * 1e9)
+    t_tensor = wl.flops() / (bf16 * 1e12)
+    out["bound_us"] = {"hbm": t_hbm * 1e6, "bf16_tensor": t_tensor * 1e6}
+    out["bound"] = "hbm" if t_hbm >= t_tensor else "tensor"
+    out["frac_of_binding_bound"] = max(t_hbm, t_tensor) / step_s
 
-    # end to end through the host-buffer entry point
-    e2e = None
-    if not args.no_e2e and w8a8:
-        A_h = case.A.pin_memory()
-        W_h = case.W.pin_memory()
-        S_h = case.scale.pin_memory()
-        C_h = case.C0.clone().pin_memory()
-        dA, dW, dS, dC = sets[0]
-        e_steps = max(3, min(args.steps, 200))
+    # ---- the dominant kernel alone
+    if kgraphs:
+        kt = {k: statistics.median(runner.regions([g], 0.1 if not headline else 0.5)) / G * 1e3
+              for k, g in kgraphs.items()}
+        kbytes = w8a8_gemm_bytes(wl, 2 if presplit else 1)
+        out["kernel"] = {"name": "w8a16_w8a8_kernel (terms 2)" if presplit else "w8a16_w8a8_kernel (terms 1)",
+                         "us": kt["gemm"], "bytes": kbytes, "gbs": kbytes / kt["gemm"] / 1e3,
+                         "frac_hbm": kbytes / kt["gemm"] / 1e3 / hbm,
+                         "timing": f"{G} launches of the GEMM alone replayed back to back from a graph"
+                                   f"{' (programmatic dependent launches)' if flags else ''}"}
+        if presplit:
+            out["kernel"]["split_prepass_us"] = kt["split"]
+            out["kernel"]["split_timing"] = f"{G} launches of split_act_kernel alone from a graph"
+    else:
+        out["kernel"] = {"name": "w8a16_tc8_kernel" if plan["variant"] == 3 else "w8a16_tc_kernel",
+                         "us": step_s * 1e6,
+                         "bytes": bytes_step, "gbs": bytes_step / step_s / 1e9,
+                         "frac_hbm": bytes_step / step_s / 1e9 / hbm,
+                         "timing": "the step is this kernel's launch" +
+                                   ("es (whole tiles + split-K tail)" if gemm_launches > 1 else " alone")}
+    traffic_key = name + ("/w8a8" if w8a8 else "/presplit" if presplit else "")
+    out["kernel"]["traffic"] = recorded_traffic(traffic_key)
+    out["gpu_launches_timed"] = len(times) * K * launches_per_step
 
+    extra = {"case": case, "sets": sets, "clocks": clk.summary() if clk else None, "nsets": nsets,
+             "set_bytes": set_bytes, "G": G, "call": call, "presplit": presplit, "w8a8": w8a8}
+    return out, extra
+
+
+def e2e_host(wl, case, sets, ctx, steps: int, w8a8: bool, call) -> dict:
+    """The same metric end to end through the host-buffer entry point."""
+    torch, w8 = ctx["torch"], ctx["w8"]
+    dev, stream = ctx["dev"], ctx["stream"]
+    A_h = case.A.pin_memory()
+    W_h = case.W.pin_memory()
+    S_h = case.scale.pin_memory()
+    C_h = case.C0.clone().pin_memory()
+    dA, dW, dS, dC = sets[0]
+    e_steps = max(3, min(steps, 200))
+
+    if w8a8:
         def host_step():
             dA.copy_(A_h, non_blocking=True)
             dW.copy_(W_h, non_blocking=True)
             dS.copy_(S_h, non_blocking=True)
             call(0, 0)
             C_h.copy_(dC, non_blocking=True)
+    else:
+        def host_step():
+            w8.gemm_host(A_h[:, :wl.K], W_h, S_h, C_h[:, :wl.N], dA, dW, dS, dC, stream=stream)
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                host_step()
-            torch.cuda.synchronize(dev)
-            s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s2.record(stream)
-            for _ in range(e_steps):
-                host_step()
-            e2.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            host_step()
         torch.cuda.synchronize(dev)
-        e_sec = s2.elapsed_time(e2) / 1e3
-        e2e = {"value": bytes_step * e_steps / e_sec / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": case.A.numel() * 2 + wl.N * wl.K + case.scale.numel() * 4,
-               "d2h_bytes_per_step": case.C0.numel() * 2, "steps": e_steps,
-               "ms_per_step": e_sec * 1e3 / e_steps,
-               "path": "pinned host copies + quantiser + W8A8 GEMM + copy of C, one stream"}
-    elif not args.no_e2e:
-        A_h = case.A.pin_memory()
-        W_h = case.W.pin_memory()
-        S_h = case.scale.pin_memory()
-        C_h = case.C0.clone().pin_memory()
-        dA, dW, dS, dC = sets[0]
-        e_steps = max(3, min(args.steps, 200))
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                w8.gemm_host(A_h[:, :wl.K], W_h, S_h, C_h[:, :wl.N], dA, dW, dS, dC, stream=stream)
-            torch.cuda.synchronize(dev)
-            s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s2.record(stream)
-            for _ in range(e_steps):
-                w8.gemm_host(A_h[:, :wl.K], W_h, S_h, C_h[:, :wl.N], dA, dW, dS, dC, stream=stream)
-            e2.record(stream)
-        torch.cuda.synchronize(dev)
-        e_sec = s2.elapsed_time(e2) / 1e3
-        h2d = wl.M * wl.K * 2 + wl.N * wl.K + case.scale.numel() * 4
-        d2h = wl.M * wl.N * 2
-        e2e = {"value": bytes_step * e_steps / e_sec / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-               "ms_per_step": e_sec * 1e3 / e_steps}
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(e_steps):
+            host_step()
+        e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e_sec = s2.elapsed_time(e2) / 1e3
+    h2d = case.A.numel() * 2 + wl.N * wl.K + case.scale.numel() * 4
+    d2h = case.C0.numel() * 2
+    return {"value": wl.roofline_bytes() * e_steps / e_sec / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+            "ms_per_step": e_sec * 1e3 / e_steps,
+            "path": ("pinned host copies + quantiser + W8A8 GEMM + copy of C, one stream" if w8a8 else
+                     "w8a16_gemm_host: pinned host copies of A (full pitch), W and block_scale, the GEMM, "
+                     "the copy of C (full pitch), one stream")}
+
+
+def bench_gpu(args, ws, rank, local):
+    import torch
+    import fp8_weight_only_gemm_gb300 as w8
+    from fp8_weight_only_gemm_gb300.build import build_library
+
+    build_library()
+    lib = w8.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    stream = torch.cuda.Stream(dev)
+    ctx = {"torch": torch, "w8": w8, "lib": lib, "dev": dev, "stream": stream, "sh": int(stream.cuda_stream),
+           "flags": w8.FLAG_PDL if args.pdl == "on" else 0, "local": local,
+           "l2": int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), "sms": props.multi_processor_count,
+           "runner": Runner(torch, dev, stream, ws)}
+    hbm, bf16, bf16_sus, src = peaks()
+    name, wl = resolve_workload(args)
+
+    head, extra = measure_workload(name, wl, args, ctx, args.steps, headline=True)
+    e2e = None if args.no_e2e else e2e_host(wl, extra["case"], extra["sets"], ctx, args.steps, extra["w8a8"],
+                                            extra["call"])
+    del extra["sets"]
+    configs = {name: head}
+    if args.configs == "all":
+        for other in workloads.CONFIG_ORDER:
+            if other == name:
+                continue
+            owl = workloads.CONFIGS[other]
+            est = owl.roofline_bytes() / (0.5 * hbm * 1e9)   # a generous guess of a step's time
+            k = max(5, min(args.steps, int(CONFIG_REGION_SECONDS / est)))
+            torch.cuda.empty_cache()
+            configs[other], _ = measure_workload(other, owl, args, ctx, k, headline=False)
+            torch.cuda.empty_cache()
 
     st = w8.device_status(stream=stream)
     if st[0] != 0:
         raise RuntimeError(f"device status {st}: a bounded wait ran out during the benchmark")
 
+    step_s = head["us_per_step"] / 1e6
+    kern = head["kernel"]
+    w8a8, presplit = extra["w8a8"], extra["presplit"]
     line = {
-        "metric": METRIC_W8A8 if w8a8 else METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8" if w8a8 else "bf16",
+        "metric": METRIC_W8A8 if w8a8 else METRIC, "value": head["gbs"] * ws, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "arithmetic": ARITHMETIC["w8a8" if w8a8 else "two_term"],
         "data": "synthetic",
-        "config": {"workload": name, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K,
-                   "a_row_stride": wl.lda, "c_row_stride": wl.ldc, "seed": wl.seed,
-                   "l2": f"inputs rotate over {nsets} buffer sets ({nsets * set_bytes / 1e6:.0f} MB, "
-                         f">= 3x the {l2 / 1e6:.0f} MB L2): weights stream from HBM every step",
-                   "graphs": f"steps replayed from CUDA graphs of {G} launches",
-                   "launch": ("programmatic dependent launch (W8A16_FLAG_PDL): each call's weight "
-                              "prefetch overlaps the previous call's tail" if flags else
-                              "plain stream order"),
-                   "plan": plan, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-        "tflops": tflops,
-        "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": kernel_gbs / hbm, "traffic": traffic,
-                     "peak_source": f"{src}: hbm copy bandwidth",
-                     "kernel": ("w8a16_w8a8_kernel (terms 1), timed alone" if w8a8 else
-                                "split pre-pass + w8a16_w8a8_kernel (terms 2): the whole step" if presplit
-                                else "w8a16_tc8_kernel, one launch per step"),
-                     "kernel_us": kernel_us,
-                     "bytes_per_launch": kernel_bytes,
-                     "tensor_frac_of_bf16_peak": tflops / bf16},
-        "gpu_launches": args.steps * launches_per_step,
-        "clocks": clk.summary(),
+        "config": config_dict(name, wl, args.path),
+        "parallelism": f"replicas x{ws} (no collective)" if ws > 1 else "single GPU",
+        "method": {
+            "l2": f"inputs rotate over {extra['nsets']} buffer sets ({extra['nsets'] * extra['set_bytes'] / 1e6:.0f} "
+                  f"MB, >= 3x the {ctx['l2'] / 1e6:.0f} MB L2): weights stream from HBM every step",
+            "graphs": f"steps replayed from CUDA graphs of {extra['G']} launches; every graph replayed once "
+                      f"and >= {args.warmup} warm-up steps run before timing",
+            "timing": f"median of {head['regions']} timed regions of exactly {args.steps} steps, each between "
+                      "two CUDA events on the launching stream after a pre-roll spin kernel; all regions "
+                      "bracketed by a barrier and torch.cuda.synchronize(); max over ranks",
+            "launch": ("programmatic dependent launch (W8A16_FLAG_PDL): each call's weight prefetch overlaps "
+                       "the previous call's tail" if ctx["flags"] else "plain stream order"),
+            "plan": head["plan"],
+        },
+        "tflops": head["tflops"] * ws,
+        "roofline": {"bound": "hbm", "achieved": kern["gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": kern["gbs"] / hbm, "traffic": kern["traffic"],
+                     "peak_source": f"{src}: HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                                    else "fallback HBM figure",
+                     "kernel": kern["name"], "kernel_us": kern["us"], "kernel_timing": kern["timing"],
+                     "bytes_per_launch": kern["bytes"],
+                     "tensor_frac_of_bf16_peak": head["tflops"] / bf16},
+        "configs": configs,
+        "gpu_launches": head["gpu_launches_timed"],
+        "clocks": extra["clocks"],
         "e2e": e2e,
     }
+    if presplit:
+        line["roofline"]["split_prepass_us"] = kern.get("split_prepass_us")
     return line
 
 
@@ -477,11 +629,11 @@ def bench_reference(args):
         step()
     sec = time.perf_counter() - t0
     v = wl.roofline_bytes() * args.steps / sec / 1e9
-    return {"impl": "reference", "metric": METRIC_W8A8 if args.path == "w8a8" else METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": name, "path": args.path, "M": wl.M, "N": wl.N, "K": wl.K},
+    return {"impl": "reference", "metric": METRIC_W8A8 if args.path == "w8a8" else METRIC, "value": v,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "arithmetic": ARITHMETIC["oracle"], "data": "synthetic",
+            "config": config_dict(name, wl, args.path),
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"{args.steps} full calls of {name} on the CPU oracle "
                                        f"({'quantiser + W8A8 product, ' if args.path == 'w8a8' else ''}"
@@ -500,6 +652,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
     ap.add_argument("--tokens", type=int, default=None,
                     help="run the workload at this token count M instead of its own")
+    ap.add_argument("--configs", choices=["all", "none"], default="all",
+                    help="also measure every other workload of the metric (entries under 'configs')")
+    ap.add_argument("--min-seconds", type=float, default=2.0,
+                    help="GPU time spent in the headline workload's timed regions (at least 5 regions)")
+    ap.add_argument("--config-seconds", type=float, default=0.5,
+                    help="GPU time spent in each other workload's timed regions")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path", choices=["w8a16", "w8a8"], default="w8a16",
                     help="w8a8: activation quantiser + W8A8 GEMM per step")
@@ -525,6 +683,8 @@ def main():
     if args.warmup is None:
         args.warmup = 2000
     args.warmup = max(3, args.warmup)
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     if ws > 1:
         import torch
         import torch.distributed as dist

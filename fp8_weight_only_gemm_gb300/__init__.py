@@ -6,20 +6,20 @@ scale per 128x128 block)^T, computed by hand-written tcgen05/TMA kernels in
 Python binding: torch provides device memory and streams only. The library also
 holds the weight block quantiser that produces W and the block scales.
 """
-from .binding import (FLAG_PDL, Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8, VARIANT_PRESPLIT,
-                      WEIGHTS_BF16, WEIGHTS_F32, W8A16Error,
-                      check_args, cluster_capacity, device_status, gemm, gemm_host, gemm_ptr,
-                      gemm_w8a8, gemm_w8a8_ptr, gemm_ws, gemm_ws_ptr, quantize_activations,
-                      workspace_bytes,
+from .binding import (FLAG_PDL, Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8,
+                      VARIANT_PRESPLIT, WEIGHTS_BF16, WEIGHTS_F32, W8A16Error,
+                      check_args, cluster_capacity, device_status, gemm, gemm_host, gemm_noalloc, gemm_ptr,
+                      gemm_split_terms, gemm_w8a8, gemm_w8a8_ptr, gemm_ws, gemm_ws_ptr, quantize_activations,
+                      split_activations, workspace_bytes,
                       header_functions, last_error, load, plan_current, plan_for, plan_variant,
                       quantize_weights, quantize_weights_ptr, selftest_wait_timeout, strerror,
                       version)
 
-__all__ = ["FLAG_PDL", "Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "VARIANT_TC8", "VARIANT_W8A8", "VARIANT_PRESPLIT",
-           "WEIGHTS_BF16", "WEIGHTS_F32", "W8A16Error",
-           "check_args", "cluster_capacity", "device_status", "gemm", "gemm_host", "gemm_ptr",
-           "gemm_w8a8", "gemm_w8a8_ptr", "gemm_ws", "gemm_ws_ptr", "quantize_activations",
-           "workspace_bytes",
+__all__ = ["FLAG_PDL", "Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "VARIANT_TC8", "VARIANT_W8A8",
+           "VARIANT_PRESPLIT", "WEIGHTS_BF16", "WEIGHTS_F32", "W8A16Error",
+           "check_args", "cluster_capacity", "device_status", "gemm", "gemm_host", "gemm_noalloc", "gemm_ptr",
+           "gemm_split_terms", "gemm_w8a8", "gemm_w8a8_ptr", "gemm_ws", "gemm_ws_ptr", "quantize_activations",
+           "split_activations", "workspace_bytes",
            "header_functions", "last_error", "load", "plan_current", "plan_for", "plan_variant",
            "quantize_weights", "quantize_weights_ptr", "selftest_wait_timeout", "strerror",
            "version"]

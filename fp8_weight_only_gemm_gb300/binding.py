@@ -65,6 +65,8 @@ _SIGS = {
     "w8a16_workspace_bytes": (_U64, [_U32, _U32]),
     "w8a16_gemm_noalloc": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32, _VP]),
     "w8a16_noalloc_scratch_bytes": (_U64, []),
+    "w8a16_split_activations": (_INT, [_VP, _U32, _U32, _U32, _VP, _U64, _VP]),
+    "w8a16_gemm_split_terms": (_INT, [_VP, _U64, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32, _VP]),
     "w8a16_gemm_ws": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, ctypes.POINTER(Plan), _VP,
                              _U64, _U32, _VP]),
     "w8a16_gemm_w8a8": (_INT, [_VP, _U32, _VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32,
@@ -305,6 +307,49 @@ def gemm_ws_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N
     return load().w8a16_gemm_ws(A_ptr or None, a_row_stride, W_ptr or None, scale_ptr or None, C_ptr or None,
                                 c_row_stride, M, N, K, ctypes.byref(plan) if plan is not None else None,
                                 ws_ptr or None, ws_bytes, flags, stream or None)
+
+
+def split_activations(A, workspace=None, *, stream=None):
+    """w8a16_split_activations: the two E4M3 terms of BF16 A [M, K] (row pitch A.stride(0))
+    and their factors, written into `workspace` (a CUDA uint8 tensor of at least
+    workspace_bytes(M, K) bytes; None allocates one with torch). Returns the workspace."""
+    import torch
+    if A.dim() != 2 or A.dtype != torch.bfloat16 or A.stride(1) != 1:
+        raise ValueError("A must be a bfloat16 [M, K] tensor with unit column stride")
+    M, K = A.shape
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_bytes(M, K)), dtype=torch.uint8, device=A.device)
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor")
+    _on_one_gpu(A, workspace)
+    with torch.cuda.device(A.device):
+        rc = load().w8a16_split_activations(A.data_ptr(), A.stride(0), M, K, workspace.data_ptr(),
+                                            workspace.numel(), _stream_handle(stream))
+    _check(rc)
+    return workspace
+
+
+def gemm_split_terms(workspace, M, W, scale, C=None, *, stream=None, flags: int = 0):
+    """w8a16_gemm_split_terms: C [M, >=N] = the product of the activations that
+    split_activations() wrote into `workspace` (for M tokens) with W and scale."""
+    import torch
+    if W.dim() != 2 or not _is_codes(W):
+        raise ValueError("W must be a uint8 or float8_e4m3fn [N, K] tensor")
+    N, K = W.shape
+    _scale_shape(scale, N, K)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=W.device)
+    if C.dtype != torch.bfloat16 or C.shape[0] != M or C.shape[1] < N or C.stride(1) != 1:
+        raise ValueError("C must be bfloat16 [M, >=N] with unit column stride")
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor")
+    _on_one_gpu(workspace, W, scale, C)
+    with torch.cuda.device(W.device):
+        rc = load().w8a16_gemm_split_terms(workspace.data_ptr(), workspace.numel(), W.data_ptr(),
+                                           scale.data_ptr(), C.data_ptr(), C.stride(0), M, N, K, flags,
+                                           _stream_handle(stream))
+    _check(rc)
+    return C
 
 
 def gemm_ptr(A_ptr, a_row_stride, W_ptr, scale_ptr, C_ptr, c_row_stride, M, N, K, stream=0,

@@ -766,6 +766,66 @@ int w8a16_gemm_noalloc(const void* A, uint32_t a_row_stride, const void* W, cons
 
 uint64_t w8a16_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
+int w8a16_split_activations(const void* A, uint32_t a_row_stride, uint32_t M, uint32_t K, void* workspace,
+                            uint64_t workspace_bytes, w8a16_stream_t stream) {
+    int rc = check_sizes(a_row_stride, 1, M, 1, K);
+    if (rc) return rc;
+    if (!A || !workspace)
+        return fail(W8A16_ERR_NULL, std::string("w8a16_split_activations: NULL ") + (!A ? "A" : "workspace") +
+                                        " pointer");
+    if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16)
+        return fail(W8A16_ERR_ALIGN, "w8a16_split_activations: A and the workspace need 16-byte alignment");
+    const uint64_t need = w8a16::split_ws_bytes(M, K);
+    if (workspace_bytes < need)
+        return fail(W8A16_ERR_ARG, "w8a16_split_activations: the workspace needs " + std::to_string(need) +
+                                       " bytes (have " + std::to_string(workspace_bytes) + ")");
+    DeviceInfo info;
+    std::string err;
+    rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    const uint32_t fstride = static_cast<uint32_t>(w8a16::split_ws_scale_stride(M));
+    uint8_t* codes = static_cast<uint8_t*>(workspace);
+    float* factors = reinterpret_cast<float*>(codes + 2ull * M * K);
+    rc = w8a16::launch_split_act(A, a_row_stride, M, K, codes, factors, fstride,
+                                 static_cast<cudaStream_t>(stream), &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
+int w8a16_gemm_split_terms(const void* workspace, uint64_t workspace_bytes, const void* W,
+                           const float* block_scale, void* C, uint32_t c_row_stride, uint32_t M, uint32_t N,
+                           uint32_t K, uint32_t flags, w8a16_stream_t stream) {
+    if (flags & ~static_cast<uint32_t>(W8A16_FLAG_PDL))
+        return fail(W8A16_ERR_ARG, "w8a16_gemm_split_terms: unknown flag bits " + u(flags));
+    int rc = check_sizes(K, c_row_stride, M, N, K);
+    if (rc) return rc;
+    rc = check_ptrs(workspace, W, block_scale, C);
+    if (rc) return rc;
+    const uint64_t need = w8a16::split_ws_bytes(M, K);
+    if (workspace_bytes < need)
+        return fail(W8A16_ERR_ARG, "w8a16_gemm_split_terms: the workspace holds " +
+                                       std::to_string(workspace_bytes) + " bytes, the split of (M, K) needs " +
+                                       std::to_string(need));
+    const TimeoutSetting& ts = timeout_setting();
+    if (!ts.valid)
+        return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
+                                       "' is not an integer number of milliseconds in 1..600000");
+    DeviceInfo info;
+    std::string err;
+    rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    w8a16_plan_t plan;
+    rc = plan_live(W8A16_VARIANT_PRESPLIT, M, N, K, info, &plan, &err);
+    if (rc) return fail(rc, err);
+    const uint32_t fstride = static_cast<uint32_t>(w8a16::split_ws_scale_stride(M));
+    const uint8_t* codes = static_cast<const uint8_t*>(workspace);
+    const float* factors = reinterpret_cast<const float*>(codes + 2ull * M * K);
+    const w8a16::W8A8Args a{codes, K, factors, fstride, W, block_scale, C, c_row_stride, M, N, K, 2u};
+    rc = w8a16::launch_w8a8(a, plan, static_cast<cudaStream_t>(stream), ts.ns, flags, &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
 int w8a16_gemm_ws(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale, void* C,
                   uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t* plan,
                   void* workspace, uint64_t workspace_bytes, uint32_t flags, w8a16_stream_t stream) {

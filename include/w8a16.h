@@ -260,6 +260,39 @@ W8A16_API int w8a16_gemm_noalloc(const void *A, uint32_t a_row_stride, const voi
                                  w8a16_stream_t stream);
 W8A16_API uint64_t w8a16_noalloc_scratch_bytes(void);
 
+/* The two halves of the pre-split path (W8A16_VARIANT_PRESPLIT) as separate calls,
+ * so that products which share one activation matrix (the Q, K and V projections
+ * of one input, say) split it once. Same operation and result contract as
+ * w8a16_gemm_ws on its pre-split path (the reading of W8A16_VARIANT_TC8: each
+ * activation of a token's 128-K block is written as two E4M3 terms).
+ *
+ * w8a16_split_activations -- BF16 A [M][a_row_stride] (first K of a row read;
+ * a_row_stride >= K, a multiple of 8) -> the workspace: hi codes [M][K], lo codes
+ * [M][K] (E4M3 bytes, rows of K) and one FP32 factor 2^(E-7) per token and 128-K
+ * group ([K/128][M rounded up to 4]). workspace: device memory, 16-byte aligned,
+ * at least w8a16_workspace_bytes(M, K) bytes, owned by the caller. A and the
+ * workspace 16-byte aligned. One kernel, queued as a programmatic dependent launch
+ * that waits for the previous kernel of the stream before touching memory. Checks
+ * (before any device work): those of w8a16_gemm on M, K and a_row_stride, NULL,
+ * alignment, and the workspace size (W8A16_ERR_ARG). */
+W8A16_API int w8a16_split_activations(const void *A, uint32_t a_row_stride, uint32_t M, uint32_t K,
+                                      void *workspace, uint64_t workspace_bytes,
+                                      w8a16_stream_t stream);
+
+/* w8a16_gemm_split_terms -- C = the W8A16 product of the activations that
+ * w8a16_split_activations wrote into `workspace` for the same (M, K), with W,
+ * block_scale, C, c_row_stride, N as in w8a16_gemm. The FP8 x FP8 kernel (one
+ * launch, or two with a split-K tail). flags: W8A16_FLAG_PDL lets the kernel read
+ * its first weight tiles and block scales before the previous kernel of the
+ * stream has finished (which must not write W or block_scale); the workspace, A's
+ * terms, is read only after it. The workspace is only read. Checks as for
+ * w8a16_gemm (the workspace takes A's place in the NULL and alignment checks),
+ * plus its size (W8A16_ERR_ARG). */
+W8A16_API int w8a16_gemm_split_terms(const void *workspace, uint64_t workspace_bytes, const void *W,
+                                     const float *block_scale, void *C, uint32_t c_row_stride,
+                                     uint32_t M, uint32_t N, uint32_t K, uint32_t flags,
+                                     w8a16_stream_t stream);
+
 /* ---- errors and status -------------------------------------------------- */
 
 /* Message of the last failed call on this host thread ("" if none). */

@@ -100,3 +100,30 @@ def test_cpu_baseline_all_cores_and_one():
     assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1
     if d["cores"] > 1:
         assert d["single_core"]["cores"] == 1 and d["single_core"]["value"] > 0
+
+
+def test_graph_split_covers_exactly_k_steps():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    for K, nsets in [(1, 25), (20, 25), (512, 3), (513, 25), (20000, 25), (20000, 2), (777, 600)]:
+        G, q, r = bench.graph_split(K, nsets)
+        assert q * G + r == K and G >= 1 and q >= 1 and 0 <= r < G
+        if K > 512:
+            assert G % nsets == 0 or G == nsets
+
+
+def test_both_arms_print_the_same_config():
+    sys.path.insert(0, str(ROOT))
+    import argparse
+    import bench
+    import workloads
+    args = argparse.Namespace(workload="strided_m32_n14336_k5120", tokens=None, path="w8a16", steps=1,
+                              warmup=0)
+    name, wl = bench.resolve_workload(args)
+    ours = bench.config_dict(name, wl, args.path)
+    small = workloads.CONFIGS["tiny_m1_n256_k256"]
+    ref = bench.bench_reference(argparse.Namespace(workload="tiny_m1_n256_k256", tokens=None, path="w8a16",
+                                                   steps=1, warmup=0))
+    assert set(ref["config"]) == set(ours)
+    assert ref["config"] == bench.config_dict("tiny_m1_n256_k256", small, "w8a16")
+    assert ours["a_row_stride"] == 5184 and ours["c_row_stride"] == 14400

@@ -268,3 +268,49 @@ def test_split_k_tail_with_shared_receive_buffer_repeated():
             first = got
         else:
             assert np.array_equal(got, first), f"run {rep} differs from run 0"
+
+
+@pytest.mark.parametrize("M,N,K,lda", [(40, 300, 1280, 1344), (32, 14336, 5120, 5184), (5, 256, 512, 512),
+                                       (129, 640, 1024, 1024)])
+def test_split_then_terms_matches_the_one_call_path(M, N, K, lda):
+    """w8a16_split_activations + w8a16_gemm_split_terms give the bits of
+    w8a16_gemm_ws's pre-split path (same split, same kernel, same plan), and each
+    of three weights multiplied from one split matches the oracle."""
+    from fp8_weight_only_gemm_gb300 import binding
+    cases = [workloads.make_case("strided_m32_n14336_k5120", M=M, N=N, K=K, a_row_stride=lda,
+                                 c_row_stride=N + 5, seed=7 * M + N + s) for s in range(3)]
+    A = cases[0].A.cuda()   # one activation matrix, three weights (the seeds differ only in W)
+    ws = binding.split_activations(A[:, :K])
+    for i, case in enumerate(cases):
+        case = workloads.Case(case.wl, cases[0].A, case.W, case.scale, case.C0)
+        W, S, C = case.W.cuda(), case.scale.cuda(), case.C0.cuda()
+        binding.gemm_split_terms(ws, M, W, S, C[:, :N])
+        torch.cuda.synchronize()
+        got = C.cpu().view(torch.int16).numpy().view(np.uint16)
+        ref, exact, absum = oracle_full(case)
+        compare(case, got, ref, exact, absum, split_k=16, label=f"split+terms M{M} w{i}", variant=3)
+        if M > 16:   # w8a16_gemm_ws takes its pre-split path above 16 tokens
+            assert np.array_equal(got, run_ws(case)), "two calls differ from w8a16_gemm_ws"
+
+
+def test_split_terms_checks():
+    from fp8_weight_only_gemm_gb300 import binding
+    lib = binding.load()
+    A = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    assert lib.w8a16_split_activations(A.data_ptr(), 256, 4, 256, small.data_ptr(), small.numel(), None) == -13
+    assert lib.w8a16_split_activations(A.data_ptr(), 256, 0, 256, small.data_ptr(), small.numel(), None) == -1
+    assert lib.w8a16_split_activations(A.data_ptr(), 256, 4, 200, small.data_ptr(), small.numel(), None) == -2
+    ws = binding.split_activations(A)
+    W = torch.zeros((256, 256), dtype=torch.uint8, device="cuda")
+    S = torch.zeros((2, 2), dtype=torch.float32, device="cuda")
+    C = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
+    assert lib.w8a16_gemm_split_terms(ws.data_ptr(), 15, W.data_ptr(), S.data_ptr(), C.data_ptr(), 256,
+                                      4, 256, 256, 0, None) == -13
+    assert lib.w8a16_gemm_split_terms(ws.data_ptr(), ws.numel(), W.data_ptr(), S.data_ptr(), C.data_ptr(), 255,
+                                      4, 256, 256, 0, None) == -3
+    assert lib.w8a16_gemm_split_terms(ws.data_ptr(), ws.numel(), W.data_ptr(), S.data_ptr(), C.data_ptr(), 256,
+                                      4, 256, 256, 2, None) == -13
+    binding.gemm_split_terms(ws, 4, W, S, C)
+    torch.cuda.synchronize()
+    assert float(C.float().abs().max()) == 0.0
