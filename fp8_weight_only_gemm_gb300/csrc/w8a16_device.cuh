@@ -122,6 +122,16 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Wait for the grids this one depends on, then start the time limit of the
+// calling role's bounded waits. A role calls this before its first wait on
+// anything downstream of the dependency (the activations, the MMAs that read
+// them), so the time a programmatic launch spends behind a long predecessor is
+// not charged to that limit.
+__device__ __forceinline__ uint64_t deadline_after_dependency(uint64_t timeout_ns) {
+    grid_dependency_wait();
+    return globaltimer_ns() + timeout_ns;
+}
+
 // ------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

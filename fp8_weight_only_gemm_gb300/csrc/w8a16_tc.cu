@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
     const uint32_t s_begin = static_cast<uint32_t>(static_cast<uint64_t>(rank) * ksteps / split_k);
     const uint32_t s_end = static_cast<uint32_t>(static_cast<uint64_t>(rank + 1) * ksteps / split_k);
     const uint32_t nsteps = s_end - s_begin;
-    const uint64_t deadline = globaltimer_ns() + timeout_ns;
+    uint64_t deadline = globaltimer_ns() + timeout_ns;   // restarted by each role after the dependency wait
     const uint32_t my_row0 = owned_row0(rank, split_k);
     const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
     const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
@@ -230,6 +230,9 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             uint32_t issued = npre;                            // issued at set-up
             for (uint32_t i = npre; i < nsteps; ++i) {
                 const uint32_t s = i % STAGES;
+                // Converters release the slots of the first NA + 1 steps before any
+                // MMA has run; later slots free only after the dependency wait.
+                if (i == STAGES + Cfg::NA + 1) deadline = deadline_after_dependency(timeout_ns);
                 if (!mbar_wait(wempty0 + 8u * s, ((i / STAGES) - 1) & 1, deadline, abort_flag,
                                &g_tc_status, kWaitEmpty))
                     break;
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             const uint64_t pol_a = l2_policy_evict_last();    // A is re-read by every tile
             // A may be written by the previous grid in the stream: wait for it
             // (returns at once unless launched as a programmatic dependent).
-            grid_dependency_wait();
+            deadline = deadline_after_dependency(timeout_ns);
             uint32_t issued = 0;
             for (uint32_t i = 0; i < nsteps; ++i) {
                 const uint32_t j = i % Cfg::SA;
@@ -276,6 +279,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
         // issuing thread's MMAs only).
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kTcRows, TN);
+            deadline = deadline_after_dependency(timeout_ns);   // the activations come after it
             for (uint32_t i = (warp == 1 ? 0u : 1u); i < nsteps; i += 2) {
                 const uint32_t a = i % Cfg::NA, p = i % Cfg::NP, j = i % Cfg::SA;
                 if (!mbar_wait(tfull0 + 8u * a, (i / Cfg::NA) & 1, deadline, abort_flag,
@@ -334,6 +338,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
                 for (uint32_t t = 0; t < 8; ++t) w[8 * c + t] = o[t];
             }
             if (i >= Cfg::NA) {   // buffer a last held step i - NA: wait for its MMAs
+                if (i == Cfg::NA) deadline = deadline_after_dependency(timeout_ns);
                 const uint32_t q2 = i - Cfg::NA;
                 if (!warp_wait(mdone0 + 8u * (q2 % Cfg::ND), (q2 / Cfg::ND) & 1, deadline, abort_flag,
                                kWaitAEmpty))
@@ -358,6 +363,7 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
         // programmatic launch the caller guarantees they are not being written.
         float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
         float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
+        deadline = deadline_after_dependency(timeout_ns);   // the products come after it
         for (uint32_t i = 0; i < nsteps; ++i) {
             if (i != 0 && (i & 31u) == 0) {
                 sc_cur = sc_next;
@@ -461,10 +467,13 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
 }
 
 // One CTA, one thread: waits on an mbarrier nothing arrives on, so the bounded
-// wait must run out, record W8A16_STATUS_WAIT_TIMEOUT and return.
+// wait must run out, record W8A16_STATUS_WAIT_TIMEOUT and return. It lets a
+// programmatic dependent start at once, so a call queued after it with
+// W8A16_FLAG_PDL runs its set-up while this wait is still going.
 __global__ void w8a16_wait_selftest_kernel(uint64_t timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
+    grid_launch_dependents();
     if (threadIdx.x != 0) return;
     abort_flag = 0;
     mbar_init(smem_u32(&bar), 1);

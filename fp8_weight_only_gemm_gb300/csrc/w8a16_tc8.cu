@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
     const uint32_t s_begin = static_cast<uint32_t>(static_cast<uint64_t>(rank) * ksteps / split_k);
     const uint32_t s_end = static_cast<uint32_t>(static_cast<uint64_t>(rank + 1) * ksteps / split_k);
     const uint32_t nsteps = s_end - s_begin;
-    const uint64_t deadline = globaltimer_ns() + timeout_ns;
+    uint64_t deadline = globaltimer_ns() + timeout_ns;   // restarted by each role after the dependency wait
     const uint32_t my_row0 = owned_row0(rank, split_k);
     const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
     const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             uint32_t issued = npre;
+            if (npre < nsteps) deadline = deadline_after_dependency(timeout_ns);   // slots free after MMAs
             for (uint32_t i = npre; i < nsteps; ++i) {
                 const uint32_t s = i % STAGES, q = i - STAGES;   // slot s last held step q
                 if (!mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline, abort_flag,
@@ -335,7 +336,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         // -------------------------------------------- activation producer (TMA)
         if (lane == 0 && !direct_x) {
             const uint64_t pol_a = l2_policy_evict_last();
-            grid_dependency_wait();   // A may be written by the previous grid in the stream
+            // A may be written by the previous grid in the stream
+            deadline = deadline_after_dependency(timeout_ns);
             uint32_t issued = 0;
             for (uint32_t i = 0; i < nsteps; ++i) {
                 const uint32_t j = i % Cfg::SA;
@@ -360,6 +362,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             // completes: the splitters of step i wait for that before arriving.
             const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
             const uint64_t db0 = smem_desc_kmajor_sw128(smem_u32(sB));
+            if (!step_par) deadline = deadline_after_dependency(timeout_ns);   // the terms come after it
             for (uint32_t i = 0; i < (step_par ? 0u : nsteps); ++i) {
                 const uint32_t s = i % STAGES, b = i % Cfg::SB, p = i % Cfg::NP;
                 if (!mbar_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, &g_tc8_status,
@@ -397,10 +400,9 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             v[1] = toks_valid > 1 ? *reinterpret_cast<const uint2*>(src + lda) : make_uint2(0u, 0u);
         };
         uint2 xnext[2] = {make_uint2(0u, 0u), make_uint2(0u, 0u)};
-        if (direct_x) {
-            grid_dependency_wait();   // A may be written by the previous grid in the stream
-            if (i_first < nsteps) load_x(i_first, xnext);
-        }
+        // A may be written by the previous grid in the stream
+        deadline = deadline_after_dependency(timeout_ns);
+        if (direct_x && i_first < nsteps) load_x(i_first, xnext);
         for (uint32_t i = i_first; i < nsteps; i += di) {
             const uint32_t j = i % Cfg::SA, b = i % Cfg::SB, f = i % Cfg::NP;
             uint2 xcur[2] = {xnext[0], xnext[1]};
@@ -468,6 +470,7 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
         // programmatic launch the caller guarantees they are not being written.
         float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
         float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
+        deadline = deadline_after_dependency(timeout_ns);   // the products come after it
         for (uint32_t i = 0; i < nsteps; ++i) {
             if (i != 0 && (i & 31u) == 0) {
                 sc_cur = sc_next;

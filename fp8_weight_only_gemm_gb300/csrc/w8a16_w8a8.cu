@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     const uint32_t s_begin = rank * ksteps / split_k;
     const uint32_t s_end = (rank + 1) * ksteps / split_k;
     const uint32_t nsteps = s_end - s_begin;
-    const uint64_t deadline = globaltimer_ns() + timeout_ns;
+    uint64_t deadline = globaltimer_ns() + timeout_ns;   // restarted by each role after the dependency wait
     const uint32_t my_row0 = owned_row0(rank, split_k);
     const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
     const uint32_t npre = nsteps < STAGES ? nsteps : STAGES;
@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             uint32_t issued = npre;
+            if (npre < nsteps) deadline = deadline_after_dependency(timeout_ns);   // slots free after MMAs
             for (uint32_t i = npre; i < nsteps; ++i) {
                 const uint32_t s = i % STAGES, q = i - STAGES;   // slot s last held step q
                 if (!mbar_wait(mdone0 + 8u * (q % Cfg::ND), (q / Cfg::ND) & 1, deadline, abort_flag,
@@ -205,7 +206,8 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         // ------------------------------------ activation producer (TMA): codes
         if (lane == 0) {
             const uint64_t pol_a = l2_policy_evict_last();
-            grid_dependency_wait();   // the activations may be the previous grid's output
+            // the activations may be the previous grid's output
+            deadline = deadline_after_dependency(timeout_ns);
             uint32_t issued = 0;
             for (uint32_t i = 0; i < nsteps; ++i) {
                 const uint32_t j = i % Cfg::SA;
@@ -233,6 +235,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             constexpr uint32_t idesc = idesc_e4m3_f32(kTcRows, Cfg::NB);
             const uint64_t dw0 = smem_desc_kmajor_sw128(smem_u32(sW));   // + (offset >> 4)
             const uint64_t dx0 = smem_desc_kmajor_sw128(smem_u32(sX));
+            deadline = deadline_after_dependency(timeout_ns);   // the activations come after it
             for (uint32_t i = (warp == 1 ? 0u : 1u); i < nsteps; i += 2) {
                 const uint32_t s = i % STAGES, j = i % Cfg::SA, p = i % Cfg::NP;
                 if (!mbar_wait(wfull0 + 8u * s, (i / STAGES) & 1, deadline, abort_flag, &g_w8a8_status,
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             }
         };
         constexpr uint32_t kAhead = 4;
-        grid_dependency_wait();
+        deadline = deadline_after_dependency(timeout_ns);
         float fq[kAhead][Cfg::kFactorRegs];
 #pragma unroll
         for (uint32_t d = 0; d < kAhead; ++d) {

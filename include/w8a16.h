@@ -380,8 +380,10 @@ W8A16_API int w8a16_device_status(w8a16_stream_t stream, int clear, uint32_t *st
 
 /* Failure-path self-test: launches one CTA whose mbarrier wait can never complete
  * (nothing arrives on it) with a limit of `timeout_us` microseconds, so the kernel
- * must record W8A16_STATUS_WAIT_TIMEOUT and return. Used by the tests to show a
- * wait that runs out leaves the context usable. */
+ * must record W8A16_STATUS_WAIT_TIMEOUT (detail 0xFF) and return. It allows a
+ * programmatic dependent launch to start at once. Used by the tests to show a wait
+ * that runs out leaves the context usable, and that a call queued behind a long
+ * kernel with W8A16_FLAG_PDL does not charge that kernel's time to its own waits. */
 W8A16_API int w8a16_selftest_wait_timeout(uint32_t timeout_us, w8a16_stream_t stream);
 
 /* Library version string. */
