@@ -404,6 +404,7 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
         "path": ("activation quantiser + W8A8 GEMM" if w8a8 else
                  "w8a16_gemm_ws: split pre-pass + FP8 x FP8 GEMM on two terms" if presplit else
                  "w8a16_gemm_ws: one launch of the two-term FP8 kernel" if plan["variant"] == 3 else
+                 "w8a16_gemm_ws: one launch of the decode kernel" if plan["variant"] == 6 else
                  "w8a16_gemm_ws: one launch of the BF16 kernel"),
         "launches_per_step": launches_per_step,
         "plan": plan,
@@ -429,7 +430,8 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
             out["kernel"]["split_prepass_us"] = kt["split"]
             out["kernel"]["split_timing"] = f"{G} launches of split_act_kernel alone from a graph"
     else:
-        out["kernel"] = {"name": "w8a16_tc8_kernel" if plan["variant"] == 3 else "w8a16_tc_kernel",
+        out["kernel"] = {"name": {3: "w8a16_tc8_kernel", 6: "w8a16_gemv_kernel"}.get(plan["variant"],
+                                                                                       "w8a16_tc_kernel"),
                          "us": step_s * 1e6,
                          "bytes": bytes_step, "gbs": bytes_step / step_s / 1e9,
                          "frac_hbm": bytes_step / step_s / 1e9 / hbm,

@@ -18,7 +18,8 @@ HEADER = PKG.parent / "include" / "w8a16.h"
 # Values mirrored from include/w8a16.h (checked against the header by the tests).
 W8A16_OK = 0
 FLAG_PDL = 1
-VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8, VARIANT_PRESPLIT = 0, 1, 2, 3, 4, 5
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8, VARIANT_PRESPLIT, VARIANT_GEMV = (
+    0, 1, 2, 3, 4, 5, 6)
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
 WEIGHTS_F32, WEIGHTS_BF16 = 0, 1
 

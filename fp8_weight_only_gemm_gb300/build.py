@@ -23,7 +23,7 @@ BUILD = PKG / "_build"
 LIB = BUILD / "libw8a16.so"
 
 SOURCES = ["w8a16_api.cu", "w8a16_simt.cu", "w8a16_tc.cu", "w8a16_tc8.cu", "w8a16_w8a8.cu",
-           "w8a16_quant.cu"]
+           "w8a16_quant.cu", "w8a16_gemv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -112,25 +112,30 @@ bool is_tc_variant(int32_t v) {
            v == W8A16_VARIANT_PRESPLIT;
 }
 bool is_fp8_act_variant(int32_t v) { return v == W8A16_VARIANT_W8A8 || v == W8A16_VARIANT_PRESPLIT; }
+bool is_gemv(int32_t v) { return v == W8A16_VARIANT_GEMV; }
 uint32_t v_terms(int32_t v) { return v == W8A16_VARIANT_PRESPLIT ? 2u : 1u; }
 uint32_t max_token_tile(int32_t v) { return v == W8A16_VARIANT_TC8 ? 64u : 128u; }
 uint32_t v_threads(int32_t v, uint32_t tn) {
-    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_threads(tn)
+    return is_gemv(v)                ? w8a16::kGvThreads
+           : v == W8A16_VARIANT_TC8   ? w8a16::tc8_threads(tn)
            : is_fp8_act_variant(v) ? w8a16::w8a8_threads(tn, v_terms(v))
                                    : w8a16::tc_threads(tn);
 }
 uint32_t v_smem(int32_t v, uint32_t tn, uint32_t st, uint32_t split) {
-    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_smem_bytes(tn, st, split)
+    return is_gemv(v)                ? w8a16::gemv_smem_bytes()
+           : v == W8A16_VARIANT_TC8   ? w8a16::tc8_smem_bytes(tn, st, split)
            : is_fp8_act_variant(v) ? w8a16::w8a8_smem_bytes(tn, st, split, v_terms(v))
                                    : w8a16::tc_smem_bytes(tn, st, split);
 }
 uint32_t v_tmem(int32_t v, uint32_t tn) {
-    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_tmem_cols(tn)
+    return is_gemv(v)                ? w8a16::kGvTmemCols
+           : v == W8A16_VARIANT_TC8   ? w8a16::tc8_tmem_cols(tn)
            : is_fp8_act_variant(v) ? w8a16::w8a8_tmem_cols(tn, v_terms(v))
                                    : w8a16::tc_tmem_cols(tn);
 }
 bool v_supported(int32_t v, uint32_t tn, uint32_t st) {
-    return v == W8A16_VARIANT_TC8   ? w8a16::tc8_supported_stages(tn, st)
+    return is_gemv(v)                ? (tn == w8a16::kGvMaxTokens && st == w8a16::kGvSlots)
+           : v == W8A16_VARIANT_TC8   ? w8a16::tc8_supported_stages(tn, st)
            : is_fp8_act_variant(v) ? w8a16::w8a8_supported_stages(tn, st, v_terms(v))
                                    : w8a16::tc_supported_stages(tn, st);
 }
@@ -190,6 +195,45 @@ void fill_simt(uint32_t M, uint32_t N, w8a16_plan_t* p) {
     p->block[0] = 256;
     p->block[1] = p->block[2] = 1;
     p->cluster[0] = p->cluster[1] = p->cluster[2] = 1;
+}
+
+// Decode kernel plan: a cluster of `split` CTAs per 128-row weight tile, one token
+// tile of up to kGvMaxTokens tokens.
+void fill_gemv(uint32_t N, uint32_t split, w8a16_plan_t* p) {
+    std::memset(p, 0, sizeof *p);
+    p->variant = W8A16_VARIANT_GEMV;
+    p->token_tile = w8a16::kGvMaxTokens;
+    p->split_k = split;
+    p->stages = w8a16::kGvSlots;
+    p->ctas_per_sm = tc_ctas_per_sm(W8A16_VARIANT_GEMV, w8a16::kGvMaxTokens, w8a16::kGvSlots, split);
+    p->grid[0] = ceil_div(N, w8a16::kTcRows) * split;
+    p->grid[1] = p->grid[2] = 1;
+    p->block[0] = w8a16::kGvThreads;
+    p->block[1] = p->block[2] = 1;
+    p->cluster[0] = split;
+    p->cluster[1] = p->cluster[2] = 1;
+    p->smem_bytes = w8a16::gemv_smem_bytes();
+    p->tmem_cols = w8a16::kGvTmemCols;
+}
+
+// Whether a decode-kernel split can run (N, K): each CTA on at most kGvMaxSteps K
+// steps, and no more CTAs than SMs, so the next call's CTAs fit beside them.
+bool gemv_split_ok(uint32_t N, uint32_t K, uint32_t split, uint32_t sm_count) {
+    const uint32_t ksteps = K / w8a16::kKStep;
+    const uint32_t sms = sm_count ? sm_count : 152u;
+    return split >= 1 && split <= 16 && split <= ksteps && ceil_div(ksteps, split) <= w8a16::kGvMaxSteps &&
+           static_cast<uint64_t>(ceil_div(N, w8a16::kTcRows)) * split <= sms;
+}
+
+// The decode kernel's split for (M, N, K), or 0 where it does not apply: the
+// largest split whose clusters stay portable (<= 8 CTAs) and fit the rule above
+// (more CTAs stream the weights from more SMs and leave each fewer steps after
+// the dependency wait); cap[s] (NULL: assume it runs) = 0 rules cluster size s out.
+uint32_t gemv_split(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, const uint32_t* cap) {
+    if (M < 1 || M > w8a16::kGvMaxTokens) return 0;
+    for (uint32_t s = 8; s >= 1; --s)
+        if (gemv_split_ok(N, K, s, sm_count) && (!cap || cap[s] != 0)) return s;
+    return 0;
 }
 
 // Choose the split-K factor by a load model: a CTA's time is its share of K
@@ -258,6 +302,20 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
     if (p.variant == W8A16_VARIANT_SIMT) {
         if (p.grid[0] != ceil_div(N, 8) || p.grid[1] != ceil_div(M, 8) || p.block[0] != 256)
             return fail(W8A16_ERR_PLAN, "SIMT plan does not match the shape");
+        return W8A16_OK;
+    }
+    if (is_gemv(p.variant)) {
+        if (M > w8a16::kGvMaxTokens)
+            return fail(W8A16_ERR_PLAN, "decode plan: M=" + u(M) + " is above " + u(w8a16::kGvMaxTokens));
+        if (p.split_k < 1 || p.split_k > 16 || p.split_k > ksteps ||
+            ceil_div(ksteps, p.split_k) > w8a16::kGvMaxSteps)
+            return fail(W8A16_ERR_PLAN, "decode plan: split_k=" + u(p.split_k) + " must be in 1..min(16, K/128) "
+                                        "with at most " + u(w8a16::kGvMaxSteps) + " K steps per CTA");
+        w8a16_plan_t ref;
+        fill_gemv(N, p.split_k, &ref);
+        if (p.grid[0] != ref.grid[0] || p.grid[1] != 1 || p.cluster[0] != p.split_k ||
+            p.token_tile != ref.token_tile || p.stages != ref.stages || p.tail_tiles || p.tail_split)
+            return fail(W8A16_ERR_PLAN, "decode plan does not match the shape");
         return W8A16_OK;
     }
     if (!is_tc_variant(p.variant))
@@ -390,6 +448,14 @@ void add_tail(w8a16_plan_t* p, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_c
 // fills every SM slot). The W8A8 variant has its own model (choose_w8a8).
 int plan_core(int32_t v, uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count,
               const uint32_t* cap, w8a16_plan_t* out) {
+    if (v == W8A16_VARIANT_AUTO || is_gemv(v)) {
+        const uint32_t gs = gemv_split(M, N, K, sm_count, nullptr);
+        if (gs) {
+            fill_gemv(N, gs, out);
+            return W8A16_OK;
+        }
+        if (is_gemv(v)) return W8A16_ERR_PLAN;
+    }
     if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
     if (is_fp8_act_variant(v)) {
         const uint32_t tn = token_tile_for(v, M);
@@ -443,7 +509,8 @@ int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::s
     }
     Entry e{dev, v, tn, stages, {0}};
     for (uint32_t c = 1; c <= 16; ++c) {
-        int rc = v == W8A16_VARIANT_TC8    ? w8a16::tc8_cluster_capacity(tn, stages, c, &e.cap[c], err)
+        int rc = is_gemv(v)                ? w8a16::gemv_cluster_capacity(c, &e.cap[c], err)
+                 : v == W8A16_VARIANT_TC8    ? w8a16::tc8_cluster_capacity(tn, stages, c, &e.cap[c], err)
                  : is_fp8_act_variant(v)   ? w8a16::w8a8_cluster_capacity(tn, stages, v_terms(v), c, &e.cap[c], err)
                                            : w8a16::tc_cluster_capacity(tn, stages, c, &e.cap[c], err);
         if (rc) return rc;
@@ -460,6 +527,16 @@ int live_capacity(int32_t v, uint32_t tn, uint32_t stages, uint32_t* cap, std::s
 // their CTAs at once).
 int plan_live(int32_t v, uint32_t M, uint32_t N, uint32_t K, const DeviceInfo& info, w8a16_plan_t* out,
               std::string* err) {
+    if (v == W8A16_VARIANT_AUTO && gemv_split(M, N, K, static_cast<uint32_t>(info.sm_count), nullptr)) {
+        uint32_t cap[17];
+        const int rc = live_capacity(W8A16_VARIANT_GEMV, w8a16::kGvMaxTokens, w8a16::kGvSlots, cap, err);
+        if (rc) return rc;
+        const uint32_t gs = gemv_split(M, N, K, static_cast<uint32_t>(info.sm_count), cap);
+        if (gs) {
+            fill_gemv(N, gs, out);
+            return W8A16_OK;
+        }
+    }
     if (v == W8A16_VARIANT_AUTO) v = auto_variant(M);
     const uint32_t tn = token_tile_for(v, M);
     if (is_fp8_act_variant(v)) {
@@ -522,6 +599,8 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
     }
     if (plan.variant == W8A16_VARIANT_SIMT)
         rc = w8a16::launch_simt(g, plan, stream, flags, &err);
+    else if (is_gemv(plan.variant))
+        rc = w8a16::launch_gemv(g, plan, stream, ts.ns, flags, &err);
     else if (plan.variant == W8A16_VARIANT_TC8)
         rc = w8a16::launch_tc8(g, plan, stream, ts.ns, flags, &err);
     else
@@ -890,7 +969,7 @@ int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t* out) {
 int w8a16_cluster_capacity(int32_t variant, uint32_t token_tile, uint32_t stages,
                            uint32_t out[17]) {
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_cluster_capacity: NULL output");
-    if (!is_tc_variant(variant) || !v_supported(variant, token_tile, stages))
+    if (!(is_tc_variant(variant) || is_gemv(variant)) || !v_supported(variant, token_tile, stages))
         return fail(W8A16_ERR_PLAN, "w8a16_cluster_capacity: no kernel instance for variant " +
                                         std::to_string(variant) + " token_tile=" + u(token_tile) +
                                         " stages=" + u(stages));
@@ -913,6 +992,13 @@ int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint
         plan_core(W8A16_VARIANT_AUTO, M, N, K, sm_count, nullptr, &p);
     } else if (variant == W8A16_VARIANT_SIMT) {
         fill_simt(M, N, &p);
+    } else if (is_gemv(variant)) {
+        const uint32_t sp = split_k ? split_k : gemv_split(M, N, K, sm_count, nullptr);
+        if (sp == 0 || M > w8a16::kGvMaxTokens || (stages && stages != w8a16::kGvSlots))
+            return fail(W8A16_ERR_PLAN, "w8a16_plan_variant: the decode kernel takes M <= " +
+                                            u(w8a16::kGvMaxTokens) + " and at most " + u(w8a16::kGvMaxSteps) +
+                                            " K steps per CTA on at most one CTA per SM");
+        fill_gemv(N, sp, &p);
     } else if (is_tc_variant(variant)) {
         w8a16_plan_t a;
         plan_core(variant, M, N, K, sm_count, nullptr, &a);
@@ -1016,14 +1102,17 @@ const char* w8a16_strerror(int code) {
 
 int w8a16_device_status(w8a16_stream_t stream, int clear, uint32_t* status, uint32_t* where,
                         uint32_t* detail) {
-    w8a16::StatusWord w{0, 0, 0}, w8{0, 0, 0}, wa{0, 0, 0};
+    w8a16::StatusWord w{0, 0, 0}, w8{0, 0, 0}, wa{0, 0, 0}, wg{0, 0, 0};
     cudaError_t e = w8a16::tc_status_read(&w, clear != 0, reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaSuccess)
         e = w8a16::tc8_status_read(&w8, clear != 0, reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaSuccess)
         e = w8a16::w8a8_status_read(&wa, clear != 0, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess)
+        e = w8a16::gemv_status_read(&wg, clear != 0, reinterpret_cast<cudaStream_t>(stream));
     if (w.code == 0) w = w8;
     if (w.code == 0) w = wa;
+    if (w.code == 0) w = wg;
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(W8A16_ERR_DEVICE, std::string("w8a16_device_status: ") + cudaGetErrorString(e));

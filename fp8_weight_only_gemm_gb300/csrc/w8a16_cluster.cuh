@@ -59,6 +59,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
     return (1u << 4) | (0u << 7) | (0u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
+// The same product with A (the weight rows) read from TMEM: lane r holds row r, and
+// column c of a K=32 slab holds its K bytes 4c..4c+3 (byte j = element 4c+j).
+__device__ __forceinline__ void tc_mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, uint32_t accumulate) {
     asm volatile(

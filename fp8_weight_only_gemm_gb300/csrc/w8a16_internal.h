@@ -165,6 +165,26 @@ constexpr uint32_t w8a8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split,
                                                                                      : tc_red_bytes(tn, split))),
         w8a8_tmem_cols(tn, terms));
 }
+// Decode kernel (W8A16_VARIANT_GEMV): one or two tokens; a cluster of split_k CTAs
+// per 128-row weight tile, each on at most kGvMaxSteps 128-K steps, all of which
+// are on chip before the grid-dependency wait: kGvSlots shared-memory slots, and
+// the first kGvResident steps moved to TMEM to free theirs. Per CTA: 256 threads,
+// < 113 KiB of shared memory and 128 TMEM columns (two CTAs per SM, so a call's
+// CTAs fit beside the previous call's).
+constexpr uint32_t kGvSlots = 5;
+constexpr uint32_t kGvMaxSteps = 8;
+constexpr uint32_t kGvResident = kGvMaxSteps - kGvSlots;
+constexpr uint32_t kGvThreads = 256;
+constexpr uint32_t kGvTmemCols = 128;          // kGvResident x 32 weight columns + 2 x 16 accumulators
+constexpr uint32_t kGvMaxTokens = 2;
+constexpr uint32_t kGvBStepBytes = 16u * kKStep;   // MMA B operand of one step: 16 rows x 128 K
+constexpr uint32_t kGvRedBytes = 2304;         // >= split x ceil(128 / split) x 16 B for split <= 16
+constexpr uint32_t gemv_smem_bytes() {
+    return 1024u + kGvSlots * kTcRows * kKStep + kGvMaxSteps * kGvBStepBytes + kGvMaxSteps * kGvMaxTokens * 4u +
+           kGvRedBytes + 256u;
+}
+static_assert(2u * (gemv_smem_bytes() + 1024u) <= 233472u, "two decode CTAs per SM");
+
 // Workspace of the two-term split: codes [2M][K] (hi rows, then lo rows) and
 // factors [K/128][round_up(M, 4)] FP32.
 constexpr uint64_t split_ws_scale_stride(uint32_t M) { return (static_cast<uint64_t>(M) + 3u) / 4u * 4u; }
@@ -205,6 +225,10 @@ int tc8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t cluster, uint32_
                          std::string* err);
 bool tc8_supported_stages(uint32_t tn, uint32_t stages);
 int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, std::string* err);
+int launch_gemv(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+                uint32_t flags, std::string* err);
+int gemv_cluster_capacity(uint32_t cluster, uint32_t* ctas, std::string* err);
+cudaError_t gemv_status_read(StatusWord* out, bool clear, cudaStream_t s);
 
 // TMA descriptors of W ([N][K] E4M3, 128x128 boxes) and A ([M][K] BF16 at the
 // caller's pitch, 64 x token_tile boxes), 128-byte swizzle; cached per device.

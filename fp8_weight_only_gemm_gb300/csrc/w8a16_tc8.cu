@@ -490,10 +490,17 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                 tmem_ld_32x32b_x16(pcol + c, vh);
                 tmem_ld_32x32b_x16(pcol + TN + c, vl);
                 tc_wait_ld();
+                // two tokens per packed FP32 instruction, each with the arithmetic of
+                // acc = fmaf(sc, fmaf(lo, 1/32, hi) * f, acc)
+                const uint64_t sc2 = pack_f32x2(sc, sc), k32 = pack_f32x2(0.03125f, 0.03125f);
 #pragma unroll
-                for (uint32_t t = 0; t < 16; ++t) {
-                    const float pt = fmaf(vl[t], 0.03125f, vh[t]) * inv[c + t];
-                    acc[c + t] = fmaf(sc, pt, acc[c + t]);
+                for (uint32_t t = 0; t < 16; t += 2) {
+                    const float2 f = *reinterpret_cast<const float2*>(inv + c + t);
+                    const uint64_t pt = fma_f32x2(pack_f32x2(vl[t], vl[t + 1]), k32, pack_f32x2(vh[t], vh[t + 1]));
+                    const float2 a = unpack_f32x2(fma_f32x2(sc2, mul_f32x2(pt, pack_f32x2(f.x, f.y)),
+                                                            pack_f32x2(acc[c + t], acc[c + t + 1])));
+                    acc[c + t] = a.x;
+                    acc[c + t + 1] = a.y;
                 }
             }
             tc_fence_before();

@@ -324,17 +324,35 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
                 float v[16];
                 tmem_ld_32x32b_x16(pcol + c, v);
+                // two tokens per packed FP32 instruction, the arithmetic of
+                // acc = fmaf(sw, fmaf(lo, 1/32, hi) * f, acc) (two terms) or
+                // acc = fmaf(sw * f, P, acc) (one term) on each
+                const uint64_t sw2 = pack_f32x2(sw, sw);
                 if (TERMS == 2) {
                     float vl[16];
                     tmem_ld_32x32b_x16(pcol + TN + c, vl);
                     tc_wait_ld();
+                    const uint64_t k32 = pack_f32x2(0.03125f, 0.03125f);
 #pragma unroll
-                    for (uint32_t t = 0; t < 16; ++t)
-                        acc[c + t] = fmaf(sw, fmaf(vl[t], 0.03125f, v[t]) * fbuf[c + t], acc[c + t]);
+                    for (uint32_t t = 0; t < 16; t += 2) {
+                        const float2 f = *reinterpret_cast<const float2*>(fbuf + c + t);
+                        const uint64_t pt = fma_f32x2(pack_f32x2(vl[t], vl[t + 1]), k32, pack_f32x2(v[t], v[t + 1]));
+                        const float2 a = unpack_f32x2(fma_f32x2(sw2, mul_f32x2(pt, pack_f32x2(f.x, f.y)),
+                                                                pack_f32x2(acc[c + t], acc[c + t + 1])));
+                        acc[c + t] = a.x;
+                        acc[c + t + 1] = a.y;
+                    }
                 } else {
                     tc_wait_ld();
 #pragma unroll
-                    for (uint32_t t = 0; t < 16; ++t) acc[c + t] = fmaf(sw * fbuf[c + t], v[t], acc[c + t]);
+                    for (uint32_t t = 0; t < 16; t += 2) {
+                        const float2 f = *reinterpret_cast<const float2*>(fbuf + c + t);
+                        const float2 a = unpack_f32x2(fma_f32x2(mul_f32x2(sw2, pack_f32x2(f.x, f.y)),
+                                                                pack_f32x2(v[t], v[t + 1]),
+                                                                pack_f32x2(acc[c + t], acc[c + t + 1])));
+                        acc[c + t] = a.x;
+                        acc[c + t + 1] = a.y;
+                    }
                 }
             }
             tc_fence_before();

@@ -102,11 +102,17 @@ enum {
                                 non-finite activation makes its token's outputs NaN */,
     W8A16_VARIANT_W8A8 = 4,  /* the W8A8 kernel (w8a16_gemm_w8a8 only): FP8 activations with
                                 per-token 128-K group scales, one kind::f8f6f4 MMA per 32 K */
-    W8A16_VARIANT_PRESPLIT = 5 /* w8a16_gemm_ws only: the activations are split into the
+    W8A16_VARIANT_PRESPLIT = 5, /* w8a16_gemm_ws only: the activations are split into the
                                 two E4M3 terms of W8A16_VARIANT_TC8 once per call, by a
                                 pre-pass into the caller's workspace, and the W8A8 kernel
                                 multiplies both terms in one MMA of N = 2 x token tile;
                                 same accuracy as W8A16_VARIANT_TC8 */
+    W8A16_VARIANT_GEMV = 6     /* decode kernel for M <= 2: the arithmetic of
+                                W8A16_VARIANT_TC8; a cluster of split_k CTAs per 128-row
+                                weight tile, each on at most 8 K steps, every one of them
+                                loaded before the grid-dependency wait (shared memory and
+                                TMEM), at most one CTA per SM; the planner's choice for
+                                M <= 2 when ceil(N/128) x ceil(K/1024) CTAs fit that rule */
 };
 
 /*

@@ -97,8 +97,8 @@ def test_c_client_through_the_abi(tmp_path):
     assert out["msg"].startswith("-2 ") and "K=100" in out["msg"] and "128" in out["msg"]
     assert "multiple of 128" in out["str"]
     rc, variant, tn, split, stages, g0, g1, cl = map(int, out["plan"].split())
-    assert rc == 0 and variant == 3 and tn == 16 and g1 == 1       # two-term FP8 kernel, one token tile
-    assert g0 == 32 * split and cl == split and 1 <= split <= 16 and stages >= 2
+    assert rc == 0 and variant == 6 and tn == 2 and g1 == 1        # the decode kernel, one token tile
+    assert g0 == 32 * split and cl == split and split == 4 and stages == 5   # 8 K steps per CTA
     ws_32, ws_bad = map(int, out["ws"].split())
     assert ws_32 == 2 * 32 * 5120 + 4 * 40 * 32 and ws_bad == 0
     assert int(out["scratch"]) == 32 << 20

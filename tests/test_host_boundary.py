@@ -96,12 +96,16 @@ def test_strerror_covers_codes(lib):
     assert binding.strerror(-999) == "unknown error code"
 
 
-@pytest.mark.parametrize("M,N,K,tn", [(1, 256, 256, 16), (1, 4096, 4096, 16), (8, 12288, 4096, 16),
+@pytest.mark.parametrize("M,N,K,tn", [(1, 256, 256, 2), (1, 4096, 4096, 2), (8, 12288, 4096, 16),
                                       (32, 14336, 5120, 32), (128, 28672, 8192, 128),
-                                      (17, 1000, 1024, 32), (64, 512, 512, 64), (300, 512, 512, 128)])
+                                      (17, 1000, 1024, 32), (64, 512, 512, 64), (300, 512, 512, 128),
+                                      (2, 4096, 4096, 2), (1, 14336, 4096, 16), (3, 4096, 4096, 16)])
 def test_plans_for_the_workloads(lib, M, N, K, tn):
     p = binding.plan_for(M, N, K, sm_count=152)
-    assert p["variant"] == (binding.VARIANT_TC8 if M <= 16 else binding.VARIANT_TC)
+    if tn == 2:
+        assert p["variant"] == binding.VARIANT_GEMV
+    else:
+        assert p["variant"] == (binding.VARIANT_TC8 if M <= 16 else binding.VARIANT_TC)
     assert p["token_tile"] == tn
     ksteps = K // 128
     assert 1 <= p["split_k"] <= min(16, ksteps)
@@ -114,6 +118,8 @@ def test_plans_for_the_workloads(lib, M, N, K, tn):
     assert p["cluster"][0] == p["split_k"]
     if p["variant"] == binding.VARIANT_TC8:
         assert p["block"][0] == 352
+    elif p["variant"] == binding.VARIANT_GEMV:
+        assert p["block"][0] == 256 and -(-ksteps // p["split_k"]) <= 8 and p["grid"][0] <= 152
     else:
         assert p["block"][0] == (768 if tn <= 32 else 640)
     assert p["tmem_cols"] * p["ctas_per_sm"] <= 512
@@ -133,13 +139,13 @@ def test_planner_uses_cluster_capacity(lib):
     # clusters fill 2 CTAs per SM: the 32-tile decode GEMV must not be split 8
     # ways (three waves of clusters); it picks a split whose clusters fit at once.
     cap = [0] + [304] * 4 + [300, 300, 294, 120] + [0] * 8
-    p = binding.plan_for(1, 4096, 4096, sm_count=152, cluster_ctas=cap)
+    p = binding.plan_for(3, 4096, 4096, sm_count=152, cluster_ctas=cap)   # 3 tokens: the two-term kernel
     s = p["split_k"]
     assert 32 * s <= cap[s], p
     assert s >= 4
     # a cluster size the device cannot run is never chosen
     cap2 = [0, 304, 0, 0, 0, 0, 0, 0, 0] + [0] * 8
-    assert binding.plan_for(1, 4096, 4096, sm_count=152, cluster_ctas=cap2)["split_k"] == 1
+    assert binding.plan_for(3, 4096, 4096, sm_count=152, cluster_ctas=cap2)["split_k"] == 1
 
 
 def test_plan_variant_validation(lib):
@@ -400,3 +406,23 @@ def test_binding_quantisers_refuse_host_tensors(lib):
         binding.quantize_weights(torch.zeros((128, 256), dtype=torch.float16))
     with pytest.raises(ValueError, match="CUDA bfloat16"):
         binding.quantize_activations(torch.zeros((4, 256), dtype=torch.bfloat16))
+
+
+def test_decode_kernel_plans(lib):
+    """The decode kernel (M <= 2): at most 8 K steps per CTA, at most one CTA per SM
+    in all, the largest portable split that satisfies both; otherwise the two-term
+    kernel. Forced decode plans are validated against the shape."""
+    for (M, N, K, split) in [(1, 4096, 4096, 4), (2, 4096, 4096, 4), (1, 256, 256, 2), (1, 2048, 4096, 8),
+                             (1, 4096, 1024, 4), (2, 130, 640, 5), (1, 19 * 128, 8192, 8)]:
+        p = binding.plan_variant(M, N, K, 0, 0, 0, 152).as_dict()
+        assert p["variant"] == binding.VARIANT_GEMV and p["split_k"] == split, (M, N, K, p)
+        assert p["grid"][0] == -(-N // 128) * split <= 152 and p["cluster"][0] == split
+        assert p["ctas_per_sm"] == 2 and p["tmem_cols"] == 128 and p["block"][0] == 256
+    for (M, N, K) in [(1, 4096, 8192), (1, 14336, 4096), (3, 4096, 4096), (1, 20 * 128, 8192)]:
+        assert binding.plan_variant(M, N, K, 0, 0, 0, 152).variant != binding.VARIANT_GEMV, (M, N, K)
+    q = binding.plan_variant(1, 4096, 4096, binding.VARIANT_GEMV, 8, 0, 152)
+    assert q.split_k == 8 and q.grid[0] == 256          # forced: more CTAs than SMs is allowed
+    for bad in [dict(M=3), dict(split=2), dict(split=17), dict(stages=4)]:
+        with pytest.raises(binding.W8A16Error):
+            binding.plan_variant(bad.get("M", 1), 4096, 4096, binding.VARIANT_GEMV, bad.get("split", 4),
+                                 bad.get("stages", 0), 152)
