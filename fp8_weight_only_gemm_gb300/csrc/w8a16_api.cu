@@ -670,32 +670,22 @@ int run_ws(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, void* ws, uint6
 }
 
 // Scratch of the allocation-free entry point: a fixed device array in this
-// module, so a call allocates nothing; its address is looked up once per device.
-// Calls that overlap in time (other streams, other host threads) share it and race.
+// module, so a call allocates nothing. Its device address is looked up on every
+// call (cudaGetSymbolAddress allocates nothing), so it stays right after a device
+// reset or under another context, where the module is loaded anew. Calls that
+// overlap in time (other streams, other host threads) share it and race.
 constexpr uint64_t kNoAllocScratchBytes = 32ull << 20;
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 int noalloc_scratch(void** out, std::string* err) {
-    static std::mutex mu;
-    static void* addr[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    void* addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (e != cudaSuccess || addr == nullptr) {
         cudaGetLastError();
-        *err = "no usable CUDA device for the scratch buffer";
+        *err = std::string("scratch buffer address: ") + cudaGetErrorString(e);
         return W8A16_ERR_DEVICE;
     }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            addr[dev] = nullptr;
-            *err = std::string("scratch buffer address: ") + cudaGetErrorString(e);
-            return W8A16_ERR_DEVICE;
-        }
-    }
-    *out = addr[dev];
+    *out = addr;
     return W8A16_OK;
 }
 

@@ -253,7 +253,8 @@ W8A16_API int w8a16_gemm_ws(const void *A, uint32_t a_row_stride, const void *W,
 /* The product without a caller's workspace and without any allocation (the paper
  * has no counterpart): w8a16_gemm_ws on a fixed 32 MiB device buffer that is part of
  * the library's module (w8a16_noalloc_scratch_bytes() bytes), whose address is
- * looked up once per device. Same arguments, checks and results as w8a16_gemm_ws
+ * looked up on the current device at each call (so a device reset does not leave
+ * a stale address behind). Same arguments, checks and results as w8a16_gemm_ws
  * with plan = NULL; M <= 16 uses no scratch. W8A16_ERR_RANGE when M > 16 and
  * w8a16_workspace_bytes(M, K) exceeds the buffer. Every value the kernels read
  * from the buffer is written earlier in the same call, so nothing needs clearing.
