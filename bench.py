@@ -47,6 +47,7 @@ reference implementation) on the same workload and metric.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import dataclasses
 import hashlib
 import json
@@ -304,12 +305,15 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
     del A0, W0, S0, C0
     w8a8 = args.path == "w8a8"
     qsets = [w8.quantize_activations(A[:, :wl.K]) for (A, _, _, _) in sets] if w8a8 else None
-    presplit = not w8a8 and wl.M > 16
-    wsb = max(16, w8.workspace_bytes(wl.M, wl.K))
-    wss = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(nsets)] if not w8a8 else None
+    # a workspace every plan fits in; the workspace path's own choice for it, or
+    # (--stream-k, 3..32 tokens) the forced persistent stream-K plan
+    wsb = max(16, w8.workspace_bytes_for(wl.M, wl.N, wl.K), w8.workspace_bytes(wl.M, wl.K))
+    wss = [torch.zeros(wsb, dtype=torch.uint8, device=dev) for _ in range(nsets)] if not w8a8 else None
+    stream_k = not w8a8 and args.stream_k and 3 <= wl.M <= 32
+    forced = w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_STREAM, 0, 0, sms) if stream_k else None
     plan = (w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_W8A8, 0, 0, sms).as_dict() if w8a8 else
-            w8.plan_variant(wl.M, wl.N, wl.K, w8.VARIANT_PRESPLIT, 0, 0, sms).as_dict() if presplit else
-            w8.plan_current(wl.M, wl.N, wl.K))
+            forced.as_dict() if stream_k else w8.plan_ws(wl.M, wl.N, wl.K, wsb))
+    presplit = not w8a8 and plan["variant"] in (w8.VARIANT_PRESPLIT, w8.VARIANT_STREAM)
     gemm_launches = 2 if plan.get("tail_tiles") else 1
     launches_per_step = (1 if (w8a8 or presplit) else 0) + gemm_launches
 
@@ -346,14 +350,15 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
             return
         ws_ = wss[i % nsets]
         ck(lib.w8a16_gemm_ws(A.data_ptr(), A.stride(0), W.data_ptr(), S.data_ptr(), C.data_ptr(),
-                             C.stride(0), wl.M, wl.N, wl.K, None, ws_.data_ptr(), ws_.numel(), fl, sh))
+                             C.stride(0), wl.M, wl.N, wl.K, ctypes.byref(forced) if forced is not None else None,
+                             ws_.data_ptr(), ws_.numel(), fl, sh))
 
     # ---- graphs: a region of exactly K steps = q replays of G steps + r steps
     G, q, r = graph_split(K, nsets)
     with torch.cuda.stream(stream):
         for i in range(min(G, 2 * nsets)):   # the launch path and the planner's caches, outside capture
             call(i)
-        if presplit:                          # the kernel-only entry points too (set 0 holds a split)
+        if presplit and not stream_k:         # the kernel-only entry points too (set 0 holds a split)
             split_only(0)
             terms_only(0)
         elif w8a8:
@@ -364,7 +369,7 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
     region = [full] * q + ([rest] if rest else [])
     # kernel-only graphs of the dominant kernel (and of the pre-pass)
     kgraphs = {}
-    if presplit:
+    if presplit and not stream_k:   # (the stream-K kernel has no kernel-only entry point)
         kgraphs["gemm"] = runner.capture(terms_only, G)
         kgraphs["split"] = runner.capture(split_only, G)
     elif w8a8:
@@ -402,6 +407,8 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
         "frac_hbm": bytes_step / step_s / 1e9 / hbm,
         "roofline_bytes": bytes_step,
         "path": ("activation quantiser + W8A8 GEMM" if w8a8 else
+                 "w8a16_gemm_ws: split pre-pass + FP8 x FP8 GEMM on two terms, persistent stream-K grid"
+                 if stream_k else
                  "w8a16_gemm_ws: split pre-pass + FP8 x FP8 GEMM on two terms" if presplit else
                  "w8a16_gemm_ws: one launch of the two-term FP8 kernel" if plan["variant"] == 3 else
                  "w8a16_gemm_ws: one launch of the decode kernel" if plan["variant"] == 6 else
@@ -429,6 +436,11 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
         if presplit:
             out["kernel"]["split_prepass_us"] = kt["split"]
             out["kernel"]["split_timing"] = f"{G} launches of split_act_kernel alone from a graph"
+    elif stream_k:
+        out["kernel"] = {"name": "split_act_kernel + w8a16_w8a8_kernel (terms 2, stream-K)",
+                         "us": step_s * 1e6, "bytes": bytes_step, "gbs": bytes_step / step_s / 1e9,
+                         "frac_hbm": bytes_step / step_s / 1e9 / hbm,
+                         "timing": "the step: the split pre-pass and the stream-K kernel"}
     else:
         out["kernel"] = {"name": {3: "w8a16_tc8_kernel", 6: "w8a16_gemv_kernel"}.get(plan["variant"],
                                                                                        "w8a16_tc_kernel"),
@@ -437,7 +449,7 @@ def measure_workload(name, wl, args, ctx, K: int, headline: bool):
                          "frac_hbm": bytes_step / step_s / 1e9 / hbm,
                          "timing": "the step is this kernel's launch" +
                                    ("es (whole tiles + split-K tail)" if gemm_launches > 1 else " alone")}
-    traffic_key = name + ("/w8a8" if w8a8 else "/presplit" if presplit else "")
+    traffic_key = name + ("/w8a8" if w8a8 else "/stream" if stream_k else "/presplit" if presplit else "")
     out["kernel"]["traffic"] = recorded_traffic(traffic_key)
     out["gpu_launches_timed"] = len(times) * K * launches_per_step
 
@@ -661,6 +673,9 @@ def main():
     ap.add_argument("--config-seconds", type=float, default=0.5,
                     help="GPU time spent in each other workload's timed regions")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stream-k", action="store_true",
+                    help="force the persistent stream-K plan on the 3..32-token workloads (never the "
+                         "planner's choice: slower on GB300)")
     ap.add_argument("--path", choices=["w8a16", "w8a8"], default="w8a16",
                     help="w8a8: activation quantiser + W8A8 GEMM per step")
     ap.add_argument("--pdl", choices=["on", "off"], default="on",

@@ -10,8 +10,8 @@ from .binding import (FLAG_PDL, Plan, VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VA
                       VARIANT_PRESPLIT, WEIGHTS_BF16, WEIGHTS_F32, W8A16Error,
                       check_args, cluster_capacity, device_status, gemm, gemm_host, gemm_noalloc, gemm_ptr,
                       gemm_split_terms, gemm_w8a8, gemm_w8a8_ptr, gemm_ws, gemm_ws_ptr, quantize_activations,
-                      split_activations, workspace_bytes,
-                      header_functions, last_error, load, plan_current, plan_for, plan_variant,
+                      split_activations, workspace_bytes, workspace_bytes_for, VARIANT_GEMV, VARIANT_STREAM,
+                      header_functions, last_error, load, plan_current, plan_for, plan_variant, plan_ws,
                       quantize_weights, quantize_weights_ptr, selftest_wait_timeout, strerror,
                       version)
 
@@ -19,7 +19,7 @@ __all__ = ["FLAG_PDL", "Plan", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_TC", "VA
            "VARIANT_PRESPLIT", "WEIGHTS_BF16", "WEIGHTS_F32", "W8A16Error",
            "check_args", "cluster_capacity", "device_status", "gemm", "gemm_host", "gemm_noalloc", "gemm_ptr",
            "gemm_split_terms", "gemm_w8a8", "gemm_w8a8_ptr", "gemm_ws", "gemm_ws_ptr", "quantize_activations",
-           "split_activations", "workspace_bytes",
-           "header_functions", "last_error", "load", "plan_current", "plan_for", "plan_variant",
+           "split_activations", "workspace_bytes", "workspace_bytes_for", "VARIANT_GEMV", "VARIANT_STREAM",
+           "header_functions", "last_error", "load", "plan_current", "plan_for", "plan_variant", "plan_ws",
            "quantize_weights", "quantize_weights_ptr", "selftest_wait_timeout", "strerror",
            "version"]

@@ -20,6 +20,7 @@ W8A16_OK = 0
 FLAG_PDL = 1
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_TC, VARIANT_TC8, VARIANT_W8A8, VARIANT_PRESPLIT, VARIANT_GEMV = (
     0, 1, 2, 3, 4, 5, 6)
+VARIANT_STREAM = 7
 STATUS_OK, STATUS_WAIT_TIMEOUT = 0, 1
 WEIGHTS_F32, WEIGHTS_BF16 = 0, 1
 
@@ -64,6 +65,8 @@ _SIGS = {
     "w8a16_quantize_weights": (_INT, [_VP, _U32, _U32, _U32, _U32, _VP, _VP, _VP]),
     "w8a16_quantize_activations": (_INT, [_VP, _U32, _U32, _U32, _VP, _VP, _U32, _VP]),
     "w8a16_workspace_bytes": (_U64, [_U32, _U32]),
+    "w8a16_workspace_bytes_for": (_U64, [_U32, _U32, _U32]),
+    "w8a16_plan_ws": (_INT, [_U32, _U32, _U32, _U64, ctypes.POINTER(Plan)]),
     "w8a16_gemm_noalloc": (_INT, [_VP, _U32, _VP, _VP, _VP, _U32, _U32, _U32, _U32, _U32, _VP]),
     "w8a16_noalloc_scratch_bytes": (_U64, []),
     "w8a16_split_activations": (_INT, [_VP, _U32, _U32, _U32, _VP, _U64, _VP]),
@@ -151,6 +154,14 @@ def plan_current(M, N, K) -> dict:
     """The plan w8a16_gemm uses on the current device."""
     p = Plan()
     _check(load().w8a16_plan_current(M, N, K, ctypes.byref(p)))
+    return p.as_dict()
+
+
+def plan_ws(M, N, K, workspace_bytes) -> dict:
+    """The plan gemm_ws takes with a workspace of that many bytes (plan=None) on the
+    current device."""
+    p = Plan()
+    _check(load().w8a16_plan_ws(M, N, K, workspace_bytes, ctypes.byref(p)))
     return p.as_dict()
 
 
@@ -246,11 +257,19 @@ def workspace_bytes(M: int, K: int) -> int:
     return int(load().w8a16_workspace_bytes(M, K))
 
 
+def workspace_bytes_for(M: int, N: int, K: int) -> int:
+    """Workspace bytes with which gemm_ws takes its fastest plan at (M, N, K) on the
+    current device."""
+    return int(load().w8a16_workspace_bytes_for(M, N, K))
+
+
 def gemm_ws(A, W, scale, C=None, *, workspace=None, stream=None, plan: Plan | None = None,
             flags: int = 0):
-    """gemm() through w8a16_gemm_ws. workspace: a CUDA uint8 tensor of at least
-    workspace_bytes(M, K) bytes, 16-byte aligned; None allocates one with torch for
-    this call (a caller that repeats calls should keep one); False passes none."""
+    """gemm() through w8a16_gemm_ws. workspace: a CUDA uint8 tensor, 16-byte aligned
+    (workspace_bytes_for(M, N, K) bytes give the fastest plan; workspace_bytes(M, K)
+    the pre-split plan above 16 tokens); None allocates one of the larger of the two
+    with torch for this call (a caller that repeats calls should keep one); False
+    passes none."""
     import torch
     M, N, K = _shapes(A, W, scale, C)
     if C is None:
@@ -264,7 +283,9 @@ def gemm_ws(A, W, scale, C=None, *, workspace=None, stream=None, plan: Plan | No
         _on_one_gpu(A, workspace)
     lib = load()
     if workspace is None:
-        workspace = torch.empty(max(16, workspace_bytes(M, K)), dtype=torch.uint8, device=A.device)
+        with torch.cuda.device(A.device):
+            need = max(workspace_bytes_for(M, N, K), workspace_bytes(M, K))
+        workspace = torch.empty(max(16, need), dtype=torch.uint8, device=A.device)
     ws_ptr, ws_bytes = (None, 0) if workspace is False else (workspace.data_ptr(), workspace.numel())
     with torch.cuda.device(A.device):
         rc = lib.w8a16_gemm_ws(A.data_ptr(), A.stride(0), W.data_ptr(), scale.data_ptr(), C.data_ptr(),

@@ -109,11 +109,14 @@ uint32_t token_tile_for(uint32_t M) {
 // up to 64). Per-variant sizes come from the shared constants.
 bool is_tc_variant(int32_t v) {
     return v == W8A16_VARIANT_TC || v == W8A16_VARIANT_TC8 || v == W8A16_VARIANT_W8A8 ||
-           v == W8A16_VARIANT_PRESPLIT;
+           v == W8A16_VARIANT_PRESPLIT || v == W8A16_VARIANT_STREAM;
 }
-bool is_fp8_act_variant(int32_t v) { return v == W8A16_VARIANT_W8A8 || v == W8A16_VARIANT_PRESPLIT; }
+bool is_stream(int32_t v) { return v == W8A16_VARIANT_STREAM; }
+bool is_fp8_act_variant(int32_t v) {
+    return v == W8A16_VARIANT_W8A8 || v == W8A16_VARIANT_PRESPLIT || v == W8A16_VARIANT_STREAM;
+}
 bool is_gemv(int32_t v) { return v == W8A16_VARIANT_GEMV; }
-uint32_t v_terms(int32_t v) { return v == W8A16_VARIANT_PRESPLIT ? 2u : 1u; }
+uint32_t v_terms(int32_t v) { return v == W8A16_VARIANT_PRESPLIT || v == W8A16_VARIANT_STREAM ? 2u : 1u; }
 uint32_t max_token_tile(int32_t v) { return v == W8A16_VARIANT_TC8 ? 64u : 128u; }
 uint32_t v_threads(int32_t v, uint32_t tn) {
     return is_gemv(v)                ? w8a16::kGvThreads
@@ -197,6 +200,40 @@ void fill_simt(uint32_t M, uint32_t N, w8a16_plan_t* p) {
     p->cluster[0] = p->cluster[1] = p->cluster[2] = 1;
 }
 
+// Persistent stream-K plans of the pre-split path (W8A16_VARIANT_STREAM): 3..32
+// tokens in one token tile of 16 or 32, 4 weight stages, two CTAs per SM.
+constexpr uint32_t kStreamMinTokens = 3, kStreamMaxTokens = 32, kStreamStages = 4;
+
+struct StreamLayout {
+    uint64_t counters_off, parts_off, total;
+    uint32_t maxseg;
+};
+// The largest number of CTAs any tile's steps fall to, with P CTAs over the units.
+uint32_t stream_maxseg(uint32_t tiles, uint32_t ksteps, uint32_t P) {
+    const uint64_t U = static_cast<uint64_t>(tiles) * ksteps;
+    uint32_t most = 1;
+    for (uint32_t t = 0; t < tiles; ++t) {
+        const uint64_t u = static_cast<uint64_t>(t) * ksteps;
+        const uint32_t n = w8a16::stream_cta_of(u + ksteps - 1, U, P) - w8a16::stream_cta_of(u, U, P) + 1;
+        most = n > most ? n : most;
+    }
+    return most;
+}
+// Workspace: the split's codes and factors, the tile counters, the partials.
+StreamLayout stream_layout(uint32_t M, uint32_t N, uint32_t K, uint32_t tn, uint32_t P) {
+    StreamLayout L;
+    const uint32_t tiles = ceil_div(N, w8a16::kTcRows);
+    L.maxseg = stream_maxseg(tiles, K / w8a16::kKStep, P);
+    L.counters_off = w8a16::align256(w8a16::split_ws_bytes(M, K));
+    L.parts_off = w8a16::align256(L.counters_off + 4ull * tiles);
+    L.total = L.parts_off + static_cast<uint64_t>(tiles) * L.maxseg * w8a16::kTcRows * tn * 4ull;
+    return L;
+}
+bool stream_applies(uint32_t M, uint32_t N, uint32_t K) {
+    return M >= kStreamMinTokens && M <= kStreamMaxTokens &&
+           static_cast<uint64_t>(ceil_div(N, w8a16::kTcRows)) * (K / w8a16::kKStep) < (1ull << 31);
+}
+
 // Decode kernel plan: a cluster of `split` CTAs per 128-row weight tile, one token
 // tile of up to kGvMaxTokens tokens.
 void fill_gemv(uint32_t N, uint32_t split, w8a16_plan_t* p) {
@@ -214,6 +251,17 @@ void fill_gemv(uint32_t N, uint32_t split, w8a16_plan_t* p) {
     p->cluster[1] = p->cluster[2] = 1;
     p->smem_bytes = w8a16::gemv_smem_bytes();
     p->tmem_cols = w8a16::kGvTmemCols;
+}
+
+// Stream-K plan: `ctas` persistent CTAs (0: two per SM), one token tile.
+void fill_stream(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count, uint32_t ctas, w8a16_plan_t* p) {
+    const uint32_t tn = M <= 16 ? 16u : 32u;
+    const uint64_t units = static_cast<uint64_t>(ceil_div(N, w8a16::kTcRows)) * (K / w8a16::kKStep);
+    fill_tc(W8A16_VARIANT_STREAM, M, N, tn, kStreamStages, 1, p);
+    const uint64_t slots = static_cast<uint64_t>(sm_count ? sm_count : 152u) * p->ctas_per_sm;
+    const uint64_t P = ctas ? ctas : (units < slots ? units : slots);
+    p->grid[0] = static_cast<uint32_t>(P);
+    p->grid[1] = 1;
 }
 
 // Whether a decode-kernel split can run (N, K): each CTA on at most kGvMaxSteps K
@@ -316,6 +364,16 @@ int validate_plan(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& p) {
         if (p.grid[0] != ref.grid[0] || p.grid[1] != 1 || p.cluster[0] != p.split_k ||
             p.token_tile != ref.token_tile || p.stages != ref.stages || p.tail_tiles || p.tail_split)
             return fail(W8A16_ERR_PLAN, "decode plan does not match the shape");
+        return W8A16_OK;
+    }
+    if (is_stream(p.variant)) {
+        const uint64_t units = static_cast<uint64_t>(ceil_div(N, w8a16::kTcRows)) * ksteps;
+        if (!stream_applies(M, N, K) || (p.token_tile != 16 && p.token_tile != 32) || M > p.token_tile ||
+            p.stages != kStreamStages || p.split_k != 1 || p.grid[1] != 1 || p.grid[0] < 1 ||
+            p.grid[0] > units || p.cluster[0] != 1 || p.tail_tiles || p.tail_split)
+            return fail(W8A16_ERR_PLAN, "stream-K plan: needs " + u(kStreamMinTokens) + " <= M <= " +
+                                            u(kStreamMaxTokens) + " tokens in one token tile, 1..units CTAs, "
+                                            "split 1, no tail");
         return W8A16_OK;
     }
     if (!is_tc_variant(p.variant))
@@ -611,22 +669,60 @@ int run(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, uint32_t flags,
 
 // W8A8: the same size rules as w8a16_gemm, plus the activation code pitch (a
 // multiple of 16 bytes: TMA row stride) and the scale pitch (>= M, a multiple of 4).
+// The stream-K operands in a workspace laid out by stream_layout.
+w8a16::StreamK stream_args(uint32_t M, uint32_t N, uint32_t K, const w8a16_plan_t& plan, uint8_t* ws) {
+    const StreamLayout L = stream_layout(M, N, K, plan.token_tile, plan.grid[0]);
+    w8a16::StreamK sk{};
+    sk.parts = reinterpret_cast<float*>(ws + L.parts_off);
+    sk.counters = reinterpret_cast<uint32_t*>(ws + L.counters_off);
+    sk.units = ceil_div(N, w8a16::kTcRows) * (K / w8a16::kKStep);
+    sk.maxseg = L.maxseg;
+    return sk;
+}
+
 // The W8A16 product through the two-term split: the split pre-pass into the
 // workspace, then the FP8 x FP8 kernel on it. Both are queued as programmatic
 // dependent launches; the kernel's weight prefetch overlaps only the split,
-// which writes neither the weights nor their scales.
+// which writes neither the weights nor their scales. A stream-K plan also gets the
+// tile counters (cleared by the split) and the partials from the workspace.
 int run_presplit(const w8a16::GemmArgs& g, const w8a16_plan_t& plan, void* ws, uint64_t ts_ns,
                  cudaStream_t stream) {
     std::string err;
     const uint32_t fstride = static_cast<uint32_t>(w8a16::split_ws_scale_stride(g.M));
     uint8_t* codes = static_cast<uint8_t*>(ws);
     float* factors = reinterpret_cast<float*>(codes + 2ull * g.M * g.K);
-    int rc = w8a16::launch_split_act(g.A, g.lda, g.M, g.K, codes, factors, fstride, stream, &err);
+    const w8a16::StreamK sk = is_stream(plan.variant) ? stream_args(g.M, g.N, g.K, plan, codes) : w8a16::StreamK{};
+    int rc = w8a16::launch_split_act(g.A, g.lda, g.M, g.K, codes, factors, fstride, sk.counters,
+                                     sk.counters ? ceil_div(g.N, w8a16::kTcRows) : 0u, stream, &err);
     if (rc) return fail(rc, err);
-    const w8a16::W8A8Args a{codes, g.K, factors, fstride, g.W, g.scale, g.C, g.ldc, g.M, g.N, g.K, 2u};
+    const w8a16::W8A8Args a{codes, g.K, factors, fstride, g.W, g.scale, g.C, g.ldc, g.M, g.N, g.K, 2u, sk};
     rc = w8a16::launch_w8a8(a, plan, stream, ts_ns, W8A16_FLAG_PDL, &err);
     if (rc) return fail(rc, err);
     return ok();
+}
+
+// Workspace bytes of the stream-K plan for (M, N, K) on `sm_count` SMs (0 where it
+// does not apply).
+uint64_t stream_ws_bytes(uint32_t M, uint32_t N, uint32_t K, uint32_t sm_count) {
+    if (!stream_applies(M, N, K)) return 0;
+    w8a16_plan_t p;
+    fill_stream(M, N, K, sm_count, 0, &p);
+    return stream_layout(M, N, K, p.token_tile, p.grid[0]).total;
+}
+
+// The plan w8a16_gemm_ws takes without a forced plan, given `have` bytes of
+// workspace: the pre-split path on the cluster split-K schedule for M > 16 (its
+// terms fit), else w8a16_gemm's own plan (*presplit = false). The persistent
+// stream-K plan is never chosen here: on GB300 it measured slower than both (its
+// fix-up of tiles split between CTAs costs several loaded memory round trips at
+// the end of every CTA), so it runs only when forced.
+int plan_ws_choice(uint32_t M, uint32_t N, uint32_t K, uint64_t have, const DeviceInfo& info,
+                   w8a16_plan_t* plan, bool* presplit, std::string* err) {
+    *presplit = true;
+    if (M > 16 && have >= w8a16::split_ws_bytes(M, K))
+        return plan_live(W8A16_VARIANT_PRESPLIT, M, N, K, info, plan, err);
+    *presplit = false;
+    return plan_live(W8A16_VARIANT_AUTO, M, N, K, info, plan, err);
 }
 
 int run_ws(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, void* ws, uint64_t ws_bytes,
@@ -640,21 +736,23 @@ int run_ws(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, void* ws, uint6
     if (ws && reinterpret_cast<uintptr_t>(ws) % 16 != 0)
         return fail(W8A16_ERR_ALIGN, "w8a16_gemm_ws: the workspace must be 16-byte aligned");
     const uint64_t need = w8a16::split_ws_bytes(g.M, g.K);
-    const bool have_ws = ws != nullptr && ws_bytes >= need;
-    if (forced && forced->variant == W8A16_VARIANT_PRESPLIT && !have_ws)
-        return fail(W8A16_ERR_ARG, "w8a16_gemm_ws: a pre-split plan needs a workspace of " +
-                                       std::to_string(need) + " bytes (have " + std::to_string(ws ? ws_bytes : 0) +
-                                       ")");
-    if (forced && forced->variant != W8A16_VARIANT_PRESPLIT) return run(g, forced, flags, stream);
-    if (!forced && (g.M <= 16 || !have_ws)) return run(g, nullptr, flags, stream);
+    const uint64_t have = ws ? ws_bytes : 0;
+    const bool pre = forced && (forced->variant == W8A16_VARIANT_PRESPLIT || is_stream(forced->variant));
+    if (forced && !pre) return run(g, forced, flags, stream);
+    if (pre) {
+        rc = validate_plan(g.M, g.N, g.K, *forced);
+        if (rc) return rc;
+        const uint64_t want = is_stream(forced->variant)
+                                  ? stream_layout(g.M, g.N, g.K, forced->token_tile, forced->grid[0]).total
+                                  : need;
+        if (have < want)
+            return fail(W8A16_ERR_ARG, "w8a16_gemm_ws: this plan needs a workspace of " + std::to_string(want) +
+                                           " bytes (have " + std::to_string(have) + ")");
+    }
     const TimeoutSetting& ts = timeout_setting();
     if (!ts.valid)
         return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
                                        "' is not an integer number of milliseconds in 1..600000");
-    if (forced) {
-        rc = validate_plan(g.M, g.N, g.K, *forced);
-        if (rc) return rc;
-    }
     DeviceInfo info;
     std::string err;
     rc = current_device_info(&info, &err);
@@ -663,8 +761,10 @@ int run_ws(const w8a16::GemmArgs& g, const w8a16_plan_t* forced, void* ws, uint6
     if (forced) {
         plan = *forced;
     } else {
-        rc = plan_live(W8A16_VARIANT_PRESPLIT, g.M, g.N, g.K, info, &plan, &err);
+        bool presplit = false;
+        rc = plan_ws_choice(g.M, g.N, g.K, have, info, &plan, &presplit, &err);
         if (rc) return fail(rc, err);
+        if (!presplit) return run(g, nullptr, flags, stream);
     }
     return run_presplit(g, plan, ws, ts.ns, stream);
 }
@@ -810,6 +910,19 @@ uint64_t w8a16_workspace_bytes(uint32_t M, uint32_t K) {
     return w8a16::split_ws_bytes(M, K);
 }
 
+uint64_t w8a16_workspace_bytes_for(uint32_t M, uint32_t N, uint32_t K) {
+    if (M == 0 || N == 0 || K == 0 || K % w8a16::kKStep != 0) return 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        sms = 152;
+    }
+    const uint64_t pre = M > 16 ? w8a16::split_ws_bytes(M, K) : 0;
+    const uint64_t sk = stream_ws_bytes(M, N, K, static_cast<uint32_t>(sms));
+    return sk > pre ? sk : pre;
+}
+
 int w8a16_gemm_noalloc(const void* A, uint32_t a_row_stride, const void* W, const float* block_scale,
                        void* C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K, uint32_t flags,
                        w8a16_stream_t stream) {
@@ -855,7 +968,7 @@ int w8a16_split_activations(const void* A, uint32_t a_row_stride, uint32_t M, ui
     const uint32_t fstride = static_cast<uint32_t>(w8a16::split_ws_scale_stride(M));
     uint8_t* codes = static_cast<uint8_t*>(workspace);
     float* factors = reinterpret_cast<float*>(codes + 2ull * M * K);
-    rc = w8a16::launch_split_act(A, a_row_stride, M, K, codes, factors, fstride,
+    rc = w8a16::launch_split_act(A, a_row_stride, M, K, codes, factors, fstride, nullptr, 0u,
                                  static_cast<cudaStream_t>(stream), &err);
     if (rc) return fail(rc, err);
     return ok();
@@ -956,6 +1069,20 @@ int w8a16_plan_current(uint32_t M, uint32_t N, uint32_t K, w8a16_plan_t* out) {
     return ok();
 }
 
+int w8a16_plan_ws(uint32_t M, uint32_t N, uint32_t K, uint64_t workspace_bytes, w8a16_plan_t* out) {
+    if (!out) return fail(W8A16_ERR_NULL, "w8a16_plan_ws: NULL plan pointer");
+    int rc = check_sizes(K, N, M, N, K);
+    if (rc) return rc;
+    DeviceInfo info;
+    std::string err;
+    rc = current_device_info(&info, &err);
+    if (rc) return fail(rc, err);
+    bool presplit = false;
+    rc = plan_ws_choice(M, N, K, workspace_bytes, info, out, &presplit, &err);
+    if (rc) return fail(rc, err);
+    return ok();
+}
+
 int w8a16_cluster_capacity(int32_t variant, uint32_t token_tile, uint32_t stages,
                            uint32_t out[17]) {
     if (!out) return fail(W8A16_ERR_NULL, "w8a16_cluster_capacity: NULL output");
@@ -982,6 +1109,12 @@ int w8a16_plan_variant(uint32_t M, uint32_t N, uint32_t K, int32_t variant, uint
         plan_core(W8A16_VARIANT_AUTO, M, N, K, sm_count, nullptr, &p);
     } else if (variant == W8A16_VARIANT_SIMT) {
         fill_simt(M, N, &p);
+    } else if (is_stream(variant)) {
+        if (!stream_applies(M, N, K) || (stages && stages != kStreamStages) || (split_k && split_k != 1))
+            return fail(W8A16_ERR_PLAN, "w8a16_plan_variant: the stream-K plan takes " + u(kStreamMinTokens) +
+                                            " <= M <= " + u(kStreamMaxTokens) + ", split 1 and " +
+                                            u(kStreamStages) + " stages");
+        fill_stream(M, N, K, sm_count, 0, &p);
     } else if (is_gemv(variant)) {
         const uint32_t sp = split_k ? split_k : gemv_split(M, N, K, sm_count, nullptr);
         if (sp == 0 || M > w8a16::kGvMaxTokens || (stages && stages != w8a16::kGvSlots))

@@ -112,6 +112,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (the source may have
+// been written by the previous grid), and its group bookkeeping.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A 32-bit load with acquire semantics at GPU scope (pairs with a release by
+// another CTA: a fence before an atomic).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A barrier among `count` threads (whole warps) of the CTA on hardware barrier
+// `id` (0 is __syncthreads').
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------ programmatic launches --
 // Wait for the grids this one depends on (a no-op unless it was launched as a
 // programmatic dependent), and allow dependents to be scheduled.

@@ -21,6 +21,31 @@ struct GemmArgs {
     uint32_t M, N, K;
 };
 
+// Persistent stream-K schedule of the FP8 x FP8 kernel (units = 0: the cluster
+// split-K schedule instead). The grid's CTAs split the units (128-row weight
+// tile, 128-K step), in tile-major order, into contiguous equal ranges; a tile
+// whose steps fall to several CTAs is summed through `parts` (FP32 partials
+// [tile][segment][128 rows][token tile]) by whichever of them finishes last,
+// in segment (= K) order; `counters` [tiles] count finished segments and are
+// zero when the kernel starts (the split pre-pass clears them; the last CTA of a
+// tile resets its counter).
+struct StreamK {
+    float* parts;
+    uint32_t* counters;
+    uint32_t units;
+    uint32_t maxseg;
+};
+// The CTA (of P) whose contiguous range [c U / P, (c + 1) U / P) holds unit u.
+__host__ __device__ constexpr uint32_t stream_cta_of(uint64_t u, uint64_t units, uint64_t ctas) {
+    return static_cast<uint32_t>(((u + 1) * ctas - 1) / units);
+}
+// How many CTAs' ranges cover tile t's units [t ksteps, (t + 1) ksteps).
+__host__ __device__ constexpr uint32_t stream_segments(uint32_t t, uint32_t ksteps, uint64_t units, uint64_t ctas) {
+    return stream_cta_of(static_cast<uint64_t>(t) * ksteps + ksteps - 1, units, ctas) -
+           stream_cta_of(static_cast<uint64_t>(t) * ksteps, units, ctas) + 1;
+}
+
+
 // Operands of the FP8 x FP8 kernel: E4M3 activation codes with FP32 factors per
 // token and 128-K group [K/128][a_scale_stride], the weights and C as in GemmArgs.
 // terms = 1 (W8A8): codes [M][lda bytes], factors the group scales. terms = 2 (the
@@ -37,11 +62,13 @@ struct W8A8Args {
     uint32_t ldc;
     uint32_t M, N, K;
     uint32_t terms;
+    StreamK sk;   // zero-initialised: the cluster split-K schedule
 };
 
 struct StatusWord {
     uint32_t code, where, detail;
 };
+
 
 // Tiling constants of the tensor-core variant.
 constexpr uint32_t kTcRows = 128;      // weight rows per tile (tcgen05 MMA M)
@@ -185,6 +212,10 @@ constexpr uint32_t gemv_smem_bytes() {
 }
 static_assert(2u * (gemv_smem_bytes() + 1024u) <= 233472u, "two decode CTAs per SM");
 
+// Stream-K workspace after the split's codes and factors: tile counters (256-byte
+// aligned) and the partials [tiles][maxseg][128][token tile] FP32.
+constexpr uint64_t align256(uint64_t x) { return (x + 255u) / 256u * 256u; }
+
 // Workspace of the two-term split: codes [2M][K] (hi rows, then lo rows) and
 // factors [K/128][round_up(M, 4)] FP32.
 constexpr uint64_t split_ws_scale_stride(uint32_t M) { return (static_cast<uint64_t>(M) + 3u) / 4u * 4u; }
@@ -215,7 +246,8 @@ int w8a8_cluster_capacity(uint32_t tn, uint32_t stages, uint32_t terms, uint32_t
                           std::string* err);
 // The two-term split of BF16 activations into the workspace layout above.
 int launch_split_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* factors,
-                     uint32_t factor_stride, cudaStream_t s, std::string* err);
+                     uint32_t factor_stride, uint32_t* counters, uint32_t ncounters, cudaStream_t s,
+                     std::string* err);
 cudaError_t w8a8_status_read(StatusWord* out, bool clear, cudaStream_t s);
 int launch_quantize_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* scales,
                         uint32_t scale_stride, cudaStream_t s, std::string* err);

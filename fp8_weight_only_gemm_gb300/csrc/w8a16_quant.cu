@@ -136,9 +136,14 @@ __global__ void __launch_bounds__(256)
 // token's outputs are NaN), then the split of the four values.
 __global__ void __launch_bounds__(256)
     split_act_kernel(const uint16_t* __restrict__ A, uint32_t lda, uint32_t M, uint32_t K,
-                     uint8_t* __restrict__ codes, float* __restrict__ factors, uint32_t factor_stride) {
+                     uint8_t* __restrict__ codes, float* __restrict__ factors, uint32_t factor_stride,
+                     uint32_t* __restrict__ counters, uint32_t ncounters) {
     grid_dependency_wait();   // A may be the previous kernel's output; the workspace its input
     grid_launch_dependents();
+    // the stream-K tile counters of the GEMM that follows start at zero
+    for (uint64_t c = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < ncounters;
+         c += static_cast<uint64_t>(gridDim.x) * blockDim.x)
+        counters[c] = 0u;
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t item = static_cast<uint64_t>(blockIdx.x) * 8u + (threadIdx.x >> 5);
     const uint32_t groups = K / kQCols;
@@ -173,7 +178,8 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 int launch_split_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* codes, float* factors,
-                     uint32_t factor_stride, cudaStream_t s, std::string* err) {
+                     uint32_t factor_stride, uint32_t* counters, uint32_t ncounters, cudaStream_t s,
+                     std::string* err) {
     const uint64_t items = static_cast<uint64_t>(M) * (K / kQCols);
     const uint64_t blocks = (items + 7) / 8;
     if (blocks > 0x7FFFFFFFull) {
@@ -191,7 +197,8 @@ int launch_split_act(const void* A, uint32_t lda, uint32_t M, uint32_t K, void* 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, split_act_kernel, static_cast<const uint16_t*>(A), lda, M, K,
-                                       static_cast<uint8_t*>(codes), factors, factor_stride);
+                                       static_cast<uint8_t*>(codes), factors, factor_stride, counters,
+                                       ncounters);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *err = std::string("activation split launch failed: ") + cudaGetErrorString(e);

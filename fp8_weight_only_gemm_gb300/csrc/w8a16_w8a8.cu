@@ -46,7 +46,7 @@ constexpr uint32_t kWTileBytes = kTcRows * kKStep;   // 16 KiB of E4M3 weights p
 
 enum : uint32_t {
     kWaitW = 21, kWaitX = 22, kWaitXSlot = 23, kWaitMdone = 24, kWaitPEmpty = 25, kWaitDone = 26,
-    kWaitDrain = 27, kWaitRed = 28
+    kWaitDrain = 27, kWaitRed = 28, kWaitFlush = 29
 };
 
 template <uint32_t TN, uint32_t STAGES, uint32_t TERMS>
@@ -60,8 +60,8 @@ struct A8Cfg {
     static constexpr uint32_t kFold0 = 4;                  // first fold warp
     static constexpr uint32_t kTokPerFold = TN * 4 / NF;
     static constexpr uint32_t ND = STAGES > SA ? (STAGES > NP ? STAGES : NP) : (SA > NP ? SA : NP);
-    // barriers: wfull[S], xfull[SA], mdone[ND], pempty[NP], done, red
-    static constexpr uint32_t kNumBars = STAGES + SA + ND + NP + 2;
+    // barriers: wfull[S], xfull[SA], mdone[ND], pempty[NP], done, red, fsync[2] (stream-K)
+    static constexpr uint32_t kNumBars = STAGES + SA + ND + NP + 4;
     static constexpr uint32_t kFactorRegs = (kTokPerFold + 31) / 32;   // per lane
     static_assert(STAGES % 2 == 0 && SA % 2 == 0 && NP % 2 == 0, "rings of even depth");
     static_assert(NP * NB <= kTmemCols, "TMEM budget");
@@ -86,12 +86,39 @@ __device__ __forceinline__ void drain_ring_a8(uint32_t bar_base, uint32_t depth,
     }
 }
 
-template <uint32_t TN, uint32_t STAGES, uint32_t TERMS>
+// acc[t] += s_w * f[t] * P[t] for CW tokens, two per packed FP32 instruction: with two
+// terms P = hi + lo / 32 (fmaf(lo, 1/32, hi), exact), folded as
+// acc = fmaf(s_w, P * f, acc); with one, acc = fmaf(s_w * f, P, acc).
+template <uint32_t TERMS, uint32_t CW>
+__device__ __forceinline__ void fold_cols(float* acc, const float* v, const float* vl, const float* f, float sw) {
+    const uint64_t sw2 = pack_f32x2(sw, sw);
+#pragma unroll
+    for (uint32_t t = 0; t < CW; t += 2) {
+        const float2 ff = *reinterpret_cast<const float2*>(f + t);
+        uint64_t r;
+        if (TERMS == 2) {
+            const uint64_t pt = fma_f32x2(pack_f32x2(vl[t], vl[t + 1]), pack_f32x2(0.03125f, 0.03125f),
+                                          pack_f32x2(v[t], v[t + 1]));
+            r = fma_f32x2(sw2, mul_f32x2(pt, pack_f32x2(ff.x, ff.y)), pack_f32x2(acc[t], acc[t + 1]));
+        } else {
+            r = fma_f32x2(mul_f32x2(sw2, pack_f32x2(ff.x, ff.y)), pack_f32x2(v[t], v[t + 1]),
+                          pack_f32x2(acc[t], acc[t + 1]));
+        }
+        const float2 a = unpack_f32x2(r);
+        acc[t] = a.x;
+        acc[t + 1] = a.y;
+    }
+}
+
+// SK: the persistent stream-K instance (two terms, up to 32 tokens); its fold code is
+// compiled only there, so the cluster split-K instances keep their register budget.
+template <uint32_t TN, uint32_t STAGES, uint32_t TERMS, bool SK = false>
 __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs(TN))
     w8a16_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const float* __restrict__ a_scale, uint32_t a_stride, const float* __restrict__ scale,
                       __nv_bfloat16* __restrict__ C, uint32_t ldc, uint32_t M, uint32_t N, uint32_t K,
-                      uint32_t split_k, uint32_t tile0, uint32_t tok_major, uint64_t timeout_ns) {
+                      uint32_t split_k, uint32_t tile0, uint32_t tok_major, const StreamK sk,
+                      uint64_t timeout_ns) {
     using Cfg = A8Cfg<TN, STAGES, TERMS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -107,6 +134,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (alias ? (ring > red ? ring : red) : ring + red));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* sk_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);   // stream-K: last of a tile
 
     // mdone[i % ND] completes when step i's MMAs have: it frees weight slot
     // i % STAGES and activation slot i % SA and fills product buffer i % NP.
@@ -117,6 +145,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     const uint32_t pempty0 = mdone0 + 8u * Cfg::ND;
     const uint32_t done_bar = pempty0 + 8u * Cfg::NP;
     const uint32_t red_bar = done_bar + 8u;
+    const uint32_t fsync0 = red_bar + 8u, fsync1 = fsync0 + 8u;   // stream-K: fold warps meet
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tok_major (no split): the token tiles of one weight tile are consecutive CTAs, so
@@ -129,7 +158,16 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
     const uint32_t ksteps = K / kKStep;                        // < 2^24: products fit 32 bits
     const uint32_t s_begin = rank * ksteps / split_k;
     const uint32_t s_end = (rank + 1) * ksteps / split_k;
-    const uint32_t nsteps = s_end - s_begin;
+    // The CTA's steps as units (128-row tile, 128-K step) in tile-major order: the
+    // range [u_first, u_first + nsteps) is one tile's [s_begin, s_end) under the
+    // cluster split-K schedule, and the CTA's share of all units under stream-K.
+    static_assert(!SK || (TERMS == 2 && TN <= 32), "stream-K instances: two terms, up to 32 tokens");
+    constexpr bool sk_mode = SK;
+    const uint32_t u_first = sk_mode ? static_cast<uint32_t>(static_cast<uint64_t>(blockIdx.x) * sk.units / gridDim.x)
+                                     : tile * ksteps + s_begin;
+    const uint32_t nsteps =
+        sk_mode ? static_cast<uint32_t>(static_cast<uint64_t>(blockIdx.x + 1) * sk.units / gridDim.x) - u_first
+                : s_end - s_begin;
     uint64_t deadline = globaltimer_ns() + timeout_ns;   // restarted by each role after the dependency wait
     const uint32_t my_row0 = owned_row0(rank, split_k);
     const uint32_t my_rows = owned_row0(rank + 1, split_k) - my_row0;
@@ -141,7 +179,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         for (uint32_t b = lane; b < Cfg::kNumBars; b += 32) {
             const uint32_t addr = bar0 + 8u * b;
             uint32_t count = 1;
-            if (addr >= pempty0 && addr < done_bar) count = Cfg::NF;        // fold warps
+            if ((addr >= pempty0 && addr < done_bar) || addr == fsync0) count = Cfg::NF;   // fold warps
             else if (addr == done_bar) count = 2;                           // MMA issuers
             mbar_init(addr, count);
         }
@@ -157,9 +195,11 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         const uint64_t pol_w = l2_policy_evict_first();
         for (uint32_t i = 0; i < npre; ++i) {
             mbar_arrive_expect_tx(wfull0 + 8u * i, kWTileBytes);
+            const uint32_t u = u_first + i;
             tma_load_2d(smem_u32(sW + i * kWTileBytes), &tmW, wfull0 + 8u * i,
-                        static_cast<int32_t>((s_begin + i) * kKStep),
-                        static_cast<int32_t>(tile * kTcRows), pol_w);
+                        static_cast<int32_t>((SK ? u % ksteps : s_begin + i) * kKStep),
+                        static_cast<int32_t>((SK ? u / ksteps : tile) * kTcRows),
+                        pol_w);
         }
         tma_prefetch_desc(&tmX);
     }
@@ -193,9 +233,10 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                                &g_w8a8_status, kWaitMdone))
                     break;
                 mbar_arrive_expect_tx(wfull0 + 8u * s, kWTileBytes);
+                const uint32_t u = u_first + i;
                 tma_load_2d(smem_u32(sW + s * kWTileBytes), &tmW, wfull0 + 8u * s,
-                            static_cast<int32_t>((s_begin + i) * kKStep),
-                            static_cast<int32_t>(tile * kTcRows), pol_w);
+                            static_cast<int32_t>((SK ? u % ksteps : s_begin + i) * kKStep),
+                            static_cast<int32_t>((SK ? u / ksteps : tile) * kTcRows), pol_w);
                 issued = i + 1;
             }
             drain_ring_a8(wfull0, STAGES, issued, timeout_ns);
@@ -216,12 +257,11 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                                                abort_flag, &g_w8a8_status, kWaitXSlot))
                     break;
                 mbar_arrive_expect_tx(xfull0 + 8u * j, Cfg::kCodeBytes);
-                tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes), &tmX, xfull0 + 8u * j,
-                            static_cast<int32_t>((s_begin + i) * kKStep), static_cast<int32_t>(token0),
-                            pol_a);
+                const int32_t kx = static_cast<int32_t>((SK ? (u_first + i) % ksteps : s_begin + i) * kKStep);
+                tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes), &tmX, xfull0 + 8u * j, kx,
+                            static_cast<int32_t>(token0), pol_a);
                 if (TERMS == 2)   // lo terms: rows M + token0.. of the [2M][K] codes
-                    tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes + TN * kKStep), &tmX, xfull0 + 8u * j,
-                                static_cast<int32_t>((s_begin + i) * kKStep),
+                    tma_load_2d(smem_u32(sX + j * Cfg::kCodeBytes + TN * kKStep), &tmX, xfull0 + 8u * j, kx,
                                 static_cast<int32_t>(M + token0), pol_a);
                 issued = i + 1;
             }
@@ -267,7 +307,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         float acc[Cfg::kTokPerFold];
 #pragma unroll
         for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) acc[t] = 0.f;
-        const float* srow = scale + static_cast<size_t>(tile) * ksteps + s_begin;
+        const float* srow = scale + u_first;   // block_scale [tiles][ksteps] is unit-major
         // this CTA's weight block scales, 32 per register (lane l: step 32c + l)
         float sc_cur = lane < nsteps ? __ldg(srow + lane) : 0.f;
         float sc_next = lane + 32u < nsteps ? __ldg(srow + 32u + lane) : 0.f;
@@ -278,11 +318,13 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
         float* fbuf = sF + (warp - Cfg::kFold0) * Cfg::kTokPerFold;
         const uint32_t tokf = token0 + fh * Cfg::kTokPerFold;
         const auto load_factors = [&](uint32_t step, float (&f)[Cfg::kFactorRegs]) {
+            // the step's 128-K group: s_begin + step, or under stream-K the unit's
+            const uint32_t kg = SK ? (u_first + step) % ksteps : s_begin + step;
 #pragma unroll
             for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r) {
                 const uint32_t t = r * 32u + lane;
                 f[r] = (t < Cfg::kTokPerFold && tokf + t < M)
-                           ? __ldcg(a_scale + static_cast<size_t>(s_begin + step) * a_stride + tokf + t)
+                           ? __ldcg(a_scale + static_cast<size_t>(kg) * a_stride + tokf + t)
                            : 0.f;
             }
         };
@@ -298,6 +340,31 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r) fq[d][r] = 0.f;
             }
         }
+        // Stream-K: the fold's current tile and step, and whether its segment started at
+        // the tile's first step. When a segment ends (the tile's last step, or the CTA's),
+        // a whole tile goes straight to C and part of one to its slot of the partials.
+        uint32_t seg_tile = u_first / ksteps, seg_k = u_first % ksteps;
+        bool seg_from0 = seg_k == 0, loop_done = false;
+        const uint32_t m0 = fh * Cfg::kTokPerFold;   // this thread's first token of the tile
+        const auto sk_store = [&](uint32_t t, bool whole) {
+            if (whole) {
+                const uint32_t rows_v = min(kTcRows, N - t * kTcRows);
+                if (row < rows_v) {
+                    __nv_bfloat16* crow = C + static_cast<size_t>(t) * kTcRows + row;
+#pragma unroll
+                    for (uint32_t tt = 0; tt < Cfg::kTokPerFold; ++tt)
+                        if (m0 + tt < toks_valid)
+                            crow[static_cast<size_t>(token0 + m0 + tt) * ldc] = __float2bfloat16_rn(acc[tt]);
+                }
+            } else {
+                const uint32_t cf = stream_cta_of(static_cast<uint64_t>(t) * ksteps, sk.units, gridDim.x);
+                float4* mine = reinterpret_cast<float4*>(
+                    sk.parts + ((static_cast<size_t>(t) * sk.maxseg + (blockIdx.x - cf)) * kTcRows + row) * TN + m0);
+#pragma unroll
+                for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)
+                    mine[g] = make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+            }
+        };
         for (uint32_t i = 0; i < nsteps; ++i) {
             if (i != 0 && (i & 31u) == 0) {
                 sc_cur = sc_next;
@@ -322,44 +389,100 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
             const uint32_t pcol = tP + lane_bits + p * Cfg::NB + fh * Cfg::kTokPerFold;
 #pragma unroll
             for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
-                float v[16];
+                float v[16], vl[16];
                 tmem_ld_32x32b_x16(pcol + c, v);
-                // two tokens per packed FP32 instruction, the arithmetic of
-                // acc = fmaf(sw, fmaf(lo, 1/32, hi) * f, acc) (two terms) or
-                // acc = fmaf(sw * f, P, acc) (one term) on each
-                const uint64_t sw2 = pack_f32x2(sw, sw);
-                if (TERMS == 2) {
-                    float vl[16];
-                    tmem_ld_32x32b_x16(pcol + TN + c, vl);
-                    tc_wait_ld();
-                    const uint64_t k32 = pack_f32x2(0.03125f, 0.03125f);
-#pragma unroll
-                    for (uint32_t t = 0; t < 16; t += 2) {
-                        const float2 f = *reinterpret_cast<const float2*>(fbuf + c + t);
-                        const uint64_t pt = fma_f32x2(pack_f32x2(vl[t], vl[t + 1]), k32, pack_f32x2(v[t], v[t + 1]));
-                        const float2 a = unpack_f32x2(fma_f32x2(sw2, mul_f32x2(pt, pack_f32x2(f.x, f.y)),
-                                                                pack_f32x2(acc[c + t], acc[c + t + 1])));
-                        acc[c + t] = a.x;
-                        acc[c + t + 1] = a.y;
-                    }
-                } else {
-                    tc_wait_ld();
-#pragma unroll
-                    for (uint32_t t = 0; t < 16; t += 2) {
-                        const float2 f = *reinterpret_cast<const float2*>(fbuf + c + t);
-                        const float2 a = unpack_f32x2(fma_f32x2(mul_f32x2(sw2, pack_f32x2(f.x, f.y)),
-                                                                pack_f32x2(v[t], v[t + 1]),
-                                                                pack_f32x2(acc[c + t], acc[c + t + 1])));
-                        acc[c + t] = a.x;
-                        acc[c + t + 1] = a.y;
-                    }
-                }
+                if (TERMS == 2) tmem_ld_32x32b_x16(pcol + TN + c, vl);
+                tc_wait_ld();
+                fold_cols<TERMS, 16>(acc + c, v, vl, fbuf + c, sw);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pempty0 + 8u * p);
+            if (sk_mode) {
+                if (seg_k == ksteps - 1 || i == nsteps - 1) {
+                    sk_store(seg_tile, seg_from0 && seg_k == ksteps - 1);
+#pragma unroll
+                    for (uint32_t t = 0; t < Cfg::kTokPerFold; ++t) acc[t] = 0.f;
+                    seg_from0 = true;
+                }
+                if (++seg_k == ksteps) {
+                    seg_k = 0;
+                    ++seg_tile;
+                }
+            }
+            loop_done = i == nsteps - 1;
         }
-        if (split_k == 1) {
+        if (sk_mode) {
+            // Only a CTA's first and last tiles can be partial; their segments are in
+            // the partials. The fold warps meet once on two mbarriers (bounded waits, so
+            // a failed role elsewhere cannot leave them waiting): every warp's partials
+            // are written before the leader's fence and counts, and the counts' verdict
+            // comes back through sk_flag. The CTA that brings a tile's count of
+            // segments to its total adds them in segment (= K) order and writes C.
+            const uint32_t u_last = u_first + nsteps - 1;
+            const uint32_t tf = u_first / ksteps, tl = u_last / ksteps;
+            const bool part_f = u_first % ksteps != 0 || (tf == tl && u_last % ksteps != ksteps - 1);
+            const bool part_l = tl != tf && u_last % ksteps != ksteps - 1;
+            if (part_f || part_l) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fsync0);
+                bool ok = warp_wait_a8(fsync0, 0, deadline, abort_flag, kWaitFlush) && loop_done;
+                if (warp == Cfg::kFold0 && lane == 0) {
+                    int bits = 0;
+                    if (ok && *abort_flag == 0) {
+                        __threadfence();   // the CTA's partials, ordered by the meeting, before the counts
+                        const uint32_t cf = part_f ? atomicAdd(sk.counters + tf, 1u) : 0u;
+                        const uint32_t cl = part_l ? atomicAdd(sk.counters + tl, 1u) : 0u;
+                        if (part_f && cf == stream_segments(tf, ksteps, sk.units, gridDim.x) - 1) bits |= 1;
+                        if (part_l && cl == stream_segments(tl, ksteps, sk.units, gridDim.x) - 1) bits |= 2;
+                        __threadfence();
+                    }
+                    *sk_flag = bits;
+                    mbar_arrive(fsync1);
+                }
+                ok = warp_wait_a8(fsync1, 0, deadline, abort_flag, kWaitFlush) && ok;
+                const int bits = ok ? *sk_flag : 0;
+                // Each thread copies its slice of every segment into the (then idle)
+                // weight ring with 16-byte asynchronous copies (one round trip), reads
+                // back only its own copies and adds them in order.
+                constexpr uint32_t kRingSegs = STAGES * kWTileBytes / (kTcRows * TN * 4u);
+                float* mine = reinterpret_cast<float*>(sW) + static_cast<size_t>(row) * TN + m0;
+                for (uint32_t j = 0; j < 2; ++j) {
+                    if (!(bits & (1 << j))) continue;
+                    const uint32_t t = j == 0 ? tf : tl;
+                    const uint32_t nseg = stream_segments(t, ksteps, sk.units, gridDim.x);
+                    const float* base = sk.parts + (static_cast<size_t>(t) * sk.maxseg * kTcRows + row) * TN + m0;
+#pragma unroll
+                    for (uint32_t tt = 0; tt < Cfg::kTokPerFold; ++tt) acc[tt] = 0.f;
+                    for (uint32_t s0 = 0; s0 < nseg; s0 += kRingSegs) {
+                        const uint32_t s1 = min(nseg, s0 + kRingSegs);
+                        for (uint32_t sg = s0; sg < s1; ++sg) {
+                            const float* src = base + static_cast<size_t>(sg) * kTcRows * TN;
+                            float* dst = mine + static_cast<size_t>(sg - s0) * kTcRows * TN;
+#pragma unroll
+                            for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)
+                                cp_async_16(smem_u32(dst + 4 * g), src + 4 * g);
+                        }
+                        cp_async_commit();
+                        cp_async_wait_group<0>();
+                        for (uint32_t sg = s0; sg < s1; ++sg) {   // segment (= K) order
+                            const float4* q4 =
+                                reinterpret_cast<const float4*>(mine + static_cast<size_t>(sg - s0) * kTcRows * TN);
+#pragma unroll
+                            for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g) {
+                                const float4 q = q4[g];
+                                acc[4 * g] += q.x;
+                                acc[4 * g + 1] += q.y;
+                                acc[4 * g + 2] += q.z;
+                                acc[4 * g + 3] += q.w;
+                            }
+                        }
+                    }
+                    sk_store(t, true);
+                    if (warp == Cfg::kFold0 && lane == 0) sk.counters[t] = 0u;   // ready for the next call
+                }
+            }
+        } else if (split_k == 1) {
             if (row < rows_valid) {
                 const uint32_t n = tile * kTcRows + row;
 #pragma unroll
@@ -427,24 +550,30 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
 }
 
 using A8KernelFn = void (*)(CUtensorMap, CUtensorMap, const float*, uint32_t, const float*, __nv_bfloat16*,
-                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+                            uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, uint32_t, StreamK,
+                            uint64_t);
 struct A8Instance {
     uint32_t tn, stages, terms;
+    bool stream_k;
     A8KernelFn fn;
 };
-#define W8A16_A8_INST(TN_, ST_, T_) {TN_, ST_, T_, &w8a16_w8a8_kernel<TN_, ST_, T_>}
+#define W8A16_A8_INST(TN_, ST_, T_) {TN_, ST_, T_, false, &w8a16_w8a8_kernel<TN_, ST_, T_>}
+#define W8A16_A8_SK(TN_, ST_) {TN_, ST_, 2, true, &w8a16_w8a8_kernel<TN_, ST_, 2, true>}
 const A8Instance kA8Instances[] = {
     W8A16_A8_INST(16, 4, 1), W8A16_A8_INST(16, 6, 1), W8A16_A8_INST(32, 4, 1), W8A16_A8_INST(32, 6, 1),
     W8A16_A8_INST(64, 4, 1), W8A16_A8_INST(64, 6, 1), W8A16_A8_INST(128, 4, 1),
     W8A16_A8_INST(16, 4, 2), W8A16_A8_INST(32, 4, 2), W8A16_A8_INST(32, 6, 2), W8A16_A8_INST(64, 4, 2),
     W8A16_A8_INST(64, 6, 2), W8A16_A8_INST(128, 4, 2),
+    W8A16_A8_SK(16, 4), W8A16_A8_SK(32, 4),
 };
 #undef W8A16_A8_INST
+#undef W8A16_A8_SK
 constexpr int kNumA8 = sizeof(kA8Instances) / sizeof(kA8Instances[0]);
 
-int find_a8(uint32_t tn, uint32_t stages, uint32_t terms) {
+int find_a8(uint32_t tn, uint32_t stages, uint32_t terms, bool stream_k = false) {
     for (int i = 0; i < kNumA8; ++i)
-        if (kA8Instances[i].tn == tn && kA8Instances[i].stages == stages && kA8Instances[i].terms == terms)
+        if (kA8Instances[i].tn == tn && kA8Instances[i].stages == stages && kA8Instances[i].terms == terms &&
+            kA8Instances[i].stream_k == stream_k)
             return i;
     return -1;
 }
@@ -479,10 +608,11 @@ bool w8a8_supported_stages(uint32_t tn, uint32_t stages, uint32_t terms) {
 
 int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
                 uint32_t flags, std::string* err) {
-    const int inst = find_a8(p.token_tile, p.stages, g.terms);
+    const int inst = find_a8(p.token_tile, p.stages, g.terms, g.sk.units != 0);
     if (inst < 0) {
         *err = "no FP8 x FP8 kernel instance for token_tile=" + std::to_string(p.token_tile) +
-               " stages=" + std::to_string(p.stages) + " terms=" + std::to_string(g.terms);
+               " stages=" + std::to_string(p.stages) + " terms=" + std::to_string(g.terms) +
+               (g.sk.units ? " (stream-K)" : "");
         return W8A16_ERR_PLAN;
     }
     int dev = 0;
@@ -501,10 +631,33 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
     if (!tc_tensor_map_w(wg, dev, &mw, err) ||
         !tensor_map_act_codes(g.A, g.M * g.terms, g.K, g.lda, p.token_tile, dev, &mx, err))
         return W8A16_ERR_LAUNCH;
+    const uint32_t row_tiles = (g.N + kTcRows - 1) / kTcRows;
+    if (g.sk.units != 0) {
+        // Stream-K: grid[0] persistent CTAs share the units in contiguous ranges, one
+        // token tile, no clusters.
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(p.grid[0], 1, 1);
+        cfg.blockDim = dim3(w8a8_threads(p.token_tile, g.terms), 1, 1);
+        cfg.dynamicSmemBytes = w8a8_smem_bytes(p.token_tile, p.stages, 1, g.terms);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, g.a_scale, g.a_scale_stride, g.scale,
+                               static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, 1u, 0u, 0u, g.sk, timeout_ns);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            *err = std::string("W8A8 kernel launch failed: ") + cudaGetErrorString(e);
+            return W8A16_ERR_LAUNCH;
+        }
+        return W8A16_OK;
+    }
     // One launch, or (a split-K tail) two: whole tiles [0, T - tail) at the plan's
     // split, then tiles [T - tail, T) over clusters of tail_split CTAs, queued as a
     // programmatic dependent launch of the first (which writes neither W nor its scales).
-    const uint32_t row_tiles = (g.N + kTcRows - 1) / kTcRows;
     const uint32_t tail = p.tail_split > 1 ? p.tail_tiles : 0u;
     for (uint32_t part = 0; part < (tail ? 2u : 1u); ++part) {
         const uint32_t split = part == 0 ? p.split_k : p.tail_split;
@@ -529,7 +682,7 @@ int launch_w8a8(const W8A8Args& g, const w8a16_plan_t& p, cudaStream_t s, uint64
         cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, kA8Instances[inst].fn, mw, mx, g.a_scale, g.a_scale_stride, g.scale,
                                static_cast<__nv_bfloat16*>(g.C), g.ldc, g.M, g.N, g.K, split, tile0,
-                               tok_major, timeout_ns);
+                               tok_major, StreamK{}, timeout_ns);
         if (e != cudaSuccess) {
             cudaGetLastError();
             *err = std::string("W8A8 kernel launch failed: ") + cudaGetErrorString(e);

@@ -107,6 +107,14 @@ enum {
                                 pre-pass into the caller's workspace, and the W8A8 kernel
                                 multiplies both terms in one MMA of N = 2 x token tile;
                                 same accuracy as W8A16_VARIANT_TC8 */
+    W8A16_VARIANT_STREAM = 7,  /* w8a16_gemm_ws with a forced plan only, 3 <= M <= 32: the
+                                pre-split path on a persistent grid (two CTAs per SM) that
+                                splits all (128-row weight tile, 128-K step) units into
+                                equal contiguous ranges, a tile split between CTAs being
+                                summed through the workspace in K order by the last of
+                                them; needs w8a16_workspace_bytes_for(M, N, K) bytes; same
+                                accuracy as W8A16_VARIANT_PRESPLIT. Never the planner's
+                                choice (slower than the other plans on GB300) */
     W8A16_VARIANT_GEMV = 6     /* decode kernel for M <= 2: the arithmetic of
                                 W8A16_VARIANT_TC8; a cluster of split_k CTAs per 128-row
                                 weight tile, each on at most 8 K steps, every one of them
@@ -228,17 +236,31 @@ W8A16_API int w8a16_gemm_with_plan(const void *A, uint32_t a_row_stride, const v
  * ([K/128][M rounded up to 4]). 0 for M = 0 or K not a positive multiple of 128. */
 W8A16_API uint64_t w8a16_workspace_bytes(uint32_t M, uint32_t K);
 
+/* Bytes of workspace that every w8a16_gemm_ws plan for (M, N, K) on the current
+ * device fits in: w8a16_workspace_bytes(M, K) for M > 16 (the pre-split terms), and
+ * where the stream-K plan applies (3 <= M <= 32) its layout: the terms, one counter
+ * per 128-row weight tile (256-byte aligned after them) and the FP32 partials of the
+ * tiles split between CTAs (256-byte aligned after the counters). 0 where no plan
+ * uses a workspace or the sizes are invalid. */
+W8A16_API uint64_t w8a16_workspace_bytes_for(uint32_t M, uint32_t N, uint32_t K);
+
+/* The plan w8a16_gemm_ws takes with plan == NULL and `workspace_bytes` bytes of
+ * workspace for (M, N, K) on the current device. Checks as w8a16_plan_current. */
+W8A16_API int w8a16_plan_ws(uint32_t M, uint32_t N, uint32_t K, uint64_t workspace_bytes,
+                            w8a16_plan_t *out);
+
 /* w8a16_gemm with a workspace: the same operation, arguments, checks and result
  * contract (within the tolerance of W8A16_VARIANT_TC8, whose split this path
- * shares). With plan == NULL the library chooses: M <= 16, or no workspace of
- * w8a16_workspace_bytes(M, K) bytes, runs exactly what w8a16_gemm runs; otherwise
- * the pre-split path (W8A16_VARIANT_PRESPLIT): a split kernel writes the workspace,
- * then the FP8 x FP8 kernel reads it (one launch, or two when the plan has a split-K
- * tail; all on `stream`, each queued as a programmatic dependent launch of the one
- * before; W8A16_FLAG_PDL governs only the split kernel's overlap with the previous
- * kernel, as for w8a16_gemm). A plan from
- * w8a16_plan_variant forces a variant (PRESPLIT needs the workspace, else
- * W8A16_ERR_ARG).
+ * shares). With plan == NULL the library chooses (w8a16_plan_ws reports it): for
+ * M > 16 with at least w8a16_workspace_bytes(M, K) bytes, W8A16_VARIANT_PRESPLIT;
+ * else exactly what w8a16_gemm runs. On the pre-split plans (PRESPLIT, or a forced
+ * STREAM plan) a split kernel writes the workspace (and clears the stream-K tile
+ * counters), then the FP8 x FP8 kernel reads it (one launch, or two when the plan
+ * has a split-K tail; all on `stream`, each queued as a programmatic dependent
+ * launch of the one before;
+ * W8A16_FLAG_PDL governs only the split kernel's overlap with the previous kernel,
+ * as for w8a16_gemm). A plan from w8a16_plan_variant forces a variant (PRESPLIT
+ * and STREAM need their workspace, else W8A16_ERR_ARG).
  *   workspace  device memory, 16-byte aligned, owned by the caller, or NULL; it is
  *              written by the call and must not be used by other work until the
  *              call's kernels have finished (calls that share one workspace must
@@ -288,13 +310,13 @@ W8A16_API int w8a16_split_activations(const void *A, uint32_t a_row_stride, uint
 
 /* w8a16_gemm_split_terms -- C = the W8A16 product of the activations that
  * w8a16_split_activations wrote into `workspace` for the same (M, K), with W,
- * block_scale, C, c_row_stride, N as in w8a16_gemm. The FP8 x FP8 kernel (one
- * launch, or two with a split-K tail). flags: W8A16_FLAG_PDL lets the kernel read
- * its first weight tiles and block scales before the previous kernel of the
- * stream has finished (which must not write W or block_scale); the workspace, A's
- * terms, is read only after it. The workspace is only read. Checks as for
- * w8a16_gemm (the workspace takes A's place in the NULL and alignment checks),
- * plus its size (W8A16_ERR_ARG). */
+ * block_scale, C, c_row_stride, N as in w8a16_gemm. The FP8 x FP8 kernel on the
+ * planner's W8A16_VARIANT_PRESPLIT plan (one launch, or two with a split-K tail).
+ * flags: W8A16_FLAG_PDL lets the kernel read its first weight tiles and block
+ * scales before the previous kernel of the stream has finished (which must not
+ * write W or block_scale); the workspace, A's terms, is read only after it. The
+ * workspace is only read. Checks as for w8a16_gemm (the workspace takes A's place
+ * in the NULL and alignment checks), plus its size (W8A16_ERR_ARG). */
 W8A16_API int w8a16_gemm_split_terms(const void *workspace, uint64_t workspace_bytes, const void *W,
                                      const float *block_scale, void *C, uint32_t c_row_stride,
                                      uint32_t M, uint32_t N, uint32_t K, uint32_t flags,

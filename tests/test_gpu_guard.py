@@ -79,6 +79,16 @@ def test_every_entry_point_stays_inside_its_buffers(M, N, K):
     torch.cuda.synchronize()
     _check_c(case, buf, nbytes, C, "gemm_ws")
     assert _bands_intact(wbuf, need), "gemm_ws wrote outside its workspace"
+    # the forced stream-K plan (3..32 tokens): counters and partials inside its layout
+    need_sk = binding.workspace_bytes_for(M, N, K)
+    if 3 <= M <= 32:
+        p = binding.plan_variant(M, N, K, binding.VARIANT_STREAM, 0, 0)
+        wbuf, ws = _guarded(need_sk)
+        buf, nbytes, C = _c_view(case)
+        binding.gemm_ws(A, W, S, C[:, :N], workspace=ws, plan=p)
+        torch.cuda.synchronize()
+        _check_c(case, buf, nbytes, C, "gemm_ws stream-K")
+        assert _bands_intact(wbuf, need_sk), "gemm_ws (stream-K) wrote outside its workspace"
 
 
 def test_quantisers_and_w8a8_stay_inside_their_buffers():

@@ -207,8 +207,9 @@ def test_workspace_holds_the_two_term_split():
 
 
 def test_entry_point_fallbacks():
-    """M <= 16, or no workspace, or one too small: the call runs what w8a16_gemm runs
-    (same bits); a pre-split plan without a workspace is refused."""
+    """No workspace, or one too small for the split: the call runs what w8a16_gemm
+    runs (same bits), as does M <= 16 with a workspace too small for the stream-K
+    layout; a pre-split plan without a workspace is refused."""
     import fp8_weight_only_gemm_gb300 as w8
     from fp8_weight_only_gemm_gb300 import binding
     for M in (8, 32):
@@ -220,7 +221,10 @@ def test_entry_point_fallbacks():
             got = binding.gemm_ws(A[:, :wl.K], W, S, workspace=ws)
             assert torch.equal(got.view(torch.int16), base.view(torch.int16))
         if M == 8:
-            assert torch.equal(binding.gemm_ws(A[:, :wl.K], W, S).view(torch.int16), base.view(torch.int16))
+            ws = torch.empty(binding.workspace_bytes_for(M, wl.N, wl.K) - 1, dtype=torch.uint8, device="cuda")
+            assert binding.plan_ws(M, wl.N, wl.K, ws.numel())["variant"] == w8.plan_current(M, wl.N, wl.K)["variant"]
+            got = binding.gemm_ws(A[:, :wl.K], W, S, workspace=ws)
+            assert torch.equal(got.view(torch.int16), base.view(torch.int16))
     p = _plan(32, 512, 1024, 32, 2, 4)
     with pytest.raises(binding.W8A16Error, match="workspace"):
         binding.gemm_ws(A[:, :1024], W, S, workspace=False, plan=p)
@@ -289,8 +293,10 @@ def test_split_then_terms_matches_the_one_call_path(M, N, K, lda):
         got = C.cpu().view(torch.int16).numpy().view(np.uint16)
         ref, exact, absum = oracle_full(case)
         compare(case, got, ref, exact, absum, split_k=16, label=f"split+terms M{M} w{i}", variant=3)
-        if M > 16:   # w8a16_gemm_ws takes its pre-split path above 16 tokens
-            assert np.array_equal(got, run_ws(case)), "two calls differ from w8a16_gemm_ws"
+        if M > 16:   # w8a16_gemm_ws with the split's workspace: the same pre-split plan
+            ws1 = torch.empty(binding.workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+            assert binding.plan_ws(M, N, K, ws1.numel())["variant"] == PRESPLIT
+            assert np.array_equal(got, run_ws(case, workspace=ws1)), "two calls differ from w8a16_gemm_ws"
 
 
 def test_split_terms_checks():

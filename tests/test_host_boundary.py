@@ -170,7 +170,7 @@ def test_plan_variant_validation(lib):
     s = binding.plan_variant(8, 1024, 1024, binding.VARIANT_SIMT)
     assert s.variant == binding.VARIANT_SIMT and s.grid[0] == 128
     with pytest.raises(binding.W8A16Error):
-        binding.plan_variant(8, 1024, 1024, 7)
+        binding.plan_variant(8, 1024, 1024, 8)   # no such variant
 
 
 def test_forced_plan_must_match_shape(lib):
@@ -426,3 +426,69 @@ def test_decode_kernel_plans(lib):
         with pytest.raises(binding.W8A16Error):
             binding.plan_variant(bad.get("M", 1), 4096, 4096, binding.VARIANT_GEMV, bad.get("split", 4),
                                  bad.get("stages", 0), 152)
+
+
+def _stream_cta_of(u, units, ctas):
+    """The CTA whose contiguous range [c U / P, (c + 1) U / P) holds unit u (brute force)."""
+    for c in range(ctas):
+        if c * units // ctas <= u < (c + 1) * units // ctas:
+            return c
+    raise AssertionError(u)
+
+
+def test_stream_plans(lib):
+    """Stream-K plans (3..32 tokens): one token tile of 16 or 32, 4 stages, split 1,
+    min(units, 2 x SMs) CTAs of at most the two-CTAs-per-SM resources; refused
+    outside 3..32 tokens or with another split or stage count."""
+    for (M, N, K) in [(3, 256, 256), (8, 12288, 4096), (16, 4096, 4096), (17, 14336, 5120), (32, 14336, 5120),
+                      (24, 300, 1280), (32, 128, 128)]:
+        p = binding.plan_variant(M, N, K, binding.VARIANT_STREAM, 0, 0, 152).as_dict()
+        units = -(-N // 128) * (K // 128)
+        assert p["variant"] == binding.VARIANT_STREAM and p["split_k"] == 1 and p["stages"] == 4
+        assert p["token_tile"] == (16 if M <= 16 else 32)
+        assert p["grid"] == [min(units, 304), 1, 1] and p["cluster"][0] == 1 and p["ctas_per_sm"] == 2
+        assert p["tmem_cols"] * p["ctas_per_sm"] <= 512 and p["smem_bytes"] * p["ctas_per_sm"] <= 232448
+        assert not p["tail_tiles"] and not p["tail_split"]
+    for bad in [dict(M=2), dict(M=33), dict(split=2), dict(stages=6)]:
+        with pytest.raises(binding.W8A16Error):
+            binding.plan_variant(bad.get("M", 8), 4096, 4096, binding.VARIANT_STREAM, bad.get("split", 0),
+                                 bad.get("stages", 0), 152)
+
+
+def test_stream_cta_ranges_cover_every_unit_once():
+    """The host's closed form for the CTA of a unit matches the brute-force range
+    search, so every unit is in exactly one CTA's range and a tile's segments are
+    the CTAs from the first unit's to the last unit's."""
+    import itertools
+    for units, ctas in itertools.product([1, 7, 64, 120, 257, 3072], [1, 3, 5, 64, 120, 304]):
+        if ctas > units:
+            continue
+        owners = [_stream_cta_of(u, units, ctas) for u in range(units)]
+        assert owners == sorted(owners) and owners[0] == 0 and owners[-1] == ctas - 1
+        assert len(set(owners)) == ctas      # every CTA has at least one unit
+        closed = [((u + 1) * ctas - 1) // units for u in range(units)]
+        assert closed == owners
+
+
+def test_stream_workspace_bytes(lib):
+    """workspace_bytes_for: where the stream-K plan applies, the split's terms, a
+    256-aligned counter per 128-row tile and, 256-aligned after them, 128 x token
+    tile FP32 partials for each of the most segments any tile has; elsewhere the
+    pre-split bytes above 16 tokens, else 0."""
+    for (M, N, K) in [(3, 256, 256), (8, 12288, 4096), (32, 14336, 5120), (24, 300, 1280), (5, 129, 128)]:
+        P = min(-(-N // 128) * (K // 128), 304)
+        tiles, ksteps = -(-N // 128), K // 128
+        units = tiles * ksteps
+        maxseg = max(_stream_cta_of(t * ksteps + ksteps - 1, units, P) - _stream_cta_of(t * ksteps, units, P) + 1
+                     for t in range(tiles))
+        tn = 16 if M <= 16 else 32
+        align = lambda x: -(-x // 256) * 256
+        parts = align(align(binding.workspace_bytes(M, K)) + 4 * tiles)
+        sms = 152
+        # the library asks the current device for its SM count; without one it assumes 152
+        got = binding.workspace_bytes_for(M, N, K)
+        if got != parts + tiles * maxseg * 128 * tn * 4:
+            pytest.skip(f"device with another SM count than {sms}")
+    assert binding.workspace_bytes_for(1, 4096, 4096) == 0
+    assert binding.workspace_bytes_for(64, 4096, 4096) == binding.workspace_bytes(64, 4096)
+    assert binding.workspace_bytes_for(8, 4096, 100) == 0
