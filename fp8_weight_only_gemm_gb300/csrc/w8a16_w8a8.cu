@@ -86,25 +86,20 @@ __device__ __forceinline__ void drain_ring_a8(uint32_t bar_base, uint32_t depth,
     }
 }
 
-// acc[t] += s_w * f[t] * P[t] for CW tokens, two per packed FP32 instruction: with two
-// terms P = hi + lo / 32 (fmaf(lo, 1/32, hi), exact), folded as
-// acc = fmaf(s_w, P * f, acc); with one, acc = fmaf(s_w * f, P, acc).
+// acc[t] += g[t] * P[t] for CW tokens, g = s_w * f (the step's block scale times the
+// token's factor, staged per step), two tokens per packed FP32 instruction. With two
+// terms P = hi + lo / 32 (fmaf(lo, 1/32, hi), exact); f is then a power of two, so
+// fmaf(g, P, acc) rounds as fmaf(s_w, P * f, acc) does wherever s_w * f stays a
+// normal FP32 number.
 template <uint32_t TERMS, uint32_t CW>
-__device__ __forceinline__ void fold_cols(float* acc, const float* v, const float* vl, const float* f, float sw) {
-    const uint64_t sw2 = pack_f32x2(sw, sw);
+__device__ __forceinline__ void fold_cols(float* acc, const float* v, const float* vl, const float* g) {
 #pragma unroll
     for (uint32_t t = 0; t < CW; t += 2) {
-        const float2 ff = *reinterpret_cast<const float2*>(f + t);
-        uint64_t r;
-        if (TERMS == 2) {
-            const uint64_t pt = fma_f32x2(pack_f32x2(vl[t], vl[t + 1]), pack_f32x2(0.03125f, 0.03125f),
-                                          pack_f32x2(v[t], v[t + 1]));
-            r = fma_f32x2(sw2, mul_f32x2(pt, pack_f32x2(ff.x, ff.y)), pack_f32x2(acc[t], acc[t + 1]));
-        } else {
-            r = fma_f32x2(mul_f32x2(sw2, pack_f32x2(ff.x, ff.y)), pack_f32x2(v[t], v[t + 1]),
-                          pack_f32x2(acc[t], acc[t + 1]));
-        }
-        const float2 a = unpack_f32x2(r);
+        const float2 gg = *reinterpret_cast<const float2*>(g + t);
+        const uint64_t p = TERMS == 2 ? fma_f32x2(pack_f32x2(vl[t], vl[t + 1]), pack_f32x2(0.03125f, 0.03125f),
+                                                  pack_f32x2(v[t], v[t + 1]))
+                                      : pack_f32x2(v[t], v[t + 1]);
+        const float2 a = unpack_f32x2(fma_f32x2(pack_f32x2(gg.x, gg.y), p, pack_f32x2(acc[t], acc[t + 1])));
         acc[t] = a.x;
         acc[t + 1] = a.y;
     }
@@ -371,10 +366,12 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 sc_next = i + 32u + lane < nsteps ? __ldg(srow + i + 32u + lane) : 0.f;
             }
             const uint32_t p = i % Cfg::NP;
+            const float sw = __shfl_sync(0xFFFFFFFFu, sc_cur, i & 31u);
             __syncwarp();   // the previous step's reads of fbuf are done
+            // staged as g = s_w * f: one FMA per product in the fold
 #pragma unroll
             for (uint32_t r = 0; r < Cfg::kFactorRegs; ++r)
-                if (r * 32u + lane < Cfg::kTokPerFold) fbuf[r * 32u + lane] = fq[0][r];
+                if (r * 32u + lane < Cfg::kTokPerFold) fbuf[r * 32u + lane] = fq[0][r] * sw;
             __syncwarp();   // ... and this step's factors are visible to the whole warp
 #pragma unroll
             for (uint32_t d = 0; d + 1 < kAhead; ++d)
@@ -385,7 +382,6 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                               kWaitMdone))
                 break;
             tc_fence_after();
-            const float sw = __shfl_sync(0xFFFFFFFFu, sc_cur, i & 31u);
             const uint32_t pcol = tP + lane_bits + p * Cfg::NB + fh * Cfg::kTokPerFold;
 #pragma unroll
             for (uint32_t c = 0; c < Cfg::kTokPerFold; c += 16) {
@@ -393,7 +389,7 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 tmem_ld_32x32b_x16(pcol + c, v);
                 if (TERMS == 2) tmem_ld_32x32b_x16(pcol + TN + c, vl);
                 tc_wait_ld();
-                fold_cols<TERMS, 16>(acc + c, v, vl, fbuf + c, sw);
+                fold_cols<TERMS, 16>(acc + c, v, vl, fbuf + c);
             }
             tc_fence_before();
             __syncwarp();
