@@ -147,7 +147,10 @@ constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) 
 // the two producers in the first four warps; each fold warp stages its tokens'
 // FP32 factors of a step in a private buffer. The 128-token two-term tile has
 // room in TMEM for 2 product buffers of 256 columns.
-constexpr uint32_t w8a8_act_stages(uint32_t, uint32_t = 1) { return 4u; }
+// Activation-code stages: 4, and 2 for the 32-token two-term tile, whose split-K
+// receive buffer then fits beside the rings at two CTAs per SM (no aliasing: the
+// partials go out as soon as a CTA's fold is done).
+constexpr uint32_t w8a8_act_stages(uint32_t tn, uint32_t terms = 1) { return terms == 2 && tn == 32 ? 2u : 4u; }
 constexpr uint32_t w8a8_p_bufs(uint32_t tn, uint32_t terms = 1) { return terms == 2 && tn >= 128 ? 2u : 4u; }
 // (16 for the 128-token two-term tile, whose fold reads two 128-column halves)
 constexpr uint32_t w8a8_fold_warps(uint32_t tn, uint32_t terms = 1) {
