@@ -818,8 +818,8 @@ int run_w8a8(const w8a16::W8A8Args& g, const w8a16_plan_t* forced, uint32_t flag
         return fail(W8A16_ERR_ARG, "W8A16_WAIT_TIMEOUT_MS='" + ts.raw +
                                        "' is not an integer number of milliseconds in 1..600000");
     if (forced) {
-        if (forced->variant != W8A16_VARIANT_W8A8)
-            return fail(W8A16_ERR_PLAN, "w8a16_gemm_w8a8: the plan is not a W8A8 plan");
+        if (forced->variant != W8A16_VARIANT_W8A8 && !is_gemv(forced->variant))
+            return fail(W8A16_ERR_PLAN, "w8a16_gemm_w8a8: the plan is neither a W8A8 nor a decode plan");
         const int rc = validate_plan(g.M, g.N, g.K, *forced);
         if (rc) return rc;
     }
@@ -831,10 +831,16 @@ int run_w8a8(const w8a16::W8A8Args& g, const w8a16_plan_t* forced, uint32_t flag
     if (forced) {
         plan = *forced;
     } else {
-        rc = plan_live(W8A16_VARIANT_W8A8, g.M, g.N, g.K, info, &plan, &err);
-        if (rc) return fail(rc, err);
+        // one or two tokens: the decode kernel where its rule admits the shape (the
+        // same plan as for W8A16), else the W8A8 kernel
+        rc = plan_live(W8A16_VARIANT_AUTO, g.M, g.N, g.K, info, &plan, &err);
+        if (rc || !is_gemv(plan.variant)) {
+            rc = plan_live(W8A16_VARIANT_W8A8, g.M, g.N, g.K, info, &plan, &err);
+            if (rc) return fail(rc, err);
+        }
     }
-    rc = w8a16::launch_w8a8(g, plan, stream, ts.ns, flags, &err);
+    rc = is_gemv(plan.variant) ? w8a16::launch_gemv_w8a8(g, plan, stream, ts.ns, flags, &err)
+                               : w8a16::launch_w8a8(g, plan, stream, ts.ns, flags, &err);
     if (rc) return fail(rc, err);
     return ok();
 }

@@ -94,11 +94,16 @@ __device__ __forceinline__ float split_block_w32(uint2 av, uint8_t* bs, uint32_t
     return fold_factor(E, mx);
 }
 
-template <uint32_t MT>   // tokens (1 or 2)
+// MT: tokens (1 or 2). Q8: the activations are already E4M3 codes (A [M][lda bytes])
+// with one FP32 scale per token and 128-K group (a_scale [K/128][a_scale_stride]), the
+// W8A8 variant: each step's codes are copied into the hi rows (the lo rows stay zero)
+// and the fold multiplies by s_w * s_a.
+template <uint32_t MT, bool Q8>
 __global__ void __launch_bounds__(kGvThreads, 2)
     w8a16_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const float* __restrict__ scale,
-                      __nv_bfloat16* __restrict__ C, uint32_t ldc, const uint16_t* __restrict__ A,
-                      uint32_t lda, uint32_t N, uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
+                      __nv_bfloat16* __restrict__ C, uint32_t ldc, const void* __restrict__ A,
+                      uint32_t lda, const float* __restrict__ a_scale, uint32_t a_scale_stride, uint32_t N,
+                      uint32_t K, uint32_t split_k, uint64_t timeout_ns) {
     // steps per 16-column accumulator: each step takes MT column pairs (hi, lo)
     constexpr uint32_t kQ = 8u / MT;
     constexpr uint32_t kAcc = kGvMaxSteps / kQ;   // accumulators (16 columns each)
@@ -245,14 +250,34 @@ __global__ void __launch_bounds__(kGvThreads, 2)
         const uint32_t acc_idx = w / kQ;
         const uint32_t pair0 = (w % kQ) * MT;
         uint8_t* bs = sB + w * kGvBStepBytes;
-        const uint16_t* src = A + static_cast<size_t>(s_begin + w) * kKStep + 4u * lane;
-        uint2 av[MT];
+        if constexpr (Q8) {
+            // the step's codes into the hi rows (4 bytes a lane, 128-byte swizzle); the
+            // factor is the token's group scale (both may be the previous grid's
+            // output: read through L2)
+            const uint8_t* src = static_cast<const uint8_t*>(A) + static_cast<size_t>(s_begin + w) * kKStep + 4u * lane;
+            uint32_t cw[MT];
 #pragma unroll
-        for (uint32_t t = 0; t < MT; ++t) av[t] = *reinterpret_cast<const uint2*>(src + static_cast<size_t>(t) * lda);
+            for (uint32_t t = 0; t < MT; ++t)
+                cw[t] = __ldcg(reinterpret_cast<const unsigned int*>(src + static_cast<size_t>(t) * lda));
+            const uint32_t in_chunk = (lane & 3u) << 2;
 #pragma unroll
-        for (uint32_t t = 0; t < MT; ++t) {
-            const float f = split_block_w32(av[t], bs, 2u * (pair0 + t), 2u * (pair0 + t) + 1u, lane);
-            if (lane == 0) sF[w * kGvMaxTokens + t] = f;
+            for (uint32_t t = 0; t < MT; ++t) {
+                const uint32_t rh = 2u * (pair0 + t);
+                *reinterpret_cast<uint32_t*>(bs + rh * 128u + ((((lane >> 2) ^ (rh & 7u)) << 4) + in_chunk)) = cw[t];
+                if (lane == 0)
+                    sF[w * kGvMaxTokens + t] = __ldcg(a_scale + static_cast<size_t>(s_begin + w) * a_scale_stride + t);
+            }
+        } else {
+            const uint16_t* src = static_cast<const uint16_t*>(A) + static_cast<size_t>(s_begin + w) * kKStep + 4u * lane;
+            uint2 av[MT];
+#pragma unroll
+            for (uint32_t t = 0; t < MT; ++t)
+                av[t] = *reinterpret_cast<const uint2*>(src + static_cast<size_t>(t) * lda);
+#pragma unroll
+            for (uint32_t t = 0; t < MT; ++t) {
+                const float f = split_block_w32(av[t], bs, 2u * (pair0 + t), 2u * (pair0 + t) + 1u, lane);
+                if (lane == 0) sF[w * kGvMaxTokens + t] = f;
+            }
         }
         fence_proxy_async_smem();   // the tensor core reads these terms
         __syncwarp();
@@ -307,9 +332,13 @@ __global__ void __launch_bounds__(kGvThreads, 2)
 #pragma unroll
                     for (uint32_t t = 0; t < MT; ++t) {
                         const uint32_t col = 2u * ((s % kQ) * MT + t);
-                        const float pt = fmaf(v[s / kQ][col + 1], 0.03125f, v[s / kQ][col]) *
-                                         sF[s * kGvMaxTokens + t];
-                        acc[t] = fmaf(sw, pt, acc[t]);
+                        if constexpr (Q8) {   // acc += (s_w * s_a) * P, as the W8A8 kernel folds
+                            acc[t] = fmaf(sw * sF[s * kGvMaxTokens + t], v[s / kQ][col], acc[t]);
+                        } else {
+                            const float pt = fmaf(v[s / kQ][col + 1], 0.03125f, v[s / kQ][col]) *
+                                             sF[s * kGvMaxTokens + t];
+                            acc[t] = fmaf(sw, pt, acc[t]);
+                        }
                     }
                 }
             }
@@ -368,9 +397,11 @@ __global__ void __launch_bounds__(kGvThreads, 2)
     }
 }
 
-using GemvKernelFn = void (*)(CUtensorMap, const float*, __nv_bfloat16*, uint32_t, const uint16_t*, uint32_t,
-                              uint32_t, uint32_t, uint32_t, uint64_t);
-const GemvKernelFn kGemvKernels[2] = {&w8a16_gemv_kernel<1>, &w8a16_gemv_kernel<2>};
+using GemvKernelFn = void (*)(CUtensorMap, const float*, __nv_bfloat16*, uint32_t, const void*, uint32_t,
+                              const float*, uint32_t, uint32_t, uint32_t, uint32_t, uint64_t);
+// [Q8][MT - 1]
+const GemvKernelFn kGemvKernels[2][2] = {{&w8a16_gemv_kernel<1, false>, &w8a16_gemv_kernel<2, false>},
+                                         {&w8a16_gemv_kernel<1, true>, &w8a16_gemv_kernel<2, true>}};
 
 cudaError_t ensure_gemv_attributes(int device) {
     static std::mutex mu;
@@ -378,7 +409,7 @@ cudaError_t ensure_gemv_attributes(int device) {
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
     if (done[device]) return cudaSuccess;
-    for (GemvKernelFn fn : kGemvKernels) {
+    for (GemvKernelFn fn : {kGemvKernels[0][0], kGemvKernels[0][1], kGemvKernels[1][0], kGemvKernels[1][1]}) {
         cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(gemv_smem_bytes()));
@@ -393,8 +424,10 @@ cudaError_t ensure_gemv_attributes(int device) {
 
 }  // namespace
 
-int launch_gemv(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
-                uint32_t flags, std::string* err) {
+namespace {
+
+int launch_gemv_any(const GemmArgs& g, const float* a_scale, uint32_t a_scale_stride, bool q8,
+                    const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns, uint32_t flags, std::string* err) {
     if (g.M < 1 || g.M > kGvMaxTokens) {
         *err = "decode kernel: M=" + std::to_string(g.M) + " is outside 1.." + std::to_string(kGvMaxTokens);
         return W8A16_ERR_PLAN;
@@ -424,14 +457,36 @@ int launch_gemv(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64
     attr[1].val.programmaticStreamSerializationAllowed = (flags & W8A16_FLAG_PDL) ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, kGemvKernels[g.M - 1], mw, g.scale, static_cast<__nv_bfloat16*>(g.C), g.ldc,
-                           static_cast<const uint16_t*>(g.A), g.lda, g.N, g.K, p.split_k, timeout_ns);
+    e = cudaLaunchKernelEx(&cfg, kGemvKernels[q8 ? 1 : 0][g.M - 1], mw, g.scale, static_cast<__nv_bfloat16*>(g.C),
+                           g.ldc, g.A, g.lda, a_scale, a_scale_stride, g.N, g.K, p.split_k, timeout_ns);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *err = std::string("decode kernel launch failed: ") + cudaGetErrorString(e);
         return W8A16_ERR_LAUNCH;
     }
     return W8A16_OK;
+}
+
+}  // namespace
+
+int launch_gemv(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+                uint32_t flags, std::string* err) {
+    return launch_gemv_any(g, nullptr, 0u, false, p, s, timeout_ns, flags, err);
+}
+
+int launch_gemv_w8a8(const W8A8Args& a, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+                     uint32_t flags, std::string* err) {
+    GemmArgs g{};
+    g.A = a.A;
+    g.lda = a.lda;
+    g.W = a.W;
+    g.scale = a.scale;
+    g.C = a.C;
+    g.ldc = a.ldc;
+    g.M = a.M;
+    g.N = a.N;
+    g.K = a.K;
+    return launch_gemv_any(g, a.a_scale, a.a_scale_stride, true, p, s, timeout_ns, flags, err);
 }
 
 int gemv_cluster_capacity(uint32_t cluster, uint32_t* ctas, std::string* err) {
@@ -456,7 +511,7 @@ int gemv_cluster_capacity(uint32_t cluster, uint32_t* ctas, std::string* err) {
     cfg.numAttrs = 1;
     int n = 0;
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kGemvKernels[0]), &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kGemvKernels[0][0]), &cfg);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *err = std::string("cudaOccupancyMaxActiveClusters failed: ") + cudaGetErrorString(e);

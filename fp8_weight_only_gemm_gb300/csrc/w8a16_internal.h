@@ -262,6 +262,9 @@ bool tc8_supported_stages(uint32_t tn, uint32_t stages);
 int launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, std::string* err);
 int launch_gemv(const GemmArgs& g, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
                 uint32_t flags, std::string* err);
+// The decode kernel on E4M3 activations with per-token group scales (the W8A8 variant).
+int launch_gemv_w8a8(const W8A8Args& a, const w8a16_plan_t& p, cudaStream_t s, uint64_t timeout_ns,
+                     uint32_t flags, std::string* err);
 int gemv_cluster_capacity(uint32_t cluster, uint32_t* ctas, std::string* err);
 cudaError_t gemv_status_read(StatusWord* out, bool clear, cudaStream_t s);
 

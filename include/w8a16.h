@@ -120,7 +120,8 @@ enum {
                                 weight tile, each on at most 8 K steps, every one of them
                                 loaded before the grid-dependency wait (shared memory and
                                 TMEM), at most one CTA per SM; the planner's choice for
-                                M <= 2 when ceil(N/128) x ceil(K/1024) CTAs fit that rule */
+                                M <= 2 when ceil(N/128) x ceil(K/1024) CTAs fit that rule,
+                                for w8a16_gemm and w8a16_gemm_w8a8 alike */
 };
 
 /*
@@ -378,17 +379,20 @@ W8A16_API int w8a16_quantize_activations(const void *A, uint32_t a_row_stride, u
  * with A and a_scale as w8a16_quantize_activations writes them (a_row_stride in bytes,
  * >= K and a multiple of 16; a_scale_stride >= M, a multiple of 4), W, block_scale
  * and C as in w8a16_gemm. Per 128-K step one FP8 x FP8 product on the tensor cores,
- * folded in FP32 as acc += block_scale * a_scale * P, split-K partials added in rank
- * order (deterministic). A, a_scale and W 16-byte aligned. flags: W8A16_FLAG_PDL
- * (the previous grid must not write W or block_scale). Same error codes and checks
- * as w8a16_gemm, plus the two pitches above. */
+ * folded in FP32 as acc += (block_scale * a_scale) * P, split-K partials added in rank
+ * order (deterministic). One or two tokens run on the decode kernel where its rule
+ * admits the shape (W8A16_VARIANT_GEMV, the codes copied in as its hi term), else on
+ * the W8A8 kernel. A, a_scale and W 16-byte aligned. flags: W8A16_FLAG_PDL (the
+ * previous grid must not write W or block_scale). Same error codes and checks as
+ * w8a16_gemm, plus the two pitches above. */
 W8A16_API int w8a16_gemm_w8a8(const void *A, uint32_t a_row_stride, const float *a_scale,
                               uint32_t a_scale_stride, const void *W, const float *block_scale,
                               void *C, uint32_t c_row_stride, uint32_t M, uint32_t N, uint32_t K,
                               uint32_t flags, w8a16_stream_t stream);
 
-/* w8a16_gemm_w8a8 with an explicit plan (variant W8A16_VARIANT_W8A8, from
- * w8a16_plan_variant); a plan of another variant is refused with W8A16_ERR_PLAN. */
+/* w8a16_gemm_w8a8 with an explicit plan (variant W8A16_VARIANT_W8A8, or
+ * W8A16_VARIANT_GEMV for M <= 2, from w8a16_plan_variant); a plan of another variant
+ * is refused with W8A16_ERR_PLAN. */
 W8A16_API int w8a16_gemm_w8a8_with_plan(const void *A, uint32_t a_row_stride,
                                         const float *a_scale, uint32_t a_scale_stride,
                                         const void *W, const float *block_scale, void *C,

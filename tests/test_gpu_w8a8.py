@@ -2,7 +2,8 @@
 bit for bit against the oracle (a code is an integer decision taken in FP32 on
 both sides), and the FP8 x FP8 block-scaled GEMM element by element against the
 oracle's W8A8 product, through the C ABI, over token tiles, forced K splits,
-stage counts, ragged M and N, padded pitches and every finite E4M3 code."""
+stage counts, ragged M and N, padded pitches and every finite E4M3 code; one and
+two tokens also on the decode kernel (the codes copied in as its hi term)."""
 from __future__ import annotations
 
 import math
@@ -271,5 +272,85 @@ def test_w8a8_rejects_foreign_plan():
     Sd = torch.zeros((2, 8), dtype=torch.float32, device="cuda")
     W = torch.zeros((256, 256), dtype=torch.uint8, device="cuda")
     s = torch.zeros((2, 2), dtype=torch.float32, device="cuda")
-    with pytest.raises(binding.W8A16Error, match="not a W8A8 plan"):
+    with pytest.raises(binding.W8A16Error, match="neither a W8A8 nor a decode plan"):
         binding.gemm_w8a8(Ad, Sd, W, s, plan=p)
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K,split", [(4096, 4096, 4), (300, 1024, 1), (300, 1280, 2), (130, 640, 5),
+                                       (256, 2048, 8), (1000, 128, 1)])
+def test_w8a8_decode_kernel(o, M, N, K, split):
+    """One or two tokens on the decode kernel: forced splits 1..8 (up to 8 K steps a
+    CTA, some read from TMEM), ragged N, padded pitches; run to run bit-identical."""
+    from fp8_weight_only_gemm_gb300 import binding
+    case = workloads.make_case(workloads.Workload(f"w8a8dec_m{M}_n{N}_k{K}", M, N, K, seed=M * 13 + N + K + split,
+                                                  c_row_stride=N + 3, outlier_frac=0.01,
+                                                  zero_blocks=((0, 1),) if K >= 256 else ()))
+    Aq, a_scale = o.quantize_activations(case.A_np(), M, K)
+    Ad, Sd = _device_w8a8_inputs(Aq, a_scale, M, K, K + 32, 8)
+    p = binding.plan_variant(M, N, K, binding.VARIANT_GEMV, split, 0, _sms())
+    assert p.variant == binding.VARIANT_GEMV and p.split_k == split
+    Wd, Sw = case.W.cuda(), case.scale.cuda()
+    outs = []
+    for _ in range(2):
+        C = case.C0.cuda()
+        binding.gemm_w8a8(Ad, Sd, Wd, Sw, C[:, :N], plan=p)
+        torch.cuda.synchronize()
+        outs.append(C.cpu().view(torch.int16).numpy().view(np.uint16))
+    _w8a8_check(o, Aq, a_scale, case.W_np(), case.scale_np(), M, N, K, outs[0], case.C0_np(), N + 3, split,
+                f"w8a8 decode M={M} N={N} K={K} split={split}")
+    assert np.array_equal(outs[0], outs[1]), "same plan, different bits"
+    assert binding.device_status() == (0, 0, 0)
+
+
+def test_w8a8_decode_nan_codes(o):
+    """A NaN weight code makes its row NaN for both tokens, a NaN activation code its
+    token's outputs NaN, on the decode kernel as in the oracle."""
+    from fp8_weight_only_gemm_gb300 import binding
+    M, N, K = 2, 256, 1024
+    case = workloads.make_case(workloads.Workload("w8a8dec_nan", M, N, K, seed=77))
+    Aq, a_scale = o.quantize_activations(case.A_np(), M, K)
+    Aq = Aq.copy()
+    Aq[1, 700] = 0x7F
+    W = case.W.clone()
+    W[5, 300] = 0xFF
+    Ad, Sd = _device_w8a8_inputs(Aq, a_scale, M, K, K, 4)
+    p = binding.plan_variant(M, N, K, binding.VARIANT_GEMV, 2, 0, _sms())
+    C = case.C0.cuda()
+    binding.gemm_w8a8(Ad, Sd, W.cuda(), case.scale.cuda(), C[:, :N], plan=p)
+    torch.cuda.synchronize()
+    got = C.cpu().view(torch.int16).numpy().view(np.uint16)
+    g = got.reshape(M, N)
+    isnan = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
+    assert isnan[0, 5] and isnan[0].sum() == 1 and isnan[1].all()
+    _w8a8_check(o, Aq, a_scale, W.numpy(), case.scale_np(), M, N, K, got, case.C0_np(), N, 2, "w8a8 decode NaN")
+
+
+def test_w8a8_decode_chain_with_gpu_quantiser(o):
+    """Quantiser then decode GEMM, five times in a row with programmatic dependent
+    launch (each quantiser waits for the previous GEMM): the bits of the same calls
+    without it, and the oracle's result."""
+    from fp8_weight_only_gemm_gb300 import binding
+    case = workloads.make_case("decode_gemv_m1_n4096_k4096")
+    wl = case.wl
+    Ad = case.A.cuda()
+    Wd, Sd = case.W.cuda(), case.scale.cuda()
+
+    def run(flags):
+        C = case.C0.cuda()
+        for _ in range(5):
+            codes, scales = binding.quantize_activations(Ad[:, :wl.K])
+            binding.gemm_w8a8(codes, scales, Wd, Sd, C[:, :wl.N], flags=flags)
+        torch.cuda.synchronize()
+        return C.cpu().view(torch.int16).numpy().view(np.uint16)
+
+    base = run(0)
+    assert np.array_equal(run(binding.FLAG_PDL), base)
+    Aq, a_scale = o.quantize_activations(case.A_np(), wl.M, wl.K, a_row_stride=wl.lda)
+    _w8a8_check(o, Aq, a_scale, case.W_np(), case.scale_np(), wl.M, wl.N, wl.K, base, case.C0_np(), wl.ldc, 4,
+                "w8a8 decode chain")
+    assert binding.device_status() == (0, 0, 0)
