@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kGvThreads, 2)
         __syncwarp();
     }
     if (threadIdx.x == 0) {
-        if (split_k > 1) mbar_arrive_expect_tx(red_bar, split_k * my_rows * 16u);
+        if (split_k > 1) mbar_arrive_expect_tx(red_bar, (split_k - 1) * my_rows * 16u);   // the other ranks'
         // every weight tile-step that has a slot, before anything else (under a
         // programmatic launch the caller guarantees the previous grid writes no W)
         const uint64_t pol_w = l2_policy_evict_first();
@@ -355,16 +355,19 @@ __global__ void __launch_bounds__(kGvThreads, 2)
             const uint32_t owner = ((row + 1u) * split_k - 1u) / kTcRows;
             const uint32_t lrow = row - owned_row0(owner, split_k);
             const uint32_t off = (rank * tc_red_rows(split_k) + lrow) * 16u;
-            st_async_v4f32(dsmem_map(smem_u32(sRed) + off, owner), dsmem_map(red_bar, owner), acc[0],
-                           MT > 1 ? acc[MT - 1] : 0.f, 0.f, 0.f);
+            if (owner != rank)   // rows this CTA owns stay in registers
+                st_async_v4f32(dsmem_map(smem_u32(sRed) + off, owner), dsmem_map(red_bar, owner), acc[0],
+                               MT > 1 ? acc[MT - 1] : 0.f, 0.f, 0.f);
             // the partials are other CTAs' st.async writes: acquire at cluster scope
             const bool got = mbar_wait<true>(red_bar, 0, deadline + timeout_ns, abort_flag, &g_gemv_status,
                                              kWaitRed);
             if (__all_sync(0xFFFFFFFFu, got) && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
                 const uint32_t lr = row - my_row0;
                 float r[2] = {0.f, 0.f};
-                for (uint32_t src = 0; src < split_k; ++src) {   // rank order
-                    const float4 q = *reinterpret_cast<const float4*>(sRed + (src * tc_red_rows(split_k) + lr) * 4u);
+                for (uint32_t src = 0; src < split_k; ++src) {   // rank order, this rank's from registers
+                    const float4 q = src == rank ? make_float4(acc[0], MT > 1 ? acc[MT - 1] : 0.f, 0.f, 0.f)
+                                                 : *reinterpret_cast<const float4*>(
+                                                       sRed + (src * tc_red_rows(split_k) + lr) * 4u);
                     r[0] += q.x;
                     r[1] += q.y;
                 }

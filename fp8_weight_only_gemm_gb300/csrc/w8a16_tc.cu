@@ -184,9 +184,9 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
         __syncwarp();
     }
     if (threadIdx.x == 0) {
-        if (split_k > 1)   // every rank pushes its partials of my rows here
+        if (split_k > 1)   // every other rank pushes its partials of my rows here
             mbar_arrive_expect_tx(red_bar,
-                                  split_k * my_rows * red_row_bytes<TN, Cfg::kTokPerFold>(toks_valid));
+                                  (split_k - 1) * my_rows * red_row_bytes<TN, Cfg::kTokPerFold>(toks_valid));
         // The first ring's weight tiles go out before anything else (TMEM
         // allocation, the CTA barrier), so their HBM latency overlaps the set-up.
         // Weights are requested before waiting on the previous grid in the
@@ -421,25 +421,32 @@ __global__ void __launch_bounds__(tc_threads(TN), 1)
             const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
             const uint32_t dbar = dsmem_map(red_bar, owner);
             const uint32_t ngroups = push_bytes(toks_valid, fh * Cfg::kTokPerFold, Cfg::kTokPerFold) / 16u;
+            if (owner != rank) {   // rows this CTA owns stay in registers
 #pragma unroll
-            for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)   // groups past M are not sent
-                if (g < ngroups)
-                    st_async_v4f32(dst + 16u * g, dbar, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2],
-                                   acc[4 * g + 3]);
+                for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)   // groups past M are not sent
+                    if (g < ngroups)
+                        st_async_v4f32(dst + 16u * g, dbar, acc[4 * g], acc[4 * g + 1], acc[4 * g + 2],
+                                       acc[4 * g + 3]);
+            }
             // This CTA's own rows: the thread holding row `row` of the tile (and
-            // tokens fh*kTokPerFold..) adds the ranks' partials in rank order.
+            // tokens fh*kTokPerFold..) adds the ranks' partials in rank order, its
+            // own rank's from its registers.
             // the partials are other CTAs' st.async writes: acquire at cluster scope
             const bool got = warp_wait<true>(red_bar, 0, deadline + timeout_ns, abort_flag, kWaitRed);
             if (got && row >= my_row0 && row < my_row0 + my_rows && row < rows_valid) {
                 const uint32_t lr = row - my_row0;
                 const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats
                 const float* src_row = sRed + lr * tc_red_stride(TN);
-                for (uint32_t t = fh * Cfg::kTokPerFold;
-                     t < toks_valid && t < (fh + 1) * Cfg::kTokPerFold; t += 4) {
+#pragma unroll
+                for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g) {
+                    const uint32_t t = fh * Cfg::kTokPerFold + 4u * g;
+                    if (t >= toks_valid) break;
                     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
                     for (uint32_t src = 0; src < split_k; ++src) {   // rank order
-                        const float4 q = *reinterpret_cast<const float4*>(src_row + src * rank_stride + t);
+                        const float4 q =
+                            src == rank ? make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3])
+                                        : *reinterpret_cast<const float4*>(src_row + src * rank_stride + t);
                         v.x += q.x;
                         v.y += q.y;
                         v.z += q.z;
