@@ -97,14 +97,20 @@ constexpr uint32_t tc_p_bufs(uint32_t tn) { return tn == 16 ? 4u : 2u; }
 constexpr uint32_t tc_a_bufs(uint32_t tn) {   // even: two MMA issuers alternate steps
     return (tc_tmem_cols(tn) - tc_p_bufs(tn) * tn) / 64u >= 4u ? 4u : 2u;   // 4 for every TN
 }
-// Split-K receive buffer of one CTA: a slot per cluster rank holding the rows
-// this CTA owns (at most ceil(128/split)) x TN FP32 partials.
+// Split-K receive buffer of one CTA: a slot per other cluster rank (a CTA's own
+// partials of the rows it owns stay in registers) holding those rows (at most
+// ceil(128/split)) x TN FP32 partials.
 constexpr uint32_t tc_red_rows(uint32_t split) { return (kTcRows + split - 1) / split; }
-// Receive layout [rank][row][token]: a row's TN partials are contiguous (16-byte
+// Receive layout [slot][row][token]: a row's TN partials are contiguous (16-byte
 // pushes), rows padded by 4 floats so that consecutive rows start in different banks.
 constexpr uint32_t tc_red_stride(uint32_t tn) { return tn + 4u; }
 constexpr uint32_t tc_red_bytes(uint32_t tn, uint32_t split) {
-    return split <= 1 ? 0u : split * tc_red_rows(split) * tc_red_stride(tn) * 4u;
+    return split <= 1 ? 0u : (split - 1) * tc_red_rows(split) * tc_red_stride(tn) * 4u;
+}
+// The slot of rank src's partials in the receive buffer of rank owner (src != owner;
+// 0 for src == owner, which has no slot, so that the index stays in range).
+constexpr uint32_t tc_red_slot(uint32_t src, uint32_t owner) {
+    return src < owner ? src : (src > owner ? src - 1u : 0u);
 }
 // A CTA that allocates all 512 TMEM columns must be alone on its SM (a second
 // one would block in tcgen05.alloc): its dynamic shared memory is padded so that
@@ -147,9 +153,10 @@ constexpr uint32_t tc8_smem_bytes(uint32_t tn, uint32_t stages, uint32_t split) 
 // the two producers in the first four warps; each fold warp stages its tokens'
 // FP32 factors of a step in a private buffer. The 128-token two-term tile has
 // room in TMEM for 2 product buffers of 256 columns.
-// Activation-code stages: 4, and 2 for the 32-token two-term tile, whose split-K
-// receive buffer then fits beside the rings at two CTAs per SM (no aliasing: the
-// partials go out as soon as a CTA's fold is done).
+// Activation-code stages: 4, and 2 for the 32-token two-term tile (4 measured no
+// faster there; 2 keeps its split-K receive buffer beside the rings at two CTAs per
+// SM with room to spare: no aliasing, so the partials go out as soon as a CTA's
+// fold is done).
 constexpr uint32_t w8a8_act_stages(uint32_t tn, uint32_t terms = 1) { return terms == 2 && tn == 32 ? 2u : 4u; }
 constexpr uint32_t w8a8_p_bufs(uint32_t tn, uint32_t terms = 1) { return terms == 2 && tn >= 128 ? 2u : 4u; }
 // (16 for the 128-token two-term tile, whose fold reads two 128-column halves)

@@ -522,10 +522,11 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
             // the last rank r with r * 128 / split_k <= row (no division by split_k)
             const uint32_t owner = ((row + 1) * split_k - 1) / kTcRows;
             const uint32_t lrow = row - owned_row0(owner, split_k);
-            // receive layout [rank][row][token]: this thread's tokens are contiguous
+            // receive layout [slot][row][token]: this thread's tokens are contiguous
             // and go as 16-byte groups; the owner reads them back the same way
             const uint32_t off =
-                ((rank * tc_red_rows(split_k) + lrow) * tc_red_stride(TN) + fh * Cfg::kTokPerFold) * 4u;
+                ((tc_red_slot(rank, owner) * tc_red_rows(split_k) + lrow) * tc_red_stride(TN) +
+                 fh * Cfg::kTokPerFold) * 4u;
             const uint32_t dst = dsmem_map(smem_u32(sRed) + off, owner);
             const uint32_t dbar = dsmem_map(red_bar, owner);
             const uint32_t ngroups = push_bytes(toks_valid, fh * Cfg::kTokPerFold, Cfg::kTokPerFold) / 16u;
@@ -554,7 +555,8 @@ __global__ void __launch_bounds__(tc8_threads(TN), TN == 16 ? 2 : 1)
                     for (uint32_t src = 0; src < split_k; ++src) {   // rank order
                         const float4 q =
                             src == rank ? make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3])
-                                        : *reinterpret_cast<const float4*>(src_row + src * rank_stride + t);
+                                        : *reinterpret_cast<const float4*>(
+                                              src_row + tc_red_slot(src, rank) * rank_stride + t);
                         v.x += q.x;
                         v.y += q.y;
                         v.z += q.z;
