@@ -520,28 +520,54 @@ __global__ void __launch_bounds__(w8a8_threads(TN, TERMS), w8a8_max_ctas_by_regs
                 const uint32_t lr = row - my_row0;
                 const uint32_t rank_stride = tc_red_rows(split_k) * tc_red_stride(TN);   // floats
                 const float* src_row = sRed + lr * tc_red_stride(TN);
+                // Two ranks (the common split): the other rank's partials of every group
+                // loaded first, then straight-line sums in rank order. Not in the 640-thread
+                // instance, whose 96 registers a thread cannot hold them beside the fold's.
+                constexpr bool kFlat2 = w8a8_threads(TN, TERMS) <= 384u;
+                if (kFlat2 && split_k == 2) {
+                    float4 q[Cfg::kTokPerFold / 4];
 #pragma unroll
-                for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g) {
-                    const uint32_t t = fh * Cfg::kTokPerFold + 4u * g;
-                    if (t >= toks_valid) break;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                    for (uint32_t src = 0; src < split_k; ++src) {   // rank order
-                        const float4 q =
-                            src == rank ? make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3])
-                                        : *reinterpret_cast<const float4*>(
-                                              src_row + tc_red_slot(src, rank) * rank_stride + t);
-                        v.x += q.x;
-                        v.y += q.y;
-                        v.z += q.z;
-                        v.w += q.w;
+                    for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g)   // slot 0: the other rank
+                        q[g] = *reinterpret_cast<const float4*>(src_row + fh * Cfg::kTokPerFold + 4u * g);
+#pragma unroll
+                    for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g) {
+                        const uint32_t t = fh * Cfg::kTokPerFold + 4u * g;
+                        const float mine[4] = {acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]};
+                        const float other[4] = {q[g].x, q[g].y, q[g].z, q[g].w};
+#pragma unroll
+                        for (uint32_t u = 0; u < 4; ++u) {
+                            float v = 0.f;   // as the general loop: 0 + rank 0's + rank 1's
+                            v += rank == 0 ? mine[u] : other[u];
+                            v += rank == 0 ? other[u] : mine[u];
+                            if (t + u < toks_valid)
+                                C[static_cast<size_t>(token0 + t + u) * ldc + tile * kTcRows + row] =
+                                    __float2bfloat16_rn(v);
+                        }
                     }
-                    const float vv[4] = {v.x, v.y, v.z, v.w};
+                } else {
 #pragma unroll
-                    for (uint32_t u = 0; u < 4; ++u)
-                        if (t + u < toks_valid)
-                            C[static_cast<size_t>(token0 + t + u) * ldc + tile * kTcRows + row] =
-                                __float2bfloat16_rn(vv[u]);
+                    for (uint32_t g = 0; g < Cfg::kTokPerFold / 4; ++g) {
+                        const uint32_t t = fh * Cfg::kTokPerFold + 4u * g;
+                        if (t >= toks_valid) break;
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                        for (uint32_t src = 0; src < split_k; ++src) {   // rank order
+                            const float4 q =
+                                src == rank ? make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3])
+                                            : *reinterpret_cast<const float4*>(
+                                                  src_row + tc_red_slot(src, rank) * rank_stride + t);
+                            v.x += q.x;
+                            v.y += q.y;
+                            v.z += q.z;
+                            v.w += q.w;
+                        }
+                        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (uint32_t u = 0; u < 4; ++u)
+                            if (t + u < toks_valid)
+                                C[static_cast<size_t>(token0 + t + u) * ldc + tile * kTcRows + row] =
+                                    __float2bfloat16_rn(vv[u]);
+                    }
                 }
             }
         }
