@@ -64,6 +64,8 @@ def test_workloads_through_the_workspace_entry(name):
     (64, 384, 1024, 1032, 64, 2, 4), (50, 130, 1280, 1280, 64, 3, 6), (64, 256, 512, 512, 64, 1, 6),
     (128, 260, 512, 512, 128, 1, 4), (100, 384, 1024, 1024, 128, 1, 4), (130, 256, 768, 776, 128, 1, 4),
     (96, 256, 768, 768, 64, 3, 4), (16, 384, 2048, 2048, 16, 16, 4),
+    # split 2 (the owner's straight-line sum) with a partial last token group and ragged N
+    (29, 520, 1536, 1544, 32, 2, 4), (13, 300, 1024, 1024, 16, 2, 4), (61, 200, 1024, 1024, 64, 2, 4),
 ])
 def test_forced_plans(M, N, K, lda, tile, split, stages):
     case = workloads.make_case("strided_m32_n14336_k5120", M=M, N=N, K=K, a_row_stride=lda,

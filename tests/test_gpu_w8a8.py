@@ -147,6 +147,10 @@ W8A8_CASES = [
     (100, 260, 512, 0, 0, (128, 1, 4)),
     (130, 260, 512, 0, 2, (128, 2, 4)),
     (200, 256, 1280, 0, 0, None),
+    # split 2 (the owner's straight-line sum) with a partial last token group and ragged N
+    (29, 520, 1536, 0, 5, (32, 2, 4)),
+    (13, 300, 1024, 16, 0, (16, 2, 4)),
+    (125, 390, 1024, 0, 0, (128, 2, 4)),
 ]
 
 
