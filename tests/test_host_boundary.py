@@ -410,10 +410,12 @@ def test_binding_quantisers_refuse_host_tensors(lib):
 
 def test_decode_kernel_plans(lib):
     """The decode kernel (M <= 2): at most 8 K steps per CTA, at most one CTA per SM
-    in all, the largest portable split that satisfies both; otherwise the two-term
-    kernel. Forced decode plans are validated against the shape."""
-    for (M, N, K, split) in [(1, 4096, 4096, 4), (2, 4096, 4096, 4), (1, 256, 256, 2), (1, 2048, 4096, 8),
-                             (1, 4096, 1024, 4), (2, 130, 640, 5), (1, 19 * 128, 8192, 8)]:
+    in all, the largest portable split that satisfies both and leaves each CTA at
+    least two K steps; otherwise the two-term kernel. Forced decode plans are
+    validated against the shape."""
+    for (M, N, K, split) in [(1, 4096, 4096, 4), (2, 4096, 4096, 4), (1, 256, 256, 1), (1, 2048, 4096, 8),
+                             (1, 4096, 1024, 4), (2, 130, 640, 2), (1, 19 * 128, 8192, 8), (1, 1024, 1024, 4),
+                             (1, 128, 128, 1), (1, 2048, 2048, 8)]:
         p = binding.plan_variant(M, N, K, 0, 0, 0, 152).as_dict()
         assert p["variant"] == binding.VARIANT_GEMV and p["split_k"] == split, (M, N, K, p)
         assert p["grid"][0] == -(-N // 128) * split <= 152 and p["cluster"][0] == split
